@@ -1,0 +1,124 @@
+"""The synthetic MoE-layer workloads: shapes, routing structure and input recipe.
+
+Sizes follow the layers named on the expert-parallelism pages (Mixtral 8x7B,
+DeepSeek-V3 routed experts, Switch-Base) plus a tiny all-float32 layer.  The
+recipe for every workload: x ~ N(0,1); router weight ~ N(0, 1/h); expert
+gate/up/down weights ~ N(0, 1/h); selection bias ~ U(-0.1, 0.1) where the
+layer uses one; seed 0.  "N" is the Irwin-Hall normal of :mod:`synth`.
+
+Layouts (row-major, the last index contiguous):
+  x [T, h]; router weight [E, h]; w13 [E, 2I, h] (gate rows 0..I-1 then up rows
+  I..2I-1 of each expert); w2 [E, h, I]; selection bias [E] float32; logit
+  offset [E] float32.
+"""
+from __future__ import annotations
+
+import dataclasses
+import math
+from typing import Optional, Tuple
+
+import numpy as np
+
+import synth
+
+
+@dataclasses.dataclass(frozen=True)
+class Workload:
+    name: str
+    T: int
+    h: int
+    E: int
+    K: int
+    I: int
+    dtype: str                  # "f32" | "bf16"
+    score: str                  # "softmax" | "sigmoid"
+    renormalize: int = 1
+    scale: float = 1.0
+    n_groups: int = 0
+    topk_groups: int = 0
+    group_topn: int = 0
+    capacity: int = 0           # <= 0: dropless
+    pad: int = 0
+    ep_size: int = 1
+    sel_bias: Optional[Tuple[float, float]] = None   # U(lo, hi) selection bias
+    zipf_s: Optional[float] = None                   # Zipf logit offsets
+    seed: int = 0
+
+    @property
+    def ds(self) -> int:
+        return 4 if self.dtype == "f32" else 2
+
+    def replace(self, **kw) -> "Workload":
+        return dataclasses.replace(self, **kw)
+
+    @property
+    def rows(self) -> int:
+        """Rows of the permuted buffer: T*K, or E*capacity when padded."""
+        return self.E * self.capacity if (self.pad and self.capacity > 0) else self.T * self.K
+
+
+def capacity_for(factor: float, T: int, K: int, E: int) -> int:
+    return int(math.ceil(factor * T * K / E))
+
+
+TINY = Workload("tiny_f32", T=256, h=256, E=8, K=2, I=512, dtype="f32", score="softmax",
+                capacity=capacity_for(1.25, 256, 2, 8), ep_size=4)
+MIXTRAL = Workload("mixtral_8x7b", T=4096, h=4096, E=8, K=2, I=14336, dtype="bf16",
+                   score="softmax", ep_size=4)
+DSV3 = Workload("deepseek_v3", T=4096, h=7168, E=256, K=8, I=2048, dtype="bf16",
+                score="sigmoid", scale=2.5, n_groups=8, topk_groups=4, group_topn=2,
+                ep_size=64, sel_bias=(-0.1, 0.1))
+SWITCH = Workload("switch_base", T=16384, h=768, E=128, K=1, I=3072, dtype="bf16",
+                  score="softmax", capacity=capacity_for(1.0, 16384, 1, 128), ep_size=16,
+                  zipf_s=1.1)
+DECODE = tuple(DSV3.replace(name=f"deepseek_v3_decode_T{t}", T=t) for t in (32, 256, 1024))
+
+ALL = {w.name: w for w in (TINY, MIXTRAL, DSV3, SWITCH) + DECODE}
+
+
+def sigma_in(w: Workload) -> float:
+    return 1.0 / math.sqrt(w.h)
+
+
+# ---------------------------------------------------------------- host side
+def host_x(w: Workload, rows=None) -> np.ndarray:
+    """x [T, h] (or the listed token rows), float32 or bf16 bits."""
+    if rows is None:
+        return synth.normal(w.seed, synth.TID_X, (w.T, w.h), 1.0, w.dtype)
+    rows = np.asarray(rows, dtype=np.int64)
+    idx = (rows[:, None] * w.h + np.arange(w.h)[None, :]).reshape(-1)
+    return synth.normal_at(w.seed, synth.TID_X, idx, 1.0, w.dtype).reshape(len(rows), w.h)
+
+
+def host_router_weight(w: Workload) -> np.ndarray:
+    return synth.normal(w.seed, synth.TID_WR, (w.E, w.h), sigma_in(w), w.dtype)
+
+
+def host_w13(w: Workload, e: int) -> np.ndarray:
+    """Expert e's gate/up weight [2I, h]."""
+    n = 2 * w.I * w.h
+    return synth.normal(w.seed, synth.TID_W13, (2 * w.I, w.h), sigma_in(w), w.dtype, start=e * n)
+
+
+def host_w2(w: Workload, e: int) -> np.ndarray:
+    """Expert e's down weight [h, I]."""
+    n = w.h * w.I
+    return synth.normal(w.seed, synth.TID_W2, (w.h, w.I), sigma_in(w), w.dtype, start=e * n)
+
+
+def host_sel_bias(w: Workload) -> Optional[np.ndarray]:
+    if w.sel_bias is None:
+        return None
+    return synth.uniform(w.seed, synth.TID_SEL_BIAS, w.E, w.sel_bias[0], w.sel_bias[1])
+
+
+_ZIPF_CACHE: dict = {}
+
+
+def host_logit_offset(w: Workload) -> Optional[np.ndarray]:
+    if w.zipf_s is None:
+        return None
+    key = (w.seed, w.E, w.zipf_s)
+    if key not in _ZIPF_CACHE:
+        _ZIPF_CACHE[key] = synth.zipf_logit_offsets(w.seed, w.E, w.zipf_s)
+    return _ZIPF_CACHE[key]
