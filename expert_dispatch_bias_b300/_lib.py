@@ -1,0 +1,208 @@
+"""ctypes binding of libmoe.so (the C ABI in include/moe.h).
+
+Argument marshalling only: every function below passes device pointers, sizes
+and the current CUDA stream to the C entry point of the same name and raises
+MoeError on a non-zero status.  No step of the layer runs here.  If the
+library is missing the import fails loudly; there is no fallback.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from ctypes import POINTER, c_float, c_int32, c_int64, c_size_t, c_void_p
+from typing import Optional
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libmoe.so")
+
+MOE_F32, MOE_BF16 = 0, 1
+MOE_SOFTMAX, MOE_SIGMOID = 0, 1
+MOE_OP_LAYOUT, MOE_OP_FFN, MOE_OP_LAYER, MOE_OP_LAYER_HOST = 0, 1, 2, 3
+
+STATUS = {
+    0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED", 3: "MOE_ERR_ALIGNMENT",
+    4: "MOE_ERR_WORKSPACE_TOO_SMALL", 5: "MOE_ERR_CUDA", 6: "MOE_ERR_DEVICE_TIMEOUT",
+    7: "MOE_ERR_DEVICE_BAD_INDEX",
+}
+
+# Every symbol the header declares (checked by the tests).
+EXPORTS = (
+    "moe_status_string", "moe_validate_config", "moe_rows", "moe_workspace_size", "moe_workspace_init",
+    "moe_router_logits", "moe_route", "moe_dispatch_layout", "moe_permute", "moe_grouped_ffn",
+    "moe_combine", "moe_layer_forward", "moe_layer_forward_host", "moe_check",
+)
+
+
+class MoeError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: {STATUS.get(status, status)}")
+
+
+class MoeConfig(ctypes.Structure):
+    _fields_ = [
+        ("T", c_int32), ("h", c_int32), ("E", c_int32), ("K", c_int32), ("I", c_int32),
+        ("dtype", c_int32), ("score", c_int32), ("renormalize", c_int32), ("scale", c_float),
+        ("n_groups", c_int32), ("topk_groups", c_int32), ("group_topn", c_int32),
+        ("capacity", c_int32), ("pad", c_int32), ("ep_size", c_int32),
+    ]
+
+
+class MoeLayoutStats(ctypes.Structure):
+    _fields_ = [("kept_total", c_int64), ("dropped", c_int64), ("offdiag_rows", c_int64),
+                ("experts_touched", c_int32), ("balancedness", c_float)]
+
+
+class MoeLayerOut(ctypes.Structure):
+    _fields_ = [(n, c_void_p) for n in ("logits", "topk_ids", "topk_w", "counts", "kept", "offsets", "slot",
+                                         "row_src", "n_ij", "rank_bytes", "stats")]
+
+
+def _load() -> ctypes.CDLL:
+    if not os.path.exists(LIB_PATH):
+        raise ImportError(f"{LIB_PATH} is missing: build it with `python -m expert_dispatch_bias_b300.build`")
+    lib = ctypes.CDLL(LIB_PATH)
+    cfgp = POINTER(MoeConfig)
+    sig = {
+        "moe_status_string": (ctypes.c_char_p, [c_int32]),
+        "moe_validate_config": (c_int32, [cfgp]),
+        "moe_rows": (c_int32, [cfgp, POINTER(c_int64)]),
+        "moe_workspace_size": (c_int32, [cfgp, c_int32, POINTER(c_size_t)]),
+        "moe_workspace_init": (c_int32, [c_void_p, c_size_t, c_void_p]),
+        "moe_router_logits": (c_int32, [cfgp, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p]),
+        "moe_route": (c_int32, [cfgp, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p]),
+        "moe_dispatch_layout": (c_int32, [cfgp] + [c_void_p] * 10 + [c_size_t, c_void_p]),
+        "moe_permute": (c_int32, [cfgp, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p]),
+        "moe_grouped_ffn": (c_int32, [cfgp] + [c_void_p] * 7 + [c_size_t, c_void_p]),
+        "moe_combine": (c_int32, [cfgp, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p]),
+        "moe_layer_forward": (c_int32, [cfgp] + [c_void_p] * 9 + [c_size_t, c_void_p]),
+        "moe_layer_forward_host": (c_int32, [cfgp] + [c_void_p] * 8 + [c_size_t, c_void_p]),
+        "moe_check": (c_int32, [c_void_p]),
+    }
+    for name, (res, args) in sig.items():
+        fn = getattr(lib, name)
+        fn.restype = res
+        fn.argtypes = args
+    return lib
+
+
+lib = _load()
+
+
+# ------------------------------------------------------------------ marshalling helpers
+def _ptr(t) -> Optional[int]:
+    if t is None:
+        return None
+    if isinstance(t, int):
+        return t
+    return t.data_ptr()
+
+
+def _stream(stream) -> Optional[int]:
+    if stream is None:
+        import torch
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def _check(status: int, where: str) -> None:
+    if status != 0:
+        raise MoeError(status, where)
+
+
+def make_config(T, h, E, K, I, dtype="bf16", score="softmax", renormalize=1, scale=1.0, n_groups=0,
+                topk_groups=0, group_topn=0, capacity=0, pad=0, ep_size=1) -> MoeConfig:
+    return MoeConfig(T, h, E, K, I, MOE_F32 if dtype in ("f32", MOE_F32) else MOE_BF16,
+                     MOE_SIGMOID if score in ("sigmoid", MOE_SIGMOID) else MOE_SOFTMAX,
+                     int(renormalize), float(scale), n_groups, topk_groups, group_topn, capacity, pad, ep_size)
+
+
+def config_from(w) -> MoeConfig:
+    """MoeConfig from any object with the layer's attributes (e.g. a synth Workload)."""
+    return make_config(w.T, w.h, w.E, w.K, w.I, w.dtype, w.score, w.renormalize, w.scale, w.n_groups,
+                       w.topk_groups, w.group_topn, w.capacity, w.pad, w.ep_size)
+
+
+# ------------------------------------------------------------------ the C entry points
+def moe_validate_config(cfg: MoeConfig) -> int:
+    return lib.moe_validate_config(ctypes.byref(cfg))
+
+
+def moe_rows(cfg: MoeConfig) -> int:
+    r = c_int64()
+    _check(lib.moe_rows(ctypes.byref(cfg), ctypes.byref(r)), "moe_rows")
+    return r.value
+
+
+def moe_workspace_size(cfg: MoeConfig, op: int) -> int:
+    n = c_size_t()
+    _check(lib.moe_workspace_size(ctypes.byref(cfg), op, ctypes.byref(n)), "moe_workspace_size")
+    return n.value
+
+
+def moe_workspace_init(ws, stream=None) -> None:
+    _check(lib.moe_workspace_init(_ptr(ws), ws.numel() * ws.element_size(), _stream(stream)), "moe_workspace_init")
+
+
+def moe_router_logits(cfg, x, w_r, logit_offset, logits, stream=None) -> None:
+    _check(lib.moe_router_logits(ctypes.byref(cfg), _ptr(x), _ptr(w_r), _ptr(logit_offset), _ptr(logits),
+                                 _stream(stream)), "moe_router_logits")
+
+
+def moe_route(cfg, logits, sel_bias, topk_ids, topk_w, stream=None) -> None:
+    _check(lib.moe_route(ctypes.byref(cfg), _ptr(logits), _ptr(sel_bias), _ptr(topk_ids), _ptr(topk_w),
+                         _stream(stream)), "moe_route")
+
+
+def moe_dispatch_layout(cfg, topk_ids, counts, kept, offsets, slot, row_src, n_ij, rank_bytes, stats, workspace,
+                        stream=None) -> None:
+    _check(lib.moe_dispatch_layout(ctypes.byref(cfg), _ptr(topk_ids), _ptr(counts), _ptr(kept), _ptr(offsets),
+                                   _ptr(slot), _ptr(row_src), _ptr(n_ij), _ptr(rank_bytes), _ptr(stats),
+                                   _ptr(workspace), workspace.numel() * workspace.element_size(),
+                                   _stream(stream)), "moe_dispatch_layout")
+
+
+def moe_permute(cfg, x, slot, row_src, xp, stream=None) -> None:
+    _check(lib.moe_permute(ctypes.byref(cfg), _ptr(x), _ptr(slot), _ptr(row_src), _ptr(xp), _stream(stream)),
+           "moe_permute")
+
+
+def moe_grouped_ffn(cfg, xp, offsets, kept, w13, w2, yp, workspace, stream=None) -> None:
+    _check(lib.moe_grouped_ffn(ctypes.byref(cfg), _ptr(xp), _ptr(offsets), _ptr(kept), _ptr(w13), _ptr(w2),
+                               _ptr(yp), _ptr(workspace), workspace.numel() * workspace.element_size(),
+                               _stream(stream)), "moe_grouped_ffn")
+
+
+def moe_combine(cfg, yp, slot, topk_w, y, stream=None) -> None:
+    _check(lib.moe_combine(ctypes.byref(cfg), _ptr(yp), _ptr(slot), _ptr(topk_w), _ptr(y), _stream(stream)),
+           "moe_combine")
+
+
+def moe_layer_forward(cfg, x, w_r, logit_offset, sel_bias, w13, w2, y, out: Optional[MoeLayerOut], workspace,
+                      stream=None) -> None:
+    _check(lib.moe_layer_forward(ctypes.byref(cfg), _ptr(x), _ptr(w_r), _ptr(logit_offset), _ptr(sel_bias),
+                                 _ptr(w13), _ptr(w2), _ptr(y), ctypes.byref(out) if out is not None else None,
+                                 _ptr(workspace), workspace.numel() * workspace.element_size(), _stream(stream)),
+           "moe_layer_forward")
+
+
+def moe_layer_forward_host(cfg, x_host, w_r, logit_offset, sel_bias, w13, w2, y_host, workspace,
+                           stream=None) -> None:
+    _check(lib.moe_layer_forward_host(ctypes.byref(cfg), _ptr(x_host), _ptr(w_r), _ptr(logit_offset),
+                                      _ptr(sel_bias), _ptr(w13), _ptr(w2), _ptr(y_host), _ptr(workspace),
+                                      workspace.numel() * workspace.element_size(), _stream(stream)),
+           "moe_layer_forward_host")
+
+
+def moe_check(stream=None) -> int:
+    """Synchronises the stream; returns the status (does not raise)."""
+    return lib.moe_check(_stream(stream))
+
+
+def layer_out(**tensors) -> MoeLayerOut:
+    o = MoeLayerOut()
+    for k, v in tensors.items():
+        setattr(o, k, _ptr(v))
+    return o

@@ -1,0 +1,359 @@
+// Grouped SwiGLU FFN on the 5th-generation tensor cores (tcgen05, sm_103a).
+//
+// One persistent CTA per SM walks a static round-robin list of output tiles
+// over the ragged expert segments.  A tile is 128 rows of one expert's segment
+// by 256 accumulator columns:
+//   gate/up GEMM: columns 0..127 hold gate units n0..n0+127 and columns
+//     128..255 the matching up units, so the epilogue forms silu(g) * u for
+//     128 intermediate units without leaving the tile;
+//   down GEMM: 256 output columns.
+// Roles (192 threads):
+//   warp 0       one thread issues TMA loads (A rows of the segment, B rows of
+//                the expert's weight) into a 4-stage shared-memory ring;
+//   warp 1       allocates 512 TMEM columns (two 256-column accumulators) and
+//                one thread issues tcgen05.mma (M=128, N=256, K=16, bf16 in,
+//                f32 accumulate), releasing ring stages with tcgen05.commit;
+//   warps 2..5   the epilogue: tcgen05.ld of the accumulator (warp w reads TMEM
+//                lanes 32*(w%4)..+31 = tile rows), SwiGLU or plain, bf16 stores
+//                of the rows inside the segment, then the accumulator is
+//                released for the tile after next.
+// Rows past a segment's end are computed (they belong to the next segment or
+// are zero-filled by TMA past the buffer) and masked on store.  Every wait is
+// bounded; a wait that runs out raises the sticky error and the CTA drains
+// and exits.
+#pragma once
+
+#include <cuda.h>
+
+#include "common.cuh"
+
+namespace moe {
+
+constexpr int kTcBM = 128, kTcBN = 256, kTcBK = 64, kTcStages = 4, kTcThreads = 192;
+constexpr uint32_t kTcABytes = kTcBM * kTcBK * 2;   // 16 KB
+constexpr uint32_t kTcBBytes = kTcBN * kTcBK * 2;   // 32 KB
+constexpr uint32_t kTcStageBytes = kTcABytes + kTcBBytes;
+constexpr size_t kTcDynSmem = (size_t)kTcStages * kTcStageBytes + 1024;  // + alignment slack
+constexpr uint32_t kTcTmemCols = 512;
+
+enum TcEpilogue { kTcSwiglu = 0, kTcStore = 1 };
+
+struct TcParams {
+  const int32_t* offsets;   // [E+1]
+  const int32_t* kept;      // [E]
+  int E;
+  int n_tiles;              // column tiles per expert
+  int k_blocks;             // K / 64
+  int64_t b_rows;           // weight rows per expert (2I or h)
+  int up_rows;              // I (gate/up only)
+  int n_valid;              // output columns per expert (I or h)
+  __nv_bfloat16* out;       // [R, ldo]
+  int64_t ldo;
+};
+
+// ------------------------------------------------------------------ PTX wrappers
+__device__ __forceinline__ void tma_load_2d(void* smem_dst, const CUtensorMap* map, int x, int y, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], "
+      "[%4];" ::"r"(smem_u32(smem_dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_u32(bar))
+      : "memory");
+}
+
+// Shared-memory matrix descriptor: K-major operand, 128-byte swizzle, rows of
+// 128 bytes in 8-row (1024-byte) atoms.
+__device__ __forceinline__ uint64_t umma_desc_sw128(uint32_t saddr) {
+  uint64_t d = 0;
+  d |= (uint64_t)((saddr >> 4) & 0x3FFFu);        // start address
+  d |= (uint64_t)1u << 16;                        // leading byte offset (unused when swizzled)
+  d |= (uint64_t)(1024u >> 4) << 32;              // stride byte offset: 8 rows x 128 B
+  d |= (uint64_t)1u << 46;                        // descriptor version
+  d |= (uint64_t)2u << 61;                        // 128-byte swizzle
+  return d;
+}
+
+// Instruction descriptor: kind::f16, A = B = bf16, D = f32, both K-major.
+__host__ __device__ constexpr uint32_t umma_idesc_bf16(int M, int N) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
+
+__device__ __forceinline__ void umma_bf16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                          uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+__device__ __forceinline__ void umma_commit(uint64_t* bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
+               : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+
+// 32 lanes x 32 consecutive 32-bit columns: thread i gets row (lane base + i).
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t* r) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
+      "%15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
+        "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
+        "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr)
+      : "memory");
+}
+
+__device__ __forceinline__ void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+
+// ------------------------------------------------------------------ tile schedule
+struct TcTile {
+  int e;        // expert
+  int m0;       // first row (absolute, in the permuted buffer)
+  int m_end;    // end of the expert's segment
+  int nt;       // column tile
+};
+
+// mbp[e] = m-blocks of experts < e (exclusive prefix), mbp[E] = total.
+__device__ __forceinline__ TcTile tc_decode(int t, const int32_t* mbp, int E, int n_tiles, const int32_t* offsets,
+                                            const int32_t* kept) {
+  int lo = 0, hi = E - 1;  // last expert whose first tile index is <= t
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (mbp[mid] * n_tiles <= t) lo = mid; else hi = mid - 1;
+  }
+  const int e = lo;
+  const int local = t - mbp[e] * n_tiles;
+  const int cnt = mbp[e + 1] - mbp[e];
+  TcTile r;
+  r.e = e;
+  r.nt = local / cnt;
+  const int mb = local - r.nt * cnt;
+  r.m0 = offsets[e] + mb * kTcBM;
+  r.m_end = offsets[e] + kept[e];
+  return r;
+}
+
+template <int EPI>
+__global__ void __launch_bounds__(kTcThreads, 1)
+    ffn_tc_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_b, TcParams p) {
+  extern __shared__ uint8_t dyn_smem[];
+  __shared__ __align__(8) uint64_t full_bar[kTcStages], empty_bar[kTcStages];
+  __shared__ __align__(8) uint64_t tmem_full[2], tmem_empty[2], drain_bar;
+  __shared__ uint32_t tmem_holder;
+  __shared__ volatile uint32_t abort_flag;
+  __shared__ int32_t mbp[1025];
+  __shared__ int32_t scan_scratch[33];
+
+  uint8_t* tiles = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(dyn_smem) + 1023) & ~uintptr_t(1023));
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+
+  // ---- per-expert m-block prefix (every CTA computes it from offsets/kept)
+  for (int e = tid; e < p.E; e += kTcThreads) mbp[e] = (p.kept[e] + kTcBM - 1) / kTcBM;
+  __syncthreads();
+  const int32_t total_mb = block_exclusive_scan(mbp, p.E, scan_scratch);
+  if (tid == 0) mbp[p.E] = total_mb;
+  const int total_tiles = total_mb * p.n_tiles;
+
+  if (tid == 0) {
+    for (int s = 0; s < kTcStages; ++s) {
+      mbar_init(&full_bar[s], 1);
+      mbar_init(&empty_bar[s], 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(&tmem_full[a], 1);
+      mbar_init(&tmem_empty[a], 128);
+    }
+    mbar_init(&drain_bar, 1);
+    abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(&tmem_holder)),
+                 "r"(kTcTmemCols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = tmem_holder;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      uint32_t armed = 0;  // bit s: stage s was ever armed; its last arm had parity (phase bit at the time)
+      uint32_t armed_parity = 0;
+      for (int t = blockIdx.x; t < total_tiles && !abort_flag; t += gridDim.x) {
+        const TcTile tl = tc_decode(t, mbp, p.E, p.n_tiles, p.offsets, p.kept);
+        const int64_t brow = (int64_t)tl.e * p.b_rows;
+        for (int kb = 0; kb < p.k_blocks; ++kb) {
+          if (!mbar_wait(&empty_bar[stage], phase ^ 1u, &abort_flag)) {
+            abort_flag = 1;
+            raise_error(kErrTimeout);
+            break;
+          }
+          uint8_t* sa = tiles + (size_t)stage * kTcStageBytes;
+          uint8_t* sb = sa + kTcABytes;
+          mbar_expect_tx(&full_bar[stage], kTcStageBytes);
+          const int kx = kb * kTcBK;
+          tma_load_2d(sa, &map_a, kx, tl.m0, &full_bar[stage]);
+          if (EPI == kTcSwiglu) {
+            const int n0 = tl.nt * (kTcBN / 2);
+            tma_load_2d(sb, &map_b, kx, (int)(brow + n0), &full_bar[stage]);
+            tma_load_2d(sb + kTcBBytes / 2, &map_b, kx, (int)(brow + p.up_rows + n0), &full_bar[stage]);
+          } else {
+            const int n0 = tl.nt * kTcBN;
+            tma_load_2d(sb, &map_b, kx, (int)(brow + n0), &full_bar[stage]);
+          }
+          armed |= 1u << stage;
+          armed_parity = (armed_parity & ~(1u << stage)) | (phase << stage);
+          if (++stage == kTcStages) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+      if (abort_flag) {
+        // let the last load armed on every stage land before the CTA's shared
+        // memory is released (bounded like every other wait)
+        for (int s = 0; s < kTcStages; ++s)
+          if ((armed >> s) & 1u) mbar_wait(&full_bar[s], (armed_parity >> s) & 1u);
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t idesc = umma_idesc_bf16(kTcBM, kTcBN);
+      int stage = 0;
+      uint32_t phase = 0;
+      int acc = 0;
+      uint32_t acc_phase = 0;
+      for (int t = blockIdx.x; t < total_tiles && !abort_flag; t += gridDim.x) {
+        if (!mbar_wait(&tmem_empty[acc], acc_phase ^ 1u, &abort_flag)) {
+          abort_flag = 1;
+          raise_error(kErrTimeout);
+          break;
+        }
+        tc_fence_after();
+        const uint32_t d_tmem = tmem_base + (uint32_t)(acc * kTcBN);
+        bool ok = true;
+        for (int kb = 0; kb < p.k_blocks; ++kb) {
+          if (!mbar_wait(&full_bar[stage], phase, &abort_flag)) {
+            abort_flag = 1;
+            raise_error(kErrTimeout);
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t sa = smem_u32(tiles + (size_t)stage * kTcStageBytes);
+          const uint32_t sb = sa + kTcABytes;
+#pragma unroll
+          for (int k = 0; k < kTcBK / 16; ++k) {
+            umma_bf16(d_tmem, umma_desc_sw128(sa + k * 32), umma_desc_sw128(sb + k * 32), idesc,
+                      (kb | k) != 0 ? 1u : 0u);
+          }
+          umma_commit(&empty_bar[stage]);
+          if (++stage == kTcStages) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+        if (!ok) break;
+        umma_commit(&tmem_full[acc]);
+        if (++acc == 2) {
+          acc = 0;
+          acc_phase ^= 1u;
+        }
+      }
+      // all MMAs issued by this thread are complete once drain_bar fires
+      umma_commit(&drain_bar);
+      mbar_wait(&drain_bar, 0u);
+    }
+  } else {
+    // ------------------------------------------------------------ epilogue (warps 2..5)
+    const int quarter = warp & 3;
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    for (int t = blockIdx.x; t < total_tiles; t += gridDim.x) {
+      if (!mbar_wait(&tmem_full[acc], acc_phase, &abort_flag)) {
+        abort_flag = 1;
+        raise_error(kErrTimeout);
+        break;
+      }
+      tc_fence_after();
+      const TcTile tl = tc_decode(t, mbp, p.E, p.n_tiles, p.offsets, p.kept);
+      const int row = tl.m0 + quarter * 32 + lane;
+      const bool valid = row < tl.m_end;
+      const uint32_t taddr = tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(acc * kTcBN);
+      __nv_bfloat16* orow = p.out + (int64_t)row * p.ldo;
+      if (EPI == kTcSwiglu) {
+        const int n0 = tl.nt * (kTcBN / 2);
+#pragma unroll 1
+        for (int c = 0; c < kTcBN / 2; c += 32) {
+          uint32_t g[32], u[32];
+          tmem_ld32(taddr + c, g);
+          tmem_ld32(taddr + kTcBN / 2 + c, u);
+          tmem_ld_wait();
+          if (valid && n0 + c + 32 <= p.n_valid) {
+            uint32_t packed[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+              const float g0 = __uint_as_float(g[2 * i]), g1 = __uint_as_float(g[2 * i + 1]);
+              const float a0 = g0 / (1.0f + expf(-g0)) * __uint_as_float(u[2 * i]);
+              const float a1 = g1 / (1.0f + expf(-g1)) * __uint_as_float(u[2 * i + 1]);
+              const __nv_bfloat162 v = __floats2bfloat162_rn(a0, a1);
+              packed[i] = *reinterpret_cast<const uint32_t*>(&v);
+            }
+            uint4* dst = reinterpret_cast<uint4*>(orow + n0 + c);
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+              dst[i] = make_uint4(packed[4 * i], packed[4 * i + 1], packed[4 * i + 2], packed[4 * i + 3]);
+          }
+        }
+      } else {
+        const int n0 = tl.nt * kTcBN;
+#pragma unroll 1
+        for (int c = 0; c < kTcBN; c += 32) {
+          uint32_t v[32];
+          tmem_ld32(taddr + c, v);
+          tmem_ld_wait();
+          if (valid && n0 + c + 32 <= p.n_valid) {
+            uint32_t packed[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+              const __nv_bfloat162 b = __floats2bfloat162_rn(__uint_as_float(v[2 * i]), __uint_as_float(v[2 * i + 1]));
+              packed[i] = *reinterpret_cast<const uint32_t*>(&b);
+            }
+            uint4* dst = reinterpret_cast<uint4*>(orow + n0 + c);
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+              dst[i] = make_uint4(packed[4 * i], packed[4 * i + 1], packed[4 * i + 2], packed[4 * i + 3]);
+          }
+        }
+      }
+      tc_fence_before();
+      mbar_arrive(&tmem_empty[acc]);
+      if (++acc == 2) {
+        acc = 0;
+        acc_phase ^= 1u;
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base), "r"(kTcTmemCols)
+                 : "memory");
+  }
+}
+
+}  // namespace moe

@@ -1,0 +1,658 @@
+// C ABI of the MoE-layer forward pass (declared in include/moe.h).
+//
+// One translation unit holds every kernel (the headers included below) so that
+// the sticky device error word is a single symbol.  Host code here validates
+// arguments, carves the caller's workspace, picks launch shapes and enqueues
+// kernels on the caller's stream; it never allocates device memory and never
+// synchronises except in moe_check.
+#include <math.h>
+#include <stdint.h>
+#include <string.h>
+
+#include <cudaTypedefs.h>
+
+#include "moe.h"
+#include "common.cuh"
+#include "ffn_tc.cuh"
+#include "layout.cuh"
+#include "permute_combine.cuh"
+#include "route.cuh"
+#include "simt_gemm.cuh"
+
+using namespace moe;
+
+namespace {
+
+#define MOE_TRY(expr)                    \
+  do {                                   \
+    const moe_status st_ = (expr);       \
+    if (st_ != MOE_OK) return st_;       \
+  } while (0)
+
+#define CUDA_TRY(expr)                               \
+  do {                                               \
+    if ((expr) != cudaSuccess) {                     \
+      (void)cudaGetLastError();                      \
+      return MOE_ERR_CUDA;                           \
+    }                                                \
+  } while (0)
+
+inline bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+inline int ds_of(const moe_config& c) { return c.dtype == MOE_F32 ? 4 : 2; }
+inline int64_t rows_of(const moe_config& c) {
+  return (c.pad && c.capacity > 0) ? (int64_t)c.E * c.capacity : (int64_t)c.T * c.K;
+}
+inline cudaStream_t as_stream(void* s) { return static_cast<cudaStream_t>(s); }
+
+moe_status validate(const moe_config* c) {
+  if (c == nullptr) return MOE_ERR_INVALID_ARG;
+  if (c->T < 0 || c->h <= 0 || c->h % 64 != 0 || c->I <= 0 || c->I % 64 != 0) return MOE_ERR_INVALID_ARG;
+  if (c->E < 1 || c->E > 1024 || c->K < 1 || c->K > 16 || c->K > c->E) return MOE_ERR_INVALID_ARG;
+  if (c->dtype != MOE_F32 && c->dtype != MOE_BF16) return MOE_ERR_INVALID_ARG;
+  if (c->score != MOE_SOFTMAX && c->score != MOE_SIGMOID) return MOE_ERR_INVALID_ARG;
+  if (c->renormalize != 0 && c->renormalize != 1) return MOE_ERR_INVALID_ARG;
+  if (!isfinite(c->scale)) return MOE_ERR_INVALID_ARG;
+  if (c->n_groups < 0) return MOE_ERR_INVALID_ARG;
+  if (c->n_groups > 0) {
+    if (c->n_groups > 32 || c->E % c->n_groups != 0) return MOE_ERR_INVALID_ARG;
+    const int gs = c->E / c->n_groups;
+    if (c->topk_groups < 1 || c->topk_groups > c->n_groups) return MOE_ERR_INVALID_ARG;
+    if (c->group_topn < 1 || c->group_topn > gs) return MOE_ERR_INVALID_ARG;
+    if (c->group_topn > kMaxGroupTopn) return MOE_ERR_UNSUPPORTED;
+    if ((int64_t)c->topk_groups * gs < c->K) return MOE_ERR_INVALID_ARG;
+  }
+  if (c->capacity < 0 || (c->pad != 0 && c->pad != 1)) return MOE_ERR_INVALID_ARG;
+  if (c->pad && c->capacity == 0) return MOE_ERR_INVALID_ARG;
+  if (c->ep_size < 1 || c->E % c->ep_size != 0) return MOE_ERR_INVALID_ARG;
+  if ((int64_t)c->T * c->K >= INT32_MAX || rows_of(*c) >= INT32_MAX) return MOE_ERR_INVALID_ARG;
+  // one permuted row must fit a shared-memory buffer of the bulk-copy permute
+  if ((int64_t)c->h * ds_of(*c) > 200 * 1024) return MOE_ERR_UNSUPPORTED;
+  return MOE_OK;
+}
+
+moe_status check_dtype_ptr(const void* p) {
+  if (p == nullptr) return MOE_ERR_INVALID_ARG;
+  return aligned(p, 16) ? MOE_OK : MOE_ERR_ALIGNMENT;
+}
+moe_status check_ptr(const void* p, size_t a) {
+  if (p == nullptr) return MOE_ERR_INVALID_ARG;
+  return aligned(p, a) ? MOE_OK : MOE_ERR_ALIGNMENT;
+}
+moe_status check_opt_ptr(const void* p, size_t a) { return (p == nullptr || aligned(p, a)) ? MOE_OK : MOE_ERR_ALIGNMENT; }
+
+struct DeviceInfo {
+  int sms = 0;
+};
+DeviceInfo device_info() {
+  static DeviceInfo cache[64];
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev < 0 || dev >= 64) dev = 0;
+  if (cache[dev].sms == 0) cudaDeviceGetAttribute(&cache[dev].sms, cudaDevAttrMultiProcessorCount, dev);
+  return cache[dev];
+}
+
+template <typename K>
+cudaError_t allow_smem(K kernel, size_t bytes) {
+  if (bytes <= 48 * 1024) return cudaSuccess;
+  return cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+}
+
+// ------------------------------------------------------------------ workspace carving
+struct Carver {
+  char* base;
+  size_t off = 0;
+  explicit Carver(void* b) : base(static_cast<char*>(b)) {}
+  template <typename T>
+  T* take(size_t count) {
+    T* p = base ? reinterpret_cast<T*>(base + off) : nullptr;
+    off += align_up(count * sizeof(T) + 0, 256);
+    return p;
+  }
+};
+
+struct LayerBuffers {
+  void* layout_ws;
+  size_t layout_ws_bytes;
+  float* logits;
+  int32_t* ids;
+  float* w;
+  int32_t* counts;
+  int32_t* kept;
+  int32_t* offsets;
+  int32_t* slot;
+  int32_t* row_src;
+  int64_t* n_ij;
+  int64_t* rank_bytes;
+  moe_layout_stats* stats;
+  void* xp;
+  void* yp;
+  void* inter;
+  void* xdev;
+  void* ydev;
+  size_t total;
+};
+
+LayerBuffers carve_layer(const moe_config& c, void* ws, bool host_io) {
+  Carver cv(ws);
+  LayerBuffers b;
+  const int64_t A = (int64_t)c.T * c.K, R = rows_of(c);
+  const int N = c.ep_size, ds = ds_of(c);
+  b.layout_ws_bytes = layout_scratch_bytes(A, c.E);
+  b.layout_ws = cv.take<char>(b.layout_ws_bytes);
+  b.logits = cv.take<float>((size_t)c.T * c.E);
+  b.ids = cv.take<int32_t>(A);
+  b.w = cv.take<float>(A);
+  b.counts = cv.take<int32_t>(c.E);
+  b.kept = cv.take<int32_t>(c.E);
+  b.offsets = cv.take<int32_t>(c.E + 1);
+  b.slot = cv.take<int32_t>(A);
+  b.row_src = cv.take<int32_t>(R);
+  b.n_ij = cv.take<int64_t>((size_t)N * N);
+  b.rank_bytes = cv.take<int64_t>(2 * (size_t)N);
+  b.stats = cv.take<moe_layout_stats>(1);
+  b.xp = cv.take<char>((size_t)R * c.h * ds);
+  b.yp = cv.take<char>((size_t)R * c.h * ds);
+  b.inter = cv.take<char>((size_t)R * c.I * ds);
+  b.xdev = host_io ? cv.take<char>((size_t)c.T * c.h * ds) : nullptr;
+  b.ydev = host_io ? cv.take<char>((size_t)c.T * c.h * ds) : nullptr;
+  b.total = cv.off;
+  return b;
+}
+
+size_t ffn_ws_bytes(const moe_config& c) { return align_up((size_t)rows_of(c) * c.I * ds_of(c), 256) + 256; }
+
+// ------------------------------------------------------------------ launchers
+moe_status launch_logits(const moe_config& c, const void* x, const void* w_r, const float* off, float* logits,
+                         cudaStream_t st) {
+  if (c.T == 0) return MOE_OK;
+  SimtParams p{};
+  p.A = x;
+  p.lda = c.h;
+  p.B = w_r;
+  p.ldb = c.h;
+  p.b_expert_rows = c.E;
+  p.C = logits;
+  p.ldc = c.E;
+  p.M = c.T;
+  p.N = c.E;
+  p.K = c.h;
+  p.col_bias = off;
+  dim3 grid((c.E + kSimtBN - 1) / kSimtBN, (c.T + kSimtBM - 1) / kSimtBM);
+  if (c.dtype == MOE_F32)
+    simt_gemm_kernel<float, kSimtLogits><<<grid, kSimtThreads, 0, st>>>(p);
+  else
+    simt_gemm_kernel<__nv_bfloat16, kSimtLogits><<<grid, kSimtThreads, 0, st>>>(p);
+  CUDA_TRY(cudaGetLastError());
+  return MOE_OK;
+}
+
+template <int PER>
+cudaError_t launch_route_per(const RouteParams& p, cudaStream_t st) {
+  const int blocks = (p.T + kRouteWarps - 1) / kRouteWarps;
+  const size_t smem = p.n_groups > 0 ? (size_t)kRouteWarps * p.E * sizeof(float) : 0;
+  route_kernel<PER><<<blocks, kRouteWarps * 32, smem, st>>>(p);
+  return cudaGetLastError();
+}
+
+moe_status launch_route(const moe_config& c, const float* logits, const float* bias, int32_t* ids, float* w,
+                        cudaStream_t st) {
+  if (c.T == 0) return MOE_OK;
+  RouteParams p{};
+  p.logits = logits;
+  p.bias = bias;
+  p.ids = ids;
+  p.w = w;
+  p.T = c.T;
+  p.E = c.E;
+  p.K = c.K;
+  p.sigmoid = c.score == MOE_SIGMOID;
+  p.renorm = c.renormalize;
+  p.scale = c.scale;
+  p.n_groups = c.n_groups;
+  p.topk_groups = c.topk_groups;
+  p.group_topn = c.group_topn;
+  p.key_is_logit = (c.score == MOE_SOFTMAX && bias == nullptr && c.n_groups == 0) ? 1 : 0;
+  const int per = (c.E + 31) / 32;
+  cudaError_t e;
+  if (per <= 1) e = launch_route_per<1>(p, st);
+  else if (per <= 2) e = launch_route_per<2>(p, st);
+  else if (per <= 4) e = launch_route_per<4>(p, st);
+  else if (per <= 8) e = launch_route_per<8>(p, st);
+  else if (per <= 16) e = launch_route_per<16>(p, st);
+  else e = launch_route_per<32>(p, st);
+  CUDA_TRY(e);
+  return MOE_OK;
+}
+
+moe_status launch_layout(const moe_config& c, const int32_t* ids, int32_t* counts, int32_t* kept,
+                         int32_t* offsets, int32_t* slot, int32_t* row_src, int64_t* n_ij, int64_t* rank_bytes,
+                         moe_layout_stats* stats, void* ws, cudaStream_t st) {
+  LayoutParams p{};
+  p.ids = ids;
+  p.A = (int64_t)c.T * c.K;
+  p.T = c.T;
+  p.K = c.K;
+  p.E = c.E;
+  p.cap = c.capacity;
+  p.pad = c.pad;
+  p.n_ep = c.ep_size;
+  p.ds = ds_of(c);
+  p.h = c.h;
+  p.R = (int)rows_of(c);
+  p.num_tiles = layout_num_tiles(p.A);
+  p.counts = counts;
+  p.kept = kept;
+  p.offsets = offsets;
+  p.slot = slot;
+  p.row_src = row_src;
+  p.n_ij = n_ij;
+  p.rank_bytes = rank_bytes;
+  p.stats = stats;
+  p.ws = layout_scratch_at(ws, p.A, c.E);
+  const size_t smem1 = (size_t)(kLayoutWarps + 2) * c.E * sizeof(int32_t);
+  CUDA_TRY(allow_smem(layout_rank_kernel, smem1));
+  layout_rank_kernel<<<p.num_tiles, kLayoutThreads, smem1, st>>>(p);
+  CUDA_TRY(cudaGetLastError());
+  const int64_t per_block = kFinalizeThreads * kFinalizeItems;
+  const int blocks2 = (int)((p.A + per_block - 1) / per_block) > 0 ? (int)((p.A + per_block - 1) / per_block) : 1;
+  layout_finalize_kernel<<<blocks2, kFinalizeThreads, (c.E + 1) * sizeof(int32_t), st>>>(p);
+  CUDA_TRY(cudaGetLastError());
+  return MOE_OK;
+}
+
+moe_status launch_permute(const moe_config& c, const void* x, const int32_t* slot, const int32_t* row_src,
+                          void* xp, cudaStream_t st) {
+  const uint32_t row_bytes = (uint32_t)c.h * ds_of(c);
+  if (c.pad && c.capacity > 0) {
+    const int64_t R = rows_of(c);
+    const uint32_t vecs = row_bytes / 16;
+    const int64_t n = R * vecs;
+    const int blocks = (int)((n + 255) / 256 < 148 * 8 ? (n + 255) / 256 : 148 * 8);
+    if (n > 0) {
+      zero_pad_rows_kernel<<<blocks, 256, 0, st>>>(row_src, R, vecs, static_cast<uint4*>(xp));
+      CUDA_TRY(cudaGetLastError());
+    }
+  }
+  if (c.T == 0) return MOE_OK;
+  PermuteParams p{};
+  p.x = static_cast<const uint8_t*>(x);
+  p.slot = slot;
+  p.xp = static_cast<uint8_t*>(xp);
+  p.T = c.T;
+  p.K = c.K;
+  p.row_bytes = row_bytes;
+  int nbuf = (int)((160 * 1024) / row_bytes);
+  p.nbuf = nbuf < 1 ? 1 : (nbuf > kPermBufs ? kPermBufs : nbuf);
+  const size_t smem = (size_t)p.nbuf * row_bytes;
+  CUDA_TRY(allow_smem(permute_bulk_kernel, smem));
+  int per_sm = 0;
+  CUDA_TRY(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, permute_bulk_kernel, 32, smem));
+  if (per_sm < 1) per_sm = 1;
+  int64_t blocks = (int64_t)device_info().sms * per_sm;
+  if (blocks > c.T) blocks = c.T;
+  permute_bulk_kernel<<<(unsigned)blocks, 32, smem, st>>>(p);
+  CUDA_TRY(cudaGetLastError());
+  return MOE_OK;
+}
+
+moe_status launch_combine(const moe_config& c, const void* yp, const int32_t* slot, const float* w, void* y,
+                          cudaStream_t st) {
+  if (c.T == 0) return MOE_OK;
+  CombineParams p{};
+  p.yp = yp;
+  p.slot = slot;
+  p.w = w;
+  p.y = y;
+  p.T = c.T;
+  p.K = c.K;
+  p.h = c.h;
+  const int warps_per_block = 8;
+  int64_t blocks = (c.T + warps_per_block - 1) / warps_per_block;
+  const int64_t cap = (int64_t)device_info().sms * 8;
+  if (blocks > cap) blocks = cap;
+  const bool bf = c.dtype == MOE_BF16;
+  if (c.K <= 1) {
+    if (bf) combine_kernel<__nv_bfloat16, 1><<<(unsigned)blocks, 256, 0, st>>>(p);
+    else combine_kernel<float, 1><<<(unsigned)blocks, 256, 0, st>>>(p);
+  } else if (c.K <= 2) {
+    if (bf) combine_kernel<__nv_bfloat16, 2><<<(unsigned)blocks, 256, 0, st>>>(p);
+    else combine_kernel<float, 2><<<(unsigned)blocks, 256, 0, st>>>(p);
+  } else if (c.K <= 8) {
+    if (bf) combine_kernel<__nv_bfloat16, 8><<<(unsigned)blocks, 256, 0, st>>>(p);
+    else combine_kernel<float, 8><<<(unsigned)blocks, 256, 0, st>>>(p);
+  } else {
+    if (bf) combine_kernel<__nv_bfloat16, 16><<<(unsigned)blocks, 256, 0, st>>>(p);
+    else combine_kernel<float, 16><<<(unsigned)blocks, 256, 0, st>>>(p);
+  }
+  CUDA_TRY(cudaGetLastError());
+  return MOE_OK;
+}
+
+template <typename T>
+cudaError_t launch_ffn_simt(const moe_config& c, const void* xp, const int32_t* offsets, const int32_t* kept,
+                            const void* w13, const void* w2, void* yp, void* inter, cudaStream_t st) {
+  const int64_t R = rows_of(c);
+  const unsigned mblocks = (unsigned)((R + kSimtBM - 1) / kSimtBM + c.E);
+  SimtParams p{};
+  p.A = xp;
+  p.lda = c.h;
+  p.B = w13;
+  p.ldb = c.h;
+  p.b_expert_rows = 2LL * c.I;
+  p.up_rows = c.I;
+  p.C = inter;
+  p.ldc = c.I;
+  p.offsets = offsets;
+  p.kept = kept;
+  p.E = c.E;
+  p.N = c.I;
+  p.K = c.h;
+  simt_gemm_kernel<T, kSimtSwiglu><<<dim3((c.I + kSimtBN - 1) / kSimtBN, mblocks), kSimtThreads, 0, st>>>(p);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  SimtParams q = p;
+  q.A = inter;
+  q.lda = c.I;
+  q.B = w2;
+  q.ldb = c.I;
+  q.b_expert_rows = c.h;
+  q.up_rows = 0;
+  q.C = yp;
+  q.ldc = c.h;
+  q.N = c.h;
+  q.K = c.I;
+  simt_gemm_kernel<T, kSimtPlain><<<dim3((c.h + kSimtBN - 1) / kSimtBN, mblocks), kSimtThreads, 0, st>>>(q);
+  return cudaGetLastError();
+}
+
+// cuTensorMapEncodeTiled through the runtime's driver entry point (no -lcuda).
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  if (fn == nullptr) {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  }
+  return fn;
+}
+
+// 2-D bf16 K-major tensor [rows, inner] read in boxes of box_rows x 64 elements
+// with the 128-byte swizzle the MMA descriptors expect.
+moe_status make_tensor_map(CUtensorMap* map, const void* base, uint64_t inner, uint64_t rows, uint32_t box_rows) {
+  PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
+  if (enc == nullptr) return MOE_ERR_CUDA;
+  const cuuint64_t dims[2] = {inner, rows};
+  const cuuint64_t strides[1] = {inner * 2};
+  const cuuint32_t box[2] = {(cuuint32_t)kTcBK, box_rows};
+  const cuuint32_t estr[2] = {1, 1};
+  const CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+                         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? MOE_OK : MOE_ERR_CUDA;
+}
+
+moe_status launch_ffn_tc(const moe_config& c, const void* xp, const int32_t* offsets, const int32_t* kept,
+                         const void* w13, const void* w2, void* yp, void* inter, cudaStream_t st) {
+  const int64_t R = rows_of(c);
+  const int grid = device_info().sms;
+  CUtensorMap a1, b1, a2, b2;
+  MOE_TRY(make_tensor_map(&a1, xp, c.h, R, kTcBM));
+  MOE_TRY(make_tensor_map(&b1, w13, c.h, (uint64_t)c.E * 2 * c.I, kTcBN / 2));
+  MOE_TRY(make_tensor_map(&a2, inter, c.I, R, kTcBM));
+  MOE_TRY(make_tensor_map(&b2, w2, c.I, (uint64_t)c.E * c.h, kTcBN));
+  TcParams p1{};
+  p1.offsets = offsets;
+  p1.kept = kept;
+  p1.E = c.E;
+  p1.n_tiles = (c.I + kTcBN / 2 - 1) / (kTcBN / 2);
+  p1.k_blocks = c.h / kTcBK;
+  p1.b_rows = 2LL * c.I;
+  p1.up_rows = c.I;
+  p1.n_valid = c.I;
+  p1.out = static_cast<__nv_bfloat16*>(inter);
+  p1.ldo = c.I;
+  TcParams p2 = p1;
+  p2.n_tiles = (c.h + kTcBN - 1) / kTcBN;
+  p2.k_blocks = c.I / kTcBK;
+  p2.b_rows = c.h;
+  p2.up_rows = 0;
+  p2.n_valid = c.h;
+  p2.out = static_cast<__nv_bfloat16*>(yp);
+  p2.ldo = c.h;
+  CUDA_TRY(allow_smem(ffn_tc_kernel<kTcSwiglu>, kTcDynSmem));
+  CUDA_TRY(allow_smem(ffn_tc_kernel<kTcStore>, kTcDynSmem));
+  ffn_tc_kernel<kTcSwiglu><<<grid, kTcThreads, kTcDynSmem, st>>>(a1, b1, p1);
+  CUDA_TRY(cudaGetLastError());
+  ffn_tc_kernel<kTcStore><<<grid, kTcThreads, kTcDynSmem, st>>>(a2, b2, p2);
+  CUDA_TRY(cudaGetLastError());
+  return MOE_OK;
+}
+
+moe_status launch_ffn(const moe_config& c, const void* xp, const int32_t* offsets, const int32_t* kept,
+                      const void* w13, const void* w2, void* yp, void* inter, cudaStream_t st) {
+  if (rows_of(c) == 0) return MOE_OK;
+  if (c.dtype == MOE_BF16) return launch_ffn_tc(c, xp, offsets, kept, w13, w2, yp, inter, st);
+  CUDA_TRY(launch_ffn_simt<float>(c, xp, offsets, kept, w13, w2, yp, inter, st));
+  return MOE_OK;
+}
+
+moe_status layer_core(const moe_config& c, const void* x, const void* w_r, const float* logit_offset,
+                      const float* sel_bias, const void* w13, const void* w2, void* y, const moe_layer_out* out,
+                      const LayerBuffers& b, cudaStream_t st) {
+  moe_layer_out o{};
+  if (out != nullptr) o = *out;
+  float* logits = o.logits ? o.logits : b.logits;
+  int32_t* ids = o.topk_ids ? o.topk_ids : b.ids;
+  float* w = o.topk_w ? o.topk_w : b.w;
+  int32_t* counts = o.counts ? o.counts : b.counts;
+  int32_t* kept = o.kept ? o.kept : b.kept;
+  int32_t* offsets = o.offsets ? o.offsets : b.offsets;
+  int32_t* slot = o.slot ? o.slot : b.slot;
+  int32_t* row_src = o.row_src ? o.row_src : b.row_src;
+  int64_t* n_ij = o.n_ij ? o.n_ij : b.n_ij;
+  int64_t* rank_bytes = o.rank_bytes ? o.rank_bytes : b.rank_bytes;
+  moe_layout_stats* stats = o.stats ? o.stats : b.stats;
+  MOE_TRY(launch_logits(c, x, w_r, logit_offset, logits, st));
+  MOE_TRY(launch_route(c, logits, sel_bias, ids, w, st));
+  MOE_TRY(launch_layout(c, ids, counts, kept, offsets, slot, row_src, n_ij, rank_bytes, stats, b.layout_ws, st));
+  MOE_TRY(launch_permute(c, x, slot, row_src, b.xp, st));
+  MOE_TRY(launch_ffn(c, b.xp, offsets, kept, w13, w2, b.yp, b.inter, st));
+  MOE_TRY(launch_combine(c, b.yp, slot, w, y, st));
+  return MOE_OK;
+}
+
+moe_status check_layer_ptrs(const moe_config& c, const void* x, const void* w_r, const float* logit_offset,
+                            const float* sel_bias, const void* w13, const void* w2) {
+  MOE_TRY(check_dtype_ptr(w_r));
+  MOE_TRY(check_dtype_ptr(w13));
+  MOE_TRY(check_dtype_ptr(w2));
+  MOE_TRY(check_opt_ptr(logit_offset, 4));
+  MOE_TRY(check_opt_ptr(sel_bias, 4));
+  (void)x;
+  (void)c;
+  return MOE_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* moe_status_string(moe_status s) {
+  switch (s) {
+    case MOE_OK: return "MOE_OK";
+    case MOE_ERR_INVALID_ARG: return "MOE_ERR_INVALID_ARG";
+    case MOE_ERR_UNSUPPORTED: return "MOE_ERR_UNSUPPORTED";
+    case MOE_ERR_ALIGNMENT: return "MOE_ERR_ALIGNMENT";
+    case MOE_ERR_WORKSPACE_TOO_SMALL: return "MOE_ERR_WORKSPACE_TOO_SMALL";
+    case MOE_ERR_CUDA: return "MOE_ERR_CUDA";
+    case MOE_ERR_DEVICE_TIMEOUT: return "MOE_ERR_DEVICE_TIMEOUT";
+    case MOE_ERR_DEVICE_BAD_INDEX: return "MOE_ERR_DEVICE_BAD_INDEX";
+  }
+  return "MOE_UNKNOWN_STATUS";
+}
+
+moe_status moe_validate_config(const moe_config* cfg) { return validate(cfg); }
+
+moe_status moe_rows(const moe_config* cfg, int64_t* rows) {
+  MOE_TRY(validate(cfg));
+  if (rows == nullptr) return MOE_ERR_INVALID_ARG;
+  *rows = rows_of(*cfg);
+  return MOE_OK;
+}
+
+moe_status moe_workspace_size(const moe_config* cfg, int32_t op, size_t* bytes) {
+  MOE_TRY(validate(cfg));
+  if (bytes == nullptr) return MOE_ERR_INVALID_ARG;
+  switch (op) {
+    case MOE_OP_LAYOUT: *bytes = layout_scratch_bytes((int64_t)cfg->T * cfg->K, cfg->E); return MOE_OK;
+    case MOE_OP_FFN: *bytes = ffn_ws_bytes(*cfg); return MOE_OK;
+    case MOE_OP_LAYER: *bytes = carve_layer(*cfg, nullptr, false).total; return MOE_OK;
+    case MOE_OP_LAYER_HOST: *bytes = carve_layer(*cfg, nullptr, true).total; return MOE_OK;
+  }
+  return MOE_ERR_INVALID_ARG;
+}
+
+moe_status moe_workspace_init(void* workspace, size_t workspace_bytes, void* stream) {
+  if (workspace == nullptr || !aligned(workspace, 256)) return workspace ? MOE_ERR_ALIGNMENT : MOE_ERR_INVALID_ARG;
+  CUDA_TRY(cudaMemsetAsync(workspace, 0, workspace_bytes, as_stream(stream)));
+  return MOE_OK;
+}
+
+moe_status moe_router_logits(const moe_config* cfg, const void* x, const void* w_r, const float* logit_offset,
+                             float* logits, void* stream) {
+  MOE_TRY(validate(cfg));
+  if (cfg->T > 0) {
+    MOE_TRY(check_dtype_ptr(x));
+    MOE_TRY(check_ptr(logits, 4));
+  }
+  MOE_TRY(check_dtype_ptr(w_r));
+  MOE_TRY(check_opt_ptr(logit_offset, 4));
+  return launch_logits(*cfg, x, w_r, logit_offset, logits, as_stream(stream));
+}
+
+moe_status moe_route(const moe_config* cfg, const float* logits, const float* sel_bias, int32_t* topk_ids,
+                     float* topk_w, void* stream) {
+  MOE_TRY(validate(cfg));
+  if (cfg->T > 0) {
+    MOE_TRY(check_ptr(logits, 4));
+    MOE_TRY(check_ptr(topk_ids, 4));
+    MOE_TRY(check_ptr(topk_w, 4));
+  }
+  MOE_TRY(check_opt_ptr(sel_bias, 4));
+  return launch_route(*cfg, logits, sel_bias, topk_ids, topk_w, as_stream(stream));
+}
+
+moe_status moe_dispatch_layout(const moe_config* cfg, const int32_t* topk_ids, int32_t* counts, int32_t* kept,
+                               int32_t* offsets, int32_t* slot, int32_t* row_src, int64_t* n_ij,
+                               int64_t* rank_bytes, moe_layout_stats* stats, void* workspace,
+                               size_t workspace_bytes, void* stream) {
+  MOE_TRY(validate(cfg));
+  if (cfg->T > 0) {
+    MOE_TRY(check_ptr(topk_ids, 4));
+    MOE_TRY(check_ptr(slot, 4));
+  }
+  if (rows_of(*cfg) > 0) MOE_TRY(check_ptr(row_src, 4));
+  MOE_TRY(check_ptr(counts, 4));
+  MOE_TRY(check_ptr(kept, 4));
+  MOE_TRY(check_ptr(offsets, 4));
+  MOE_TRY(check_ptr(n_ij, 8));
+  MOE_TRY(check_ptr(rank_bytes, 8));
+  MOE_TRY(check_ptr(stats, 8));
+  MOE_TRY(check_ptr(workspace, 256));
+  if (workspace_bytes < layout_scratch_bytes((int64_t)cfg->T * cfg->K, cfg->E)) return MOE_ERR_WORKSPACE_TOO_SMALL;
+  return launch_layout(*cfg, topk_ids, counts, kept, offsets, slot, row_src, n_ij, rank_bytes, stats, workspace,
+                       as_stream(stream));
+}
+
+moe_status moe_permute(const moe_config* cfg, const void* x, const int32_t* slot, const int32_t* row_src, void* xp,
+                       void* stream) {
+  MOE_TRY(validate(cfg));
+  if (cfg->T > 0) {
+    MOE_TRY(check_dtype_ptr(x));
+    MOE_TRY(check_ptr(slot, 4));
+  }
+  if (rows_of(*cfg) > 0) MOE_TRY(check_dtype_ptr(xp));
+  if (cfg->pad && rows_of(*cfg) > 0) MOE_TRY(check_ptr(row_src, 4));
+  return launch_permute(*cfg, x, slot, row_src, xp, as_stream(stream));
+}
+
+moe_status moe_grouped_ffn(const moe_config* cfg, const void* xp, const int32_t* offsets, const int32_t* kept,
+                           const void* w13, const void* w2, void* yp, void* workspace, size_t workspace_bytes,
+                           void* stream) {
+  MOE_TRY(validate(cfg));
+  if (rows_of(*cfg) > 0) {
+    MOE_TRY(check_dtype_ptr(xp));
+    MOE_TRY(check_dtype_ptr(yp));
+  }
+  MOE_TRY(check_ptr(offsets, 4));
+  MOE_TRY(check_ptr(kept, 4));
+  MOE_TRY(check_dtype_ptr(w13));
+  MOE_TRY(check_dtype_ptr(w2));
+  MOE_TRY(check_ptr(workspace, 256));
+  if (workspace_bytes < ffn_ws_bytes(*cfg)) return MOE_ERR_WORKSPACE_TOO_SMALL;
+  return launch_ffn(*cfg, xp, offsets, kept, w13, w2, yp, static_cast<char*>(workspace) + 256, as_stream(stream));
+}
+
+moe_status moe_combine(const moe_config* cfg, const void* yp, const int32_t* slot, const float* topk_w, void* y,
+                       void* stream) {
+  MOE_TRY(validate(cfg));
+  if (cfg->T > 0) {
+    MOE_TRY(check_ptr(slot, 4));
+    MOE_TRY(check_ptr(topk_w, 4));
+    MOE_TRY(check_dtype_ptr(y));
+    if (rows_of(*cfg) > 0) MOE_TRY(check_dtype_ptr(yp));
+  }
+  return launch_combine(*cfg, yp, slot, topk_w, y, as_stream(stream));
+}
+
+moe_status moe_layer_forward(const moe_config* cfg, const void* x, const void* w_r, const float* logit_offset,
+                             const float* sel_bias, const void* w13, const void* w2, void* y,
+                             const moe_layer_out* out, void* workspace, size_t workspace_bytes, void* stream) {
+  MOE_TRY(validate(cfg));
+  if (cfg->T > 0) {
+    MOE_TRY(check_dtype_ptr(x));
+    MOE_TRY(check_dtype_ptr(y));
+  }
+  MOE_TRY(check_layer_ptrs(*cfg, x, w_r, logit_offset, sel_bias, w13, w2));
+  MOE_TRY(check_ptr(workspace, 256));
+  const LayerBuffers b = carve_layer(*cfg, workspace, false);
+  if (workspace_bytes < b.total) return MOE_ERR_WORKSPACE_TOO_SMALL;
+  return layer_core(*cfg, x, w_r, logit_offset, sel_bias, w13, w2, y, out, b, as_stream(stream));
+}
+
+moe_status moe_layer_forward_host(const moe_config* cfg, const void* x_host, const void* w_r,
+                                  const float* logit_offset, const float* sel_bias, const void* w13, const void* w2,
+                                  void* y_host, void* workspace, size_t workspace_bytes, void* stream) {
+  MOE_TRY(validate(cfg));
+  if (cfg->T > 0 && (x_host == nullptr || y_host == nullptr)) return MOE_ERR_INVALID_ARG;
+  MOE_TRY(check_layer_ptrs(*cfg, x_host, w_r, logit_offset, sel_bias, w13, w2));
+  MOE_TRY(check_ptr(workspace, 256));
+  const LayerBuffers b = carve_layer(*cfg, workspace, true);
+  if (workspace_bytes < b.total) return MOE_ERR_WORKSPACE_TOO_SMALL;
+  const cudaStream_t st = as_stream(stream);
+  const size_t bytes = (size_t)cfg->T * cfg->h * ds_of(*cfg);
+  if (bytes > 0) CUDA_TRY(cudaMemcpyAsync(b.xdev, x_host, bytes, cudaMemcpyHostToDevice, st));
+  MOE_TRY(layer_core(*cfg, b.xdev, w_r, logit_offset, sel_bias, w13, w2, b.ydev, nullptr, b, st));
+  if (bytes > 0) CUDA_TRY(cudaMemcpyAsync(y_host, b.ydev, bytes, cudaMemcpyDeviceToHost, st));
+  return MOE_OK;
+}
+
+moe_status moe_check(void* stream) {
+  if (cudaStreamSynchronize(as_stream(stream)) != cudaSuccess) {
+    (void)cudaGetLastError();
+    return MOE_ERR_CUDA;
+  }
+  if (cudaGetLastError() != cudaSuccess) return MOE_ERR_CUDA;
+  uint32_t err = 0;
+  CUDA_TRY(cudaMemcpyFromSymbol(&err, g_dev_error, sizeof(err)));
+  if (err == 0) return MOE_OK;
+  const uint32_t zero = 0;
+  CUDA_TRY(cudaMemcpyToSymbol(g_dev_error, &zero, sizeof(zero)));
+  return (err & kErrTimeout) ? MOE_ERR_DEVICE_TIMEOUT : MOE_ERR_DEVICE_BAD_INDEX;
+}
+
+}  // extern "C"

@@ -1,0 +1,213 @@
+/*
+ * moe.h - C ABI of a B300-native (sm_103a) forward pass of a Mixture-of-Experts
+ * FFN layer on one GPU: router logits -> top-K routing -> dispatch layout ->
+ * permute -> grouped SwiGLU FFN -> weighted combine.
+ *
+ * Sources (cited by page title and section):
+ *  [overview] "专家并行 / 总览" (t6page.pages.dev): glossary table
+ *             tbl-ep-overview-glossary (Router, top-K, Dispatch, Combine, EP 组,
+ *             Expert group, Balancedness); "MoE 路由机制是什么" (the flow Router ->
+ *             Dispatch -> Expert Compute -> Combine); "Dispatch 通信矩阵" (eq.
+ *             par-ep-dispatch-matrix, expert_id / experts_per_chip = chip_id);
+ *             "通信量公式" (eqs. par-ep-comm-total / per-chip / pair).
+ *  [notes]    "专家并行与 MoE" (note.yj-dis.top): "MoE 结构回顾" (router, capacity
+ *             factor, token drop); "负载均衡" (aux-loss-free per-expert bias;
+ *             drop/pad).
+ *  [compass]  "專家並行（Expert Parallelism, EP）" (compassingai.com): "技術原理"
+ *             (route, dispatch, expert compute, weighted combine); "關鍵引數與考量"
+ *             (capacity factor).
+ *  [serving]  "MoE 服務的專家並行性" (aiunderstanding.org): "技術洞察" (capacity,
+ *             drop or pad so every expert GEMM has a predictable shape).
+ *
+ * Conventions shared by every call:
+ *  - All tensor pointers are DEVICE pointers owned by the caller, except the
+ *    two host buffers of moe_layer_forward_host.  The library never allocates
+ *    or frees memory.
+ *  - Every call is asynchronous on `stream` (a cudaStream_t; NULL = legacy
+ *    default stream) and does not synchronise the host, except moe_check.
+ *  - Arguments are validated on the host before any launch; a bad argument
+ *    returns an error status and launches nothing.  There is no CPU fallback.
+ *  - Row-major layouts, the last index contiguous.  "dtype" tensors hold
+ *    float32 (MOE_F32) or bfloat16 (MOE_BF16) elements.
+ *  - Tensor pointers of dtype must be 16-byte aligned; int32/float32 index and
+ *    weight arrays 4-byte aligned; int64 arrays 8-byte aligned.
+ *  - Device-side failures (a bounded wait that ran out, an out-of-range expert
+ *    id) set a sticky per-device error word; moe_check reports and clears it.
+ */
+#ifndef MOE_H_
+#define MOE_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  MOE_OK = 0,
+  MOE_ERR_INVALID_ARG = 1,          /* NULL config/pointer, size out of range */
+  MOE_ERR_UNSUPPORTED = 2,          /* valid but not implemented combination */
+  MOE_ERR_ALIGNMENT = 3,            /* pointer misaligned (see conventions) */
+  MOE_ERR_WORKSPACE_TOO_SMALL = 4,  /* workspace_bytes below moe_workspace_size */
+  MOE_ERR_CUDA = 5,                 /* a CUDA runtime call or launch failed */
+  MOE_ERR_DEVICE_TIMEOUT = 6,       /* a bounded device-side wait ran out */
+  MOE_ERR_DEVICE_BAD_INDEX = 7      /* an expert id outside [0, E) reached the device */
+} moe_status;
+
+typedef enum { MOE_F32 = 0, MOE_BF16 = 1 } moe_dtype;
+typedef enum { MOE_SOFTMAX = 0, MOE_SIGMOID = 1 } moe_score;
+typedef enum { MOE_OP_LAYOUT = 0, MOE_OP_FFN = 1, MOE_OP_LAYER = 2, MOE_OP_LAYER_HOST = 3 } moe_op;
+
+/* Layer description.  Limits: T >= 0; h % 64 == 0; I % 64 == 0; 1 <= E <= 1024;
+ * 1 <= K <= min(E, 16); T*K and the permuted row count below 2^31. */
+typedef struct moe_config {
+  int32_t T;            /* tokens (the pages' B) */
+  int32_t h;            /* hidden size */
+  int32_t E;            /* routed experts */
+  int32_t K;            /* experts per token (top-K) */
+  int32_t I;            /* expert intermediate size (SwiGLU) */
+  int32_t dtype;        /* moe_dtype of activations, weights and outputs */
+  int32_t score;        /* moe_score: softmax over experts or elementwise sigmoid */
+  int32_t renormalize;  /* 1: chosen weights are divided by their sum */
+  float scale;          /* routed scaling factor applied to the weights */
+  int32_t n_groups;     /* 0: no group limit; else E % n_groups == 0, n_groups <= 32 */
+  int32_t topk_groups;  /* groups kept per token (group-limited routing) */
+  int32_t group_topn;   /* a group's score = sum of its group_topn largest keys */
+  int32_t capacity;     /* 0: dropless; > 0: per-expert cap, overflow dropped in token order */
+  int32_t pad;          /* 1 (needs capacity > 0): expert e owns rows [e*cap, (e+1)*cap) */
+  int32_t ep_size;      /* virtual expert-parallel group size N_EP; E % ep_size == 0 */
+} moe_config;
+
+/* Scalar results of moe_dispatch_layout (device memory, 32 bytes). */
+typedef struct moe_layout_stats {
+  int64_t kept_total;       /* assignments kept (permuted rows that carry a token) */
+  int64_t dropped;          /* T*K - kept_total */
+  int64_t offdiag_rows;     /* sum of n_ij over i != j: rows that would cross chips */
+  int32_t experts_touched;  /* experts with at least one kept row */
+  float balancedness;       /* sum_j recv_j / (N_EP * max_j recv_j); 1 if nothing received */
+} moe_layout_stats;
+
+/* Optional device outputs of moe_layer_forward.  Any NULL member is kept in the
+ * workspace instead.  Shapes as in the individual calls below. */
+typedef struct moe_layer_out {
+  float* logits;            /* [T, E] */
+  int32_t* topk_ids;        /* [T, K] */
+  float* topk_w;            /* [T, K] */
+  int32_t* counts;          /* [E] */
+  int32_t* kept;            /* [E] */
+  int32_t* offsets;         /* [E + 1] */
+  int32_t* slot;            /* [T, K] */
+  int32_t* row_src;         /* [R] */
+  int64_t* n_ij;            /* [N_EP, N_EP] */
+  int64_t* rank_bytes;      /* [2, N_EP]: sent then received bytes per chip */
+  moe_layout_stats* stats;  /* [1] */
+} moe_layer_out;
+
+/* Human-readable name of a status code (static string). */
+const char* moe_status_string(moe_status s);
+
+/* Checks a configuration against the limits above (host only, no CUDA call). */
+moe_status moe_validate_config(const moe_config* cfg);
+
+/* Rows R of the permuted buffers: T*K, or E*capacity when pad is set. */
+moe_status moe_rows(const moe_config* cfg, int64_t* rows);
+
+/* Workspace bytes needed by `op` (host only).  MOE_OP_LAYOUT: moe_dispatch_layout;
+ * MOE_OP_FFN: moe_grouped_ffn; MOE_OP_LAYER / MOE_OP_LAYER_HOST: the whole layer. */
+moe_status moe_workspace_size(const moe_config* cfg, int32_t op, size_t* bytes);
+
+/* Zero-fills a workspace.  Must run once after allocation, and again after a call
+ * on it returned MOE_ERR_DEVICE_TIMEOUT; calls that succeed leave it reusable. */
+moe_status moe_workspace_init(void* workspace, size_t workspace_bytes, void* stream);
+
+/* Router logits ([overview] glossary "Router"): logits[t,e] = sum_j x[t,j] w_r[e,j]
+ * (+ logit_offset[e]), float32 accumulation.  x [T,h] dtype; w_r [E,h] dtype;
+ * logit_offset [E] float32 or NULL; logits [T,E] float32. */
+moe_status moe_router_logits(const moe_config* cfg, const void* x, const void* w_r,
+                             const float* logit_offset, float* logits, void* stream);
+
+/* Top-K routing ([overview] glossary "top-K"; [notes] "负载均衡": the aux-loss-free
+ * per-expert bias steers selection only; [overview] glossary "Expert group").
+ * Scores s = softmax(logits) or sigmoid(logits) in float64.  Selection key
+ * fl32(s + sel_bias) (logits themselves for softmax without bias or groups).
+ * Group limit: keep the topk_groups groups with the largest float32 sum of their
+ * group_topn best keys (ties to the lower group).  Top-K by key descending,
+ * ties to the lower id, written in that order.  Weights: unbiased scores of the
+ * chosen experts, divided by their sum if renormalize, times scale, float32.
+ * logits [T,E] float32; sel_bias [E] float32 or NULL; topk_ids [T,K] int32;
+ * topk_w [T,K] float32. */
+moe_status moe_route(const moe_config* cfg, const float* logits, const float* sel_bias,
+                     int32_t* topk_ids, float* topk_w, void* stream);
+
+/* Dispatch layout ([overview] "Dispatch 通信矩阵", eq. par-ep-dispatch-matrix;
+ * [compass] "關鍵引數與考量"; [notes] "负载均衡" drop/pad).  Histogram and a stable
+ * rank of every assignment (t,k) inside its expert in token order (one pass,
+ * decoupled look-back); capacity drop in token order; offsets = exclusive scan of
+ * kept (pad: e*capacity); slot[t,k] = offsets[e] + rank or -1 if dropped;
+ * row_src[r] = token of permuted row r or -1; n_ij[i][j] = kept assignments from
+ * chip i = t*N_EP/T to chip j = e/(E/N_EP); rank_bytes = n_ij row/column sums times
+ * h*dtype_size; stats as in moe_layout_stats.
+ * topk_ids [T,K] int32; counts, kept [E] int32; offsets [E+1] int32; slot [T,K]
+ * int32; row_src [R] int32; n_ij [N_EP,N_EP] int64; rank_bytes [2,N_EP] int64;
+ * stats [1]; workspace >= moe_workspace_size(MOE_OP_LAYOUT), initialised once. */
+moe_status moe_dispatch_layout(const moe_config* cfg, const int32_t* topk_ids, int32_t* counts,
+                               int32_t* kept, int32_t* offsets, int32_t* slot, int32_t* row_src,
+                               int64_t* n_ij, int64_t* rank_bytes, moe_layout_stats* stats,
+                               void* workspace, size_t workspace_bytes, void* stream);
+
+/* Permute: the on-device stand-in for the dispatch All-to-All ([overview] glossary
+ * "Dispatch"; [compass] "技術原理" step 2).  xp[slot[t,k]] = x[t] for every kept
+ * (t,k); with pad, rows whose row_src is -1 are zero-filled; other rows are not
+ * written.  x [T,h] dtype; slot [T,K]; row_src [R] (read only with pad; may be
+ * NULL otherwise); xp [R,h] dtype. */
+moe_status moe_permute(const moe_config* cfg, const void* x, const int32_t* slot,
+                       const int32_t* row_src, void* xp, void* stream);
+
+/* Grouped SwiGLU FFN over ragged expert segments ([compass] "技術原理" step 3;
+ * [serving] "技術洞察": grouped GEMM).  For every expert e and row r in
+ * [offsets[e], offsets[e] + kept[e]): a = silu(xp[r] Wg_e^T) * (xp[r] Wu_e^T),
+ * stored in dtype; yp[r] = a Wd_e^T, stored in dtype.  float32 accumulation.
+ * xp [R,h] dtype; offsets [E+1]; kept [E]; w13 [E,2I,h] dtype (gate rows 0..I-1
+ * then up rows I..2I-1); w2 [E,h,I] dtype; yp [R,h] dtype (rows outside the
+ * segments are not written); workspace >= moe_workspace_size(MOE_OP_FFN). */
+moe_status moe_grouped_ffn(const moe_config* cfg, const void* xp, const int32_t* offsets,
+                           const int32_t* kept, const void* w13, const void* w2, void* yp,
+                           void* workspace, size_t workspace_bytes, void* stream);
+
+/* Weighted combine ([compass] "技術原理" step 4; [overview] glossary "Combine"):
+ * y[t] = sum_{k: slot[t,k] >= 0} topk_w[t,k] * yp[slot[t,k]], float32 sum in k order,
+ * stored in dtype; dropped assignments contribute nothing (no renormalisation).
+ * yp [R,h] dtype; slot [T,K]; topk_w [T,K] float32; y [T,h] dtype. */
+moe_status moe_combine(const moe_config* cfg, const void* yp, const int32_t* slot,
+                       const float* topk_w, void* y, void* stream);
+
+/* The whole layer ([overview] "MoE 路由机制是什么"): router_logits -> route ->
+ * dispatch_layout -> permute -> grouped_ffn -> combine on one stream.
+ * x [T,h]; w_r [E,h]; logit_offset, sel_bias [E] float32 or NULL; w13, w2 as in
+ * moe_grouped_ffn; y [T,h]; out: optional extra outputs (NULL = none);
+ * workspace >= moe_workspace_size(MOE_OP_LAYER), initialised once. */
+moe_status moe_layer_forward(const moe_config* cfg, const void* x, const void* w_r,
+                             const float* logit_offset, const float* sel_bias, const void* w13,
+                             const void* w2, void* y, const moe_layer_out* out, void* workspace,
+                             size_t workspace_bytes, void* stream);
+
+/* moe_layer_forward with HOST activations: copies x_host [T,h] (pinned host
+ * memory recommended) to the device, runs the layer, and copies y back to
+ * y_host [T,h], all asynchronously on `stream`; weights stay on the device.
+ * workspace >= moe_workspace_size(MOE_OP_LAYER_HOST). */
+moe_status moe_layer_forward_host(const moe_config* cfg, const void* x_host, const void* w_r,
+                                  const float* logit_offset, const float* sel_bias,
+                                  const void* w13, const void* w2, void* y_host,
+                                  void* workspace, size_t workspace_bytes, void* stream);
+
+/* Synchronises `stream`, then reports and clears the sticky device error word of
+ * the current device: MOE_ERR_DEVICE_TIMEOUT, MOE_ERR_DEVICE_BAD_INDEX,
+ * MOE_ERR_CUDA for a pending CUDA error, else MOE_OK. */
+moe_status moe_check(void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MOE_H_ */

@@ -189,6 +189,25 @@ def route(L: np.ndarray, cfg, bias: Optional[np.ndarray] = None):
     return ids, w, keys, allowed
 
 
+def group_margin(keys: np.ndarray, cfg) -> np.ndarray:
+    """Relative gap between the last kept and the first dropped group score of every
+    token (inf without a group limit).  See topk_margin."""
+    T, E = keys.shape
+    out = np.full(T, np.inf)
+    if cfg.n_groups <= 0 or cfg.topk_groups >= cfg.n_groups:
+        return out
+    gs = E // cfg.n_groups
+    for t in range(T):
+        sc = []
+        for g in range(cfg.n_groups):
+            top = sorted(keys[t, g * gs:(g + 1) * gs].tolist(), reverse=True)[:cfg.group_topn]
+            sc.append(sum(top))
+        sc.sort(reverse=True)
+        a, b = sc[cfg.topk_groups - 1], sc[cfg.topk_groups]
+        out[t] = abs(a - b) / max(abs(a), 1e-30)
+    return out
+
+
 def topk_margin(keys: np.ndarray, allowed: np.ndarray, K: int) -> np.ndarray:
     """Relative gap between the K-th and (K+1)-th allowed key of every token
     (inf when fewer than K+1 experts are allowed).  Used to tell genuine routing
@@ -310,64 +329,71 @@ def silu(g: np.ndarray) -> np.ndarray:
     return g / (1.0 + np.exp(-g))
 
 
-def expert_ffn(xrows: np.ndarray, w13: np.ndarray, w2: np.ndarray, dtype: str, I: int) -> np.ndarray:
+def expert_ffn(xrows: np.ndarray, w13: np.ndarray, w2: np.ndarray, dtype: str, I: int,
+               rounded: bool = True) -> np.ndarray:
     """One expert's SwiGLU FFN on a block of rows ([compass] "技術原理" step 3:
     every expert is an independent FFN; SwiGLU per the layer's configuration).
 
     g = X Wg^T, u = X Wu^T (Wg = w13[:I], Wu = w13[I:]); a = silu(g) * u,
     stored in the data type (READING: the intermediate activation is a stored
     tensor of the layer's data type); y = a Wd^T with Wd = w2 [h, I], stored in
-    the data type.  float64 sums.
+    the data type.  float64 sums.  With ``rounded=False`` the output is returned
+    in float64 before its final rounding (the intermediate is still rounded).
     """
     X = to_f64(xrows, dtype)
     W = to_f64(w13, dtype)
     g = X @ W[:I].T
     u = X @ W[I:].T
     a = to_f64(store(silu(g) * u, dtype), dtype)
-    return store(a @ to_f64(w2, dtype).T, dtype)
+    y = a @ to_f64(w2, dtype).T
+    return store(y, dtype) if rounded else y
 
 
 def grouped_ffn(xp: np.ndarray, offsets: np.ndarray, kept: np.ndarray, get_w13, get_w2,
-                cfg, experts=None) -> dict:
+                cfg, experts=None, rows=None, rounded: bool = True) -> dict:
     """Runs expert_ffn on every expert's rows [offsets[e], offsets[e] + kept[e]).
 
     ``get_w13(e)`` / ``get_w2(e)`` return an expert's weights (so a caller can
-    stream them); ``experts`` restricts the work to a subset.  Returns
-    {e: yp rows of e}.
+    stream them); ``experts`` restricts the work to a subset and ``rows`` (a
+    dict e -> absolute row indices inside e's segment) to some of its rows.
+    Returns {e: (row indices, yp rows)}.
     """
     out = {}
     for e in (range(cfg.E) if experts is None else experts):
         n = int(kept[e])
-        if n == 0:
-            out[e] = np.zeros((0, cfg.h), dtype=xp.dtype)
-            continue
         r0 = int(offsets[e])
-        out[e] = expert_ffn(xp[r0:r0 + n], get_w13(e), get_w2(e), cfg.dtype, cfg.I)
+        idx = np.arange(r0, r0 + n) if rows is None else np.asarray(rows[e], dtype=np.int64)
+        assert np.all((idx >= r0) & (idx < r0 + n))
+        if len(idx) == 0:
+            out[e] = (idx, np.zeros((0, cfg.h)))
+            continue
+        out[e] = (idx, expert_ffn(xp[idx], get_w13(e), get_w2(e), cfg.dtype, cfg.I, rounded))
     return out
 
 
 # ----------------------------------------------------------------- step 6: combine
 
 
-def combine(yp: np.ndarray, slot: np.ndarray, w: np.ndarray, cfg, tokens=None) -> np.ndarray:
+def combine(yp: np.ndarray, slot: np.ndarray, w: np.ndarray, cfg, tokens=None, rounded: bool = True) -> np.ndarray:
     """Weighted combine back into token order ([compass] "技術原理" step 4: results
     return to the token's device and are summed with the routing weights;
     [overview] glossary "Combine").
 
     y[t] = sum over k = 0..K-1 with slot[t,k] >= 0 of w[t,k] * yp[slot[t,k]],
     float64, stored in the data type.  Dropped assignments contribute nothing
-    and the remaining weights are not renormalised (READING).
+    and the remaining weights are not renormalised (READING).  ``yp`` may be
+    float64 (unrounded rows); ``rounded=False`` returns float64.
     """
     T = slot.shape[0]
     tok = range(T) if tokens is None else tokens
-    Y = to_f64(yp, cfg.dtype)
+    Y = yp if yp.dtype == np.float64 else to_f64(yp, cfg.dtype)
     out = np.zeros((len(tok), cfg.h), dtype=np.float64)
     for i, t in enumerate(tok):
         for k in range(cfg.K):
             s = int(slot[t, k])
             if s >= 0:
                 out[i] += float(w[t, k]) * Y[s]
-    return store(out, cfg.dtype)
+    return store(out, cfg.dtype) if rounded else out
 
 
 # ----------------------------------------------------------------- whole layer
@@ -380,14 +406,15 @@ def layer_forward(x, w_r, get_w13, get_w2, cfg, sel_bias=None, logit_offset=None
     ids, w, keys, allowed = route(L, cfg, sel_bias)
     lay = dispatch_layout(ids, cfg)
     xp = permute(x, lay["row_src"])
-    parts = grouped_ffn(xp, lay["offsets"], lay["kept"], get_w13, get_w2, cfg)
-    yp = np.zeros_like(xp)
-    for e, rows in parts.items():
-        r0 = int(lay["offsets"][e])
-        yp[r0:r0 + len(rows)] = rows
+    parts = grouped_ffn(xp, lay["offsets"], lay["kept"], get_w13, get_w2, cfg, rounded=False)
+    yp_exact = np.zeros(xp.shape, dtype=np.float64)
+    for e, (idx, rows) in parts.items():
+        yp_exact[idx] = rows
+    yp = store(yp_exact, cfg.dtype)
     y = combine(yp, lay["slot"], w, cfg)
+    y_exact = combine(yp, lay["slot"], w, cfg, rounded=False)
     return {"logits": L, "ids": ids, "w": w, "keys": keys, "allowed": allowed,
-            "layout": lay, "xp": xp, "yp": yp, "y": y}
+            "layout": lay, "xp": xp, "yp": yp, "y": y, "y_exact": y_exact}
 
 
 # ----------------------------------------------------------------- page formulas

@@ -114,10 +114,39 @@ def normal_at(seed: int, tensor_id: int, index, sigma: float, dtype: str, chunk:
     return out
 
 
-def normal(seed: int, tensor_id: int, shape, sigma: float, dtype: str, start: int = 0) -> np.ndarray:
-    """A whole tensor (or a contiguous slice of one starting at flat element ``start``)."""
+def _host_lib():
+    """The C host generator (synth/libsynth_host.so), or None if not built."""
+    global _HOST
+    if _HOST is None:
+        import ctypes
+        import os
+        path = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libsynth_host.so")
+        if not os.path.exists(path):
+            return None
+        lib = ctypes.CDLL(path)
+        lib.synth_host_fill_normal.restype = None
+        lib.synth_host_fill_normal.argtypes = [ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_uint64,
+                                               ctypes.c_uint64, ctypes.c_int64, ctypes.c_float]
+        _HOST = lib
+    return _HOST
+
+
+_HOST = None
+
+
+def normal(seed: int, tensor_id: int, shape, sigma: float, dtype: str, start: int = 0,
+           use_c: bool = True) -> np.ndarray:
+    """A whole tensor (or a contiguous slice of one starting at flat element ``start``).
+
+    Uses the C host generator when it is built (same values, many times faster)."""
     n = int(np.prod(shape))
-    return normal_at(seed, tensor_id, np.arange(start, start + n, dtype=np.int64), sigma, dtype).reshape(shape)
+    lib = _host_lib() if use_c else None
+    if lib is None:
+        return normal_at(seed, tensor_id, np.arange(start, start + n, dtype=np.int64), sigma, dtype).reshape(shape)
+    out = np.empty(n, dtype=np.float32 if dtype == "f32" else np.uint16)
+    lib.synth_host_fill_normal(out.ctypes.data, n, 0 if dtype == "f32" else 1, seed, tensor_id, start,
+                               float(np.float32(sigma)))
+    return out.reshape(shape)
 
 
 def uniform(seed: int, tensor_id: int, n: int, lo: float, hi: float) -> np.ndarray:

@@ -1,0 +1,84 @@
+"""GPU parity of router logits and routing against the oracle, at full workload sizes."""
+import numpy as np
+import pytest
+import torch
+
+import expert_dispatch_bias_b300 as moe
+import oracle
+from synth import workloads
+
+from gpu_helpers import dev_of, host_inputs, np_of, oracle_routing, rel_err
+
+pytestmark = pytest.mark.gpu
+NAMES = list(workloads.ALL)
+
+
+@pytest.mark.parametrize("name", NAMES)
+def test_router_logits(name):
+    w = workloads.ALL[name]
+    h = host_inputs(name)
+    ref = oracle_routing(name)["logits"]
+    cfg = moe.config_from(w)
+    L = torch.empty(w.T, w.E, dtype=torch.float32, device="cuda")
+    off = dev_of(h["logit_offset"]) if h["logit_offset"] is not None else None
+    moe.moe_router_logits(cfg, dev_of(h["x"]), dev_of(h["w_r"]), off, L)
+    assert moe.moe_check() == 0
+    # float32 accumulation of exact bf16/f32 products vs float64 sums
+    assert rel_err(np_of(L), ref, "f32") < 1e-4
+
+
+@pytest.mark.parametrize("name", NAMES)
+def test_route_bit_exact_from_oracle_logits(name):
+    w = workloads.ALL[name]
+    o = oracle_routing(name)
+    h = host_inputs(name)
+    cfg = moe.config_from(w)
+    ids = torch.empty(w.T, w.K, dtype=torch.int32, device="cuda")
+    wt = torch.empty(w.T, w.K, dtype=torch.float32, device="cuda")
+    bias = dev_of(h["sel_bias"]) if h["sel_bias"] is not None else None
+    moe.moe_route(cfg, dev_of(o["logits"]), bias, ids, wt)
+    assert moe.moe_check() == 0
+    got = np_of(ids)
+    mism = np.argwhere(got != o["ids"])
+    assert len(mism) == 0, f"{len(mism)} id mismatches, first at {mism[:4].tolist()}"
+    # weights: float64 evaluation on both sides, one rounding to float32
+    np.testing.assert_allclose(np_of(wt), o["w"], rtol=3e-7, atol=0)
+
+
+def _route_case(cfg_kw, L, bias=None):
+    T, E = L.shape
+    base = dict(T=T, h=64, E=E, K=2, I=64, dtype="bf16", score="softmax")
+    base.update(cfg_kw)
+    w = workloads.Workload(name="case", **base)
+    ids_o, w_o, _, _ = oracle.route(L, w, bias)
+    cfg = moe.config_from(w)
+    ids = torch.empty(T, w.K, dtype=torch.int32, device="cuda")
+    wt = torch.empty(T, w.K, dtype=torch.float32, device="cuda")
+    moe.moe_route(cfg, dev_of(L), dev_of(bias) if bias is not None else None, ids, wt)
+    assert moe.moe_check() == 0
+    assert np.array_equal(np_of(ids), ids_o)
+    np.testing.assert_allclose(np_of(wt), w_o, rtol=3e-7, atol=0)
+
+
+@pytest.mark.parametrize("E,K", [(1, 1), (5, 3), (32, 32 // 2), (33, 7), (1000, 16), (1024, 1)])
+def test_route_shapes_and_ties(E, K):
+    """Odd expert counts, K up to 16, E up to 1024, and heavy exact ties (quantised
+    logits) for softmax, sigmoid+bias and group-limited sigmoid."""
+    rng = np.random.default_rng(E * 31 + K)
+    T = 301
+    L = (rng.integers(-6, 7, size=(T, E)) / 8.0).astype(np.float32)
+    _route_case(dict(K=K), L)
+    bias = (rng.integers(-3, 4, size=E) / 32.0).astype(np.float32)
+    _route_case(dict(K=K, score="sigmoid", scale=2.5), L, bias)
+    _route_case(dict(K=K, score="softmax", renormalize=0), L, bias)
+    for G in (2, 4, 8, 32):
+        if E % G == 0 and E // G >= 2 and (G // 2) * (E // G) >= K:
+            _route_case(dict(K=K, score="sigmoid", n_groups=G, topk_groups=G // 2, group_topn=2), L, bias)
+
+
+def test_route_empty_batch():
+    w = workloads.TINY.replace(T=0)
+    cfg = moe.config_from(w)
+    moe.moe_route(cfg, torch.empty(0, device="cuda"), None, torch.empty(0, dtype=torch.int32, device="cuda"),
+                  torch.empty(0, device="cuda"))
+    assert moe.moe_check() == 0

@@ -58,3 +58,11 @@ def test_zipf_offsets_skew():
     p /= p.sum()
     assert abs(freq[0] - p[0]) < 0.01
     assert freq[0] * E > 20
+
+
+def test_c_host_generator_matches_numpy_definition():
+    for dtype, sigma in (("f32", 1.0), ("bf16", 1.0 / 84.66), ("f32", 0.037)):
+        start = (1 << 33) + 12345            # beyond 32-bit element indices
+        a = synth.normal(0, synth.TID_W13, (5000,), sigma, dtype, start=start, use_c=True)
+        b = synth.normal(0, synth.TID_W13, (5000,), sigma, dtype, start=start, use_c=False)
+        assert a.dtype == b.dtype and np.array_equal(a, b)
