@@ -55,6 +55,23 @@ def workload_config(w):
             "parallelism": "replicas"}
 
 
+# ---------------------------------------------------------------------------- ranks
+def max_over_ranks(value: float, world: int, device) -> float:
+    """The largest `value` over all ranks (one scalar all-reduce; timing only)."""
+    if world <= 1:
+        return value
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(tokens_per_rank: int, world: int, steps: int, max_ms: float) -> float:
+    """Whole-job tokens/s: every rank's tokens over the slowest rank's time."""
+    return world * tokens_per_rank * steps / (max_ms / 1e3)
+
+
 # ---------------------------------------------------------------------------- clocks
 class ClockSampler:
     FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
@@ -115,7 +132,7 @@ def run_ours(args, rank, world, local_rank):
     from synth import device, workloads
 
     torch.cuda.set_device(local_rank)
-    w = workloads.ALL[args.workload]
+    w = workloads.ALL.get(args.workload) or workloads.EXTRA[args.workload]
     cfg = moe.config_from(w)
     inp = device.layer_inputs(w)
     dt = inp["x"].dtype
@@ -172,10 +189,7 @@ def run_ours(args, rank, world, local_rank):
     total_ms = events[0][0].elapsed_time(events[-1][6])
     per_stage = {s: statistics.mean(events[i][j].elapsed_time(events[i][j + 1]) for i in range(args.steps))
                  for j, s in enumerate(stages)}
-    if world > 1:
-        t = torch.tensor([total_ms], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = max_over_ranks(total_ms, world, "cuda")
     clocks = clk.summary()
 
     # ---- end to end through the public call with host buffers
@@ -199,10 +213,7 @@ def run_ours(args, rank, world, local_rank):
     e1.record(stream)
     torch.cuda.synchronize()
     e2e_ms = e0.elapsed_time(e1)
-    if world > 1:
-        t = torch.tensor([e2e_ms], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_ms = float(t.item())
+    e2e_ms = max_over_ranks(e2e_ms, world, "cuda")
     if moe.moe_check() != 0:
         raise RuntimeError("device error in the end-to-end run")
 
@@ -230,7 +241,7 @@ def run_ours(args, rank, world, local_rank):
     ms = total_ms / args.steps
     out = {
         "metric": METRIC,
-        "value": world * T * args.steps / (total_ms / 1e3),
+        "value": job_throughput(T, world, args.steps, total_ms),
         "unit": "tokens/s",
         "n_gpus": world,
         "steps": args.steps,
@@ -242,7 +253,7 @@ def run_ours(args, rank, world, local_rank):
         "dtype": w.dtype,
         "data": "synthetic: seeded counter-based generator (x~N(0,1), weights~N(0,1/h)), no dataset",
         "config": workload_config(w),
-        "e2e": {"value": world * T * args.steps / (e2e_ms / 1e3), "unit": "tokens/s",
+        "e2e": {"value": job_throughput(T, world, args.steps, e2e_ms), "unit": "tokens/s",
                 "h2d_bytes_per_step": T * w.h * ds, "d2h_bytes_per_step": T * w.h * ds},
         "gpu_launches": launches_per_step * args.steps,
         "roofline": {"kernel": "grouped SwiGLU FFN (gate/up + down tcgen05 GEMMs)", "bound": "hbm",
@@ -316,7 +327,7 @@ def oracle_sample_time(w, sample_tokens: int, seed: int):
 def run_reference(args):
     from synth import workloads
 
-    w = workloads.ALL[args.workload]
+    w = workloads.ALL.get(args.workload) or workloads.EXTRA[args.workload]
     vals = []
     for i in range(args.warmup + args.steps):
         r = oracle_sample_time(w, args.ref_sample, seed=i)
@@ -339,7 +350,7 @@ def run_reference(args):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=100)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--workload", default="deepseek_v3")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
@@ -367,7 +378,8 @@ def main():
     if rank == 0 and out is not None:
         if world == 1 and not args.no_cpu_baseline:
             from synth import workloads
-            r = oracle_sample_time(workloads.ALL[args.workload], args.cpu_sample, seed=1234)
+            w = workloads.ALL.get(args.workload) or workloads.EXTRA[args.workload]
+            r = oracle_sample_time(w, args.cpu_sample, seed=1234)
             out["cpu_baseline"] = {
                 "value": r["value"], "unit": "tokens/s", "cores": blas_threads(), "kind": "oracle",
                 "sample": (f"routing, layout and index outputs for all tokens ({r['index_s']:.1f} s) plus FFN and "

@@ -60,7 +60,7 @@ class MoeLayerOut(ctypes.Structure):
 
 def _load() -> ctypes.CDLL:
     if not os.path.exists(LIB_PATH):
-        raise ImportError(f"{LIB_PATH} is missing: build it with `python -m expert_dispatch_bias_b300.build`")
+        raise ImportError(f"{LIB_PATH} is missing: build it with `python expert_dispatch_bias_b300/build.py`")
     lib = ctypes.CDLL(LIB_PATH)
     cfgp = POINTER(MoeConfig)
     sig = {

@@ -4,7 +4,8 @@
   synth/libsynth.so                    - the device side of the seeded input generator
   synth/libsynth_host.so               - its host side in C (gcc + OpenMP)
 
-Run as ``python -m expert_dispatch_bias_b300.build`` from the repository root.
+Run as ``python expert_dispatch_bias_b300/build.py [--force]`` (by path: importing the
+package first would load the library that is about to be rebuilt).
 """
 from __future__ import annotations
 

@@ -15,7 +15,7 @@ from synth import workloads
 
 _LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libsynth.so")
 if not os.path.exists(_LIB_PATH):
-    raise ImportError(f"{_LIB_PATH} is missing: build it with `python -m expert_dispatch_bias_b300.build`")
+    raise ImportError(f"{_LIB_PATH} is missing: build it with `python expert_dispatch_bias_b300/build.py`")
 _lib = ctypes.CDLL(_LIB_PATH)
 _lib.synth_fill_normal.restype = ctypes.c_int
 _lib.synth_fill_normal.argtypes = [ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_uint64,

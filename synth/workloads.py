@@ -73,7 +73,13 @@ SWITCH = Workload("switch_base", T=16384, h=768, E=128, K=1, I=3072, dtype="bf16
                   zipf_s=1.1)
 DECODE = tuple(DSV3.replace(name=f"deepseek_v3_decode_T{t}", T=t) for t in (32, 256, 1024))
 
+# The DeepSeek-V3 expert shape (h=7168, I=2048, ~128 rows per expert) with 16
+# experts: 1.4 GB of weights, small enough for a profiler capture that replays a
+# kernel many times, yet larger than the 126 MB L2.
+PROFILE_DSV3 = DSV3.replace(name="deepseek_v3_e16_T256", T=256, E=16, ep_size=16)
+
 ALL = {w.name: w for w in (TINY, MIXTRAL, DSV3, SWITCH) + DECODE}
+EXTRA = {PROFILE_DSV3.name: PROFILE_DSV3}
 
 
 def sigma_in(w: Workload) -> float:
