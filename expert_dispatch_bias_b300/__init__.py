@@ -7,7 +7,7 @@ streams only.
 from ._lib import (  # noqa: F401
     EXPORTS, LIB_PATH, MOE_BF16, MOE_F32, MOE_OP_FFN, MOE_OP_LAYER, MOE_OP_LAYER_HOST, MOE_OP_LAYOUT,
     MOE_SIGMOID, MOE_SOFTMAX, STATUS, MoeConfig, MoeError, MoeLayerOut, MoeLayoutStats, config_from, layer_out,
-    lib, make_config, moe_check, moe_combine, moe_dispatch_layout, moe_grouped_ffn, moe_layer_forward,
+    lib, make_config, moe_check, moe_combine, moe_dispatch_layout, moe_dispatch_layout_static, moe_grouped_ffn, moe_layer_forward,
     moe_layer_forward_host, moe_permute, moe_route, moe_router_logits, moe_rows, moe_validate_config,
     moe_workspace_init, moe_workspace_size,
 )

@@ -28,7 +28,8 @@ STATUS = {
 # Every symbol the header declares (checked by the tests).
 EXPORTS = (
     "moe_status_string", "moe_validate_config", "moe_rows", "moe_workspace_size", "moe_workspace_init",
-    "moe_router_logits", "moe_route", "moe_dispatch_layout", "moe_permute", "moe_grouped_ffn",
+    "moe_router_logits", "moe_route", "moe_dispatch_layout", "moe_dispatch_layout_static", "moe_permute",
+    "moe_grouped_ffn",
     "moe_combine", "moe_layer_forward", "moe_layer_forward_host", "moe_check",
 )
 
@@ -72,6 +73,7 @@ def _load() -> ctypes.CDLL:
         "moe_router_logits": (c_int32, [cfgp, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p]),
         "moe_route": (c_int32, [cfgp, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p]),
         "moe_dispatch_layout": (c_int32, [cfgp] + [c_void_p] * 10 + [c_size_t, c_void_p]),
+        "moe_dispatch_layout_static": (c_int32, [cfgp] + [c_void_p] * 9 + [c_void_p]),
         "moe_permute": (c_int32, [cfgp, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p]),
         "moe_grouped_ffn": (c_int32, [cfgp] + [c_void_p] * 7 + [c_size_t, c_void_p]),
         "moe_combine": (c_int32, [cfgp, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p]),
@@ -162,6 +164,15 @@ def moe_dispatch_layout(cfg, topk_ids, counts, kept, offsets, slot, row_src, n_i
                                    _ptr(slot), _ptr(row_src), _ptr(n_ij), _ptr(rank_bytes), _ptr(stats),
                                    _ptr(workspace), workspace.numel() * workspace.element_size(),
                                    _stream(stream)), "moe_dispatch_layout")
+
+
+def moe_dispatch_layout_static(cfg, topk_ids, counts, kept, offsets, slot, row_src, n_ij, rank_bytes, stats,
+                               stream=None) -> None:
+    """moe_dispatch_layout for callers that cannot allocate: no workspace, the
+    library's fixed scratch array instead (see include/moe.h)."""
+    _check(lib.moe_dispatch_layout_static(ctypes.byref(cfg), _ptr(topk_ids), _ptr(counts), _ptr(kept),
+                                          _ptr(offsets), _ptr(slot), _ptr(row_src), _ptr(n_ij), _ptr(rank_bytes),
+                                          _ptr(stats), _stream(stream)), "moe_dispatch_layout_static")
 
 
 def moe_permute(cfg, x, slot, row_src, xp, stream=None) -> None:

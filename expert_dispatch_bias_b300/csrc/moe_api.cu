@@ -21,6 +21,10 @@
 
 using namespace moe;
 
+// Look-back scratch of moe_dispatch_layout_static: a fixed array, so that the
+// call needs no workspace from its caller.  Zero-initialised at module load.
+static __device__ __align__(256) unsigned char g_layout_static_scratch[MOE_LAYOUT_STATIC_SCRATCH_BYTES];
+
 namespace {
 
 #define MOE_TRY(expr)                    \
@@ -158,6 +162,23 @@ LayerBuffers carve_layer(const moe_config& c, void* ws, bool host_io) {
   b.ydev = host_io ? cv.take<char>((size_t)c.T * c.h * ds) : nullptr;
   b.total = cv.off;
   return b;
+}
+
+// Device address of g_layout_static_scratch on the current device, looked up
+// once per device (host code cannot use the symbol itself as an address).
+moe_status static_layout_scratch(void** out) {
+  static void* addr[64] = {};
+  int dev = 0;
+  CUDA_TRY(cudaGetDevice(&dev));
+  if (dev < 0 || dev >= 64) return MOE_ERR_UNSUPPORTED;
+  if (addr[dev] == nullptr) {
+    void* p = nullptr;
+    CUDA_TRY(cudaGetSymbolAddress(&p, g_layout_static_scratch));
+    if (p == nullptr) return MOE_ERR_CUDA;
+    addr[dev] = p;
+  }
+  *out = addr[dev];
+  return MOE_OK;
 }
 
 size_t ffn_ws_bytes(const moe_config& c) { return align_up((size_t)rows_of(c) * c.I * ds_of(c), 256) + 256; }
@@ -565,6 +586,33 @@ moe_status moe_dispatch_layout(const moe_config* cfg, const int32_t* topk_ids, i
   MOE_TRY(check_ptr(workspace, 256));
   if (workspace_bytes < layout_scratch_bytes((int64_t)cfg->T * cfg->K, cfg->E)) return MOE_ERR_WORKSPACE_TOO_SMALL;
   return launch_layout(*cfg, topk_ids, counts, kept, offsets, slot, row_src, n_ij, rank_bytes, stats, workspace,
+                       as_stream(stream));
+}
+
+moe_status moe_dispatch_layout_static(const moe_config* cfg, const int32_t* topk_ids, int32_t* counts,
+                                      int32_t* kept, int32_t* offsets, int32_t* slot, int32_t* row_src,
+                                      int64_t* n_ij, int64_t* rank_bytes, moe_layout_stats* stats, void* stream) {
+  MOE_TRY(validate(cfg));
+  if (cfg->T > 0) {
+    MOE_TRY(check_ptr(topk_ids, 4));
+    MOE_TRY(check_ptr(slot, 4));
+  }
+  if (rows_of(*cfg) > 0) MOE_TRY(check_ptr(row_src, 4));
+  MOE_TRY(check_ptr(counts, 4));
+  MOE_TRY(check_ptr(kept, 4));
+  MOE_TRY(check_ptr(offsets, 4));
+  MOE_TRY(check_ptr(n_ij, 8));
+  MOE_TRY(check_ptr(rank_bytes, 8));
+  MOE_TRY(check_ptr(stats, 8));
+  const int64_t A = (int64_t)cfg->T * cfg->K;
+  if (layout_scratch_bytes(A, cfg->E) > MOE_LAYOUT_STATIC_SCRATCH_BYTES) return MOE_ERR_WORKSPACE_TOO_SMALL;
+  void* scratch = nullptr;
+  MOE_TRY(static_layout_scratch(&scratch));
+  // the counters and tile flags must start at zero; the per-tile sums are
+  // written before they are read
+  const size_t zero_bytes = 256 + align_up((size_t)layout_num_tiles(A) * 4, 256);
+  CUDA_TRY(cudaMemsetAsync(scratch, 0, zero_bytes, as_stream(stream)));
+  return launch_layout(*cfg, topk_ids, counts, kept, offsets, slot, row_src, n_ij, rank_bytes, stats, scratch,
                        as_stream(stream));
 }
 

@@ -156,6 +156,32 @@ moe_status moe_dispatch_layout(const moe_config* cfg, const int32_t* topk_ids, i
                                int64_t* n_ij, int64_t* rank_bytes, moe_layout_stats* stats,
                                void* workspace, size_t workspace_bytes, void* stream);
 
+/* Largest scratch moe_dispatch_layout_static can use (bytes of device memory
+ * held by every GPU that loads the library, until the process exits). */
+#define MOE_LAYOUT_STATIC_SCRATCH_BYTES ((size_t)1 << 20)
+
+/* moe_dispatch_layout without a workspace, for callers that cannot allocate
+ * device memory and have none to lend: for example code running inside a host
+ * framework that owns all device memory through its own allocator and forbids
+ * direct allocations, or a latency-critical loop that cannot afford the implicit
+ * device synchronisation of cudaMalloc.  The pages have no counterpart of this
+ * call; it exists for such callers only.
+ *
+ * Same arguments, outputs and checks as moe_dispatch_layout, minus the
+ * workspace.  The look-back scratch lives in a fixed device array of
+ * MOE_LAYOUT_STATIC_SCRATCH_BYTES inside the library; a configuration whose
+ * layout needs more (moe_workspace_size(cfg, MOE_OP_LAYOUT) above that limit)
+ * is refused with MOE_ERR_WORKSPACE_TOO_SMALL before any launch.  The call
+ * allocates nothing: no cudaMalloc, no cudaFree.  Its first call on a device
+ * looks up the array's device address for that device (cudaGetSymbolAddress),
+ * so make that first call before any stream capture.  Every call clears the
+ * part of the array that must start at zero.  All calls on a device share the
+ * one array: two calls that overlap on the GPU (different streams, no ordering
+ * between them) race and give wrong results; serialise them. */
+moe_status moe_dispatch_layout_static(const moe_config* cfg, const int32_t* topk_ids, int32_t* counts,
+                                      int32_t* kept, int32_t* offsets, int32_t* slot, int32_t* row_src,
+                                      int64_t* n_ij, int64_t* rank_bytes, moe_layout_stats* stats, void* stream);
+
 /* Permute: the on-device stand-in for the dispatch All-to-All ([overview] glossary
  * "Dispatch"; [compass] "技術原理" step 2).  xp[slot[t,k]] = x[t] for every kept
  * (t,k); with pad, rows whose row_src is -1 are zero-filled; other rows are not
