@@ -13,11 +13,11 @@
 
 #include "moe.h"
 #include "common.cuh"
-#include "ffn_tc.cuh"
 #include "layout.cuh"
 #include "permute_combine.cuh"
 #include "route.cuh"
 #include "simt_gemm.cuh"
+#include "tc_gemm.cuh"
 
 using namespace moe;
 
@@ -184,7 +184,7 @@ moe_status static_layout_scratch(void** out) {
 size_t ffn_ws_bytes(const moe_config& c) { return align_up((size_t)rows_of(c) * c.I * ds_of(c), 256) + 256; }
 
 // ------------------------------------------------------------------ launchers
-moe_status launch_logits(const moe_config& c, const void* x, const void* w_r, const float* off, float* logits,
+moe_status launch_logits_simt(const moe_config& c, const void* x, const void* w_r, const float* off, float* logits,
                          cudaStream_t st) {
   if (c.T == 0) return MOE_OK;
   SimtParams p{};
@@ -416,41 +416,103 @@ moe_status make_tensor_map(CUtensorMap* map, const void* base, uint64_t inner, u
   return r == CUDA_SUCCESS ? MOE_OK : MOE_ERR_CUDA;
 }
 
+// The grouped FFN: gate/up GEMM with the SwiGLU epilogue into the bf16
+// intermediate, then the down GEMM into yp.  256-column tiles (128 gate + 128
+// up units; 256 output columns), a 4-stage ring of 48 KB stages.
+constexpr int kFfnBN = 256, kFfnStages = 4;
+
 moe_status launch_ffn_tc(const moe_config& c, const void* xp, const int32_t* offsets, const int32_t* kept,
                          const void* w13, const void* w2, void* yp, void* inter, cudaStream_t st) {
+  using S = TcShape<kFfnBN, kFfnStages>;
   const int64_t R = rows_of(c);
   const int grid = device_info().sms;
   CUtensorMap a1, b1, a2, b2;
   MOE_TRY(make_tensor_map(&a1, xp, c.h, R, kTcBM));
-  MOE_TRY(make_tensor_map(&b1, w13, c.h, (uint64_t)c.E * 2 * c.I, kTcBN / 2));
+  MOE_TRY(make_tensor_map(&b1, w13, c.h, (uint64_t)c.E * 2 * c.I, kFfnBN / 2));
   MOE_TRY(make_tensor_map(&a2, inter, c.I, R, kTcBM));
-  MOE_TRY(make_tensor_map(&b2, w2, c.I, (uint64_t)c.E * c.h, kTcBN));
+  MOE_TRY(make_tensor_map(&b2, w2, c.I, (uint64_t)c.E * c.h, kFfnBN));
   TcParams p1{};
   p1.offsets = offsets;
   p1.kept = kept;
   p1.E = c.E;
-  p1.n_tiles = (c.I + kTcBN / 2 - 1) / (kTcBN / 2);
+  p1.n_tiles = (c.I + kFfnBN / 2 - 1) / (kFfnBN / 2);
   p1.k_blocks = c.h / kTcBK;
   p1.b_rows = 2LL * c.I;
   p1.up_rows = c.I;
   p1.n_valid = c.I;
-  p1.out = static_cast<__nv_bfloat16*>(inter);
+  p1.out = inter;
   p1.ldo = c.I;
   TcParams p2 = p1;
-  p2.n_tiles = (c.h + kTcBN - 1) / kTcBN;
+  p2.n_tiles = (c.h + kFfnBN - 1) / kFfnBN;
   p2.k_blocks = c.I / kTcBK;
   p2.b_rows = c.h;
   p2.up_rows = 0;
   p2.n_valid = c.h;
-  p2.out = static_cast<__nv_bfloat16*>(yp);
+  p2.out = yp;
   p2.ldo = c.h;
-  CUDA_TRY(allow_smem(ffn_tc_kernel<kTcSwiglu>, kTcDynSmem));
-  CUDA_TRY(allow_smem(ffn_tc_kernel<kTcStore>, kTcDynSmem));
-  ffn_tc_kernel<kTcSwiglu><<<grid, kTcThreads, kTcDynSmem, st>>>(a1, b1, p1);
+  auto k1 = tc_gemm_kernel<kTcSwiglu, kFfnBN, kFfnStages>;
+  auto k2 = tc_gemm_kernel<kTcStore, kFfnBN, kFfnStages>;
+  CUDA_TRY(allow_smem(k1, S::kDynSmem));
+  CUDA_TRY(allow_smem(k2, S::kDynSmem));
+  k1<<<grid, kTcThreads, S::kDynSmem, st>>>(a1, b1, p1);
   CUDA_TRY(cudaGetLastError());
-  ffn_tc_kernel<kTcStore><<<grid, kTcThreads, kTcDynSmem, st>>>(a2, b2, p2);
+  k2<<<grid, kTcThreads, S::kDynSmem, st>>>(a2, b2, p2);
   CUDA_TRY(cudaGetLastError());
   return MOE_OK;
+}
+
+// Router logits of a bf16 layer on the tensor cores: one segment of T rows
+// times the [E, h] router weight, BN columns per tile with BN chosen so that
+// the tiles cover the SMs (BN halves while twice the tiles still fit one wave).
+template <int BN, int STAGES>
+moe_status launch_logits_tc_bn(const moe_config& c, const void* x, const void* w_r, const float* off,
+                               float* logits, cudaStream_t st) {
+  using S = TcShape<BN, STAGES>;
+  CUtensorMap a, b;
+  MOE_TRY(make_tensor_map(&a, x, c.h, c.T, kTcBM));
+  MOE_TRY(make_tensor_map(&b, w_r, c.h, c.E, BN));
+  TcParams p{};
+  p.offsets = nullptr;
+  p.kept = nullptr;
+  p.E = 1;
+  p.dense_rows = c.T;
+  p.n_tiles = (c.E + BN - 1) / BN;
+  p.k_blocks = c.h / kTcBK;
+  p.b_rows = 0;
+  p.n_valid = c.E;
+  p.out = logits;
+  p.ldo = c.E;
+  p.col_bias = off;
+  const int64_t tiles = (int64_t)((c.T + kTcBM - 1) / kTcBM) * p.n_tiles;
+  const int sms = device_info().sms;
+  const int grid = (int)(tiles < sms ? tiles : sms);
+  auto k = tc_gemm_kernel<kTcLogits, BN, STAGES>;
+  CUDA_TRY(allow_smem(k, S::kDynSmem));
+  k<<<grid, kTcThreads, S::kDynSmem, st>>>(a, b, p);
+  CUDA_TRY(cudaGetLastError());
+  return MOE_OK;
+}
+
+int logits_tile_n(const moe_config& c, int sms) {
+  int bn = 16;
+  while (bn < c.E && bn < 256) bn *= 2;
+  const int64_t mblocks = (c.T + kTcBM - 1) / kTcBM;
+  while (bn > 16 && mblocks * ((c.E + bn / 2 - 1) / (bn / 2)) <= sms) bn /= 2;
+  return bn;
+}
+
+moe_status launch_logits(const moe_config& c, const void* x, const void* w_r, const float* off, float* logits,
+                         cudaStream_t st) {
+  if (c.T == 0) return MOE_OK;
+  // float32 layers stay on CUDA cores: a TF32 product would miss their 1e-4 tolerance
+  if (c.dtype == MOE_F32) return launch_logits_simt(c, x, w_r, off, logits, st);
+  switch (logits_tile_n(c, device_info().sms)) {
+    case 16: return launch_logits_tc_bn<16, 8>(c, x, w_r, off, logits, st);
+    case 32: return launch_logits_tc_bn<32, 8>(c, x, w_r, off, logits, st);
+    case 64: return launch_logits_tc_bn<64, 8>(c, x, w_r, off, logits, st);
+    case 128: return launch_logits_tc_bn<128, 6>(c, x, w_r, off, logits, st);
+    default: return launch_logits_tc_bn<256, 4>(c, x, w_r, off, logits, st);
+  }
 }
 
 moe_status launch_ffn(const moe_config& c, const void* xp, const int32_t* offsets, const int32_t* kept,

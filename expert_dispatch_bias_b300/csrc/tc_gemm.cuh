@@ -1,22 +1,32 @@
-// Grouped SwiGLU FFN on the 5th-generation tensor cores (tcgen05, sm_103a).
+// Persistent GEMM on the 5th-generation tensor cores (tcgen05, sm_103a) over
+// ragged row segments: the grouped SwiGLU FFN of the experts and the router
+// logits of the bf16 layer.
 //
-// One persistent CTA per SM walks a static round-robin list of output tiles
-// over the ragged expert segments.  A tile is 128 rows of one expert's segment
-// by 256 accumulator columns:
-//   gate/up GEMM: columns 0..127 hold gate units n0..n0+127 and columns
-//     128..255 the matching up units, so the epilogue forms silu(g) * u for
-//     128 intermediate units without leaving the tile;
-//   down GEMM: 256 output columns.
+// C[m, n] = sum_k A[m, k] * B[n, k], both operands bf16 and K-major, float32
+// accumulation in TMEM.  Rows of A come in segments: expert e owns rows
+// [offsets[e], offsets[e] + kept[e]) of the permuted buffer and multiplies them
+// by its own weight matrix B_e; the router is the one-segment case (all T rows,
+// one B).  One persistent CTA per SM walks a static round-robin list of output
+// tiles of 128 rows by BN accumulator columns, ordered (segment, column tile,
+// m-block) so that the m-blocks sharing a weight tile run on neighbouring SMs
+// at the same time and the second read of that tile hits L2.
+//
+// Epilogues:
+//   SwiGLU  columns 0..BN/2-1 hold gate units n0.. and columns BN/2..BN-1 the
+//           matching up units, so silu(g) * u is formed without leaving the
+//           tile and stored in bf16 (the intermediate activation);
+//   store   bf16 store of the accumulator (the down projection);
+//   logits  float32 store plus an optional per-column offset (the router).
 // Roles (192 threads):
-//   warp 0       one thread issues TMA loads (A rows of the segment, B rows of
-//                the expert's weight) into a 4-stage shared-memory ring;
-//   warp 1       allocates 512 TMEM columns (two 256-column accumulators) and
-//                one thread issues tcgen05.mma (M=128, N=256, K=16, bf16 in,
-//                f32 accumulate), releasing ring stages with tcgen05.commit;
-//   warps 2..5   the epilogue: tcgen05.ld of the accumulator (warp w reads TMEM
-//                lanes 32*(w%4)..+31 = tile rows), SwiGLU or plain, bf16 stores
-//                of the rows inside the segment, then the accumulator is
-//                released for the tile after next.
+//   warp 0       one thread issues TMA loads (128 A rows and BN B rows of one
+//                64-element k-block, 128-byte swizzle) into a STAGES-deep ring;
+//   warp 1       allocates two BN-column TMEM accumulators and one thread
+//                issues tcgen05.mma (M=128, N=BN, K=16), releasing ring stages
+//                with tcgen05.commit;
+//   warps 2..5   drain an accumulator with tcgen05.ld (warp w reads TMEM lanes
+//                32*(w%4)..+31 = tile rows), apply the epilogue, store the rows
+//                inside the segment, and release the accumulator to the tile
+//                after next.
 // Rows past a segment's end are computed (they belong to the next segment or
 // are zero-filled by TMA past the buffer) and masked on store.  Every wait is
 // bounded; a wait that runs out raises the sticky error and the CTA drains
@@ -29,26 +39,35 @@
 
 namespace moe {
 
-constexpr int kTcBM = 128, kTcBN = 256, kTcBK = 64, kTcStages = 4, kTcThreads = 192;
-constexpr uint32_t kTcABytes = kTcBM * kTcBK * 2;   // 16 KB
-constexpr uint32_t kTcBBytes = kTcBN * kTcBK * 2;   // 32 KB
-constexpr uint32_t kTcStageBytes = kTcABytes + kTcBBytes;
-constexpr size_t kTcDynSmem = (size_t)kTcStages * kTcStageBytes + 1024;  // + alignment slack
-constexpr uint32_t kTcTmemCols = 512;
+constexpr int kTcBM = 128, kTcBK = 64, kTcThreads = 192;
 
-enum TcEpilogue { kTcSwiglu = 0, kTcStore = 1 };
+enum TcEpilogue { kTcSwiglu = 0, kTcStore = 1, kTcLogits = 2 };
+
+// Shared-memory and TMEM footprint of a BN-column tile with a STAGES-deep ring.
+template <int BN, int STAGES>
+struct TcShape {
+  static_assert(BN % 16 == 0 && BN >= 16 && BN <= 256, "tcgen05 M=128 needs N % 16 == 0, 16 <= N <= 256");
+  static constexpr uint32_t kABytes = kTcBM * kTcBK * 2;  // 16 KB
+  static constexpr uint32_t kBBytes = BN * kTcBK * 2;     // BN rows of 128 bytes
+  static constexpr uint32_t kStageBytes = kABytes + kBBytes;
+  static constexpr size_t kDynSmem = (size_t)STAGES * kStageBytes + 1024;  // + alignment slack
+  static constexpr uint32_t kTmemCols = 2 * BN < 32 ? 32 : 2 * BN;       // power of two >= 32
+  static constexpr int kChunk = BN < 32 ? BN : 32;                         // columns per tcgen05.ld
+};
 
 struct TcParams {
-  const int32_t* offsets;   // [E+1]
-  const int32_t* kept;      // [E]
-  int E;
-  int n_tiles;              // column tiles per expert
+  const int32_t* offsets;   // [E+1] segment starts, or null: one segment of dense_rows rows at row 0
+  const int32_t* kept;      // [E] segment lengths (ignored when offsets is null)
+  int E;                    // segments (1 when offsets is null)
+  int dense_rows;
+  int n_tiles;              // column tiles per segment
   int k_blocks;             // K / 64
-  int64_t b_rows;           // weight rows per expert (2I or h)
-  int up_rows;              // I (gate/up only)
-  int n_valid;              // output columns per expert (I or h)
-  __nv_bfloat16* out;       // [R, ldo]
+  int64_t b_rows;           // rows of B per segment (2I, h or 0 when all segments share B)
+  int up_rows;              // SwiGLU: row offset of the up half (I)
+  int n_valid;              // output columns (I, h or E)
+  void* out;                // [rows, ldo] bf16 (SwiGLU, store) or float32 (logits)
   int64_t ldo;
+  const float* col_bias;    // logits: per-column offset [n_valid] or null
 };
 
 // ------------------------------------------------------------------ PTX wrappers
@@ -95,8 +114,12 @@ __device__ __forceinline__ void umma_commit(uint64_t* bar) {
 __device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
 __device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
 
-// 32 lanes x 32 consecutive 32-bit columns: thread i gets row (lane base + i).
-__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t* r) {
+// 32 lanes x N consecutive 32-bit columns: thread i gets row (lane base + i).
+template <int N>
+__device__ __forceinline__ void tmem_ld(uint32_t taddr, uint32_t* r);
+
+template <>
+__device__ __forceinline__ void tmem_ld<32>(uint32_t taddr, uint32_t* r) {
   asm volatile(
       "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
       "%15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
@@ -108,41 +131,69 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t* r) {
       : "memory");
 }
 
+template <>
+__device__ __forceinline__ void tmem_ld<16>(uint32_t taddr, uint32_t* r) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
+      "%15}, [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr)
+      : "memory");
+}
+
 __device__ __forceinline__ void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+
+// Packs 2*n float32 values into n bf16 pairs and stores them as 16-byte vectors.
+template <int N>
+__device__ __forceinline__ void store_bf16_row(__nv_bfloat16* dst, const float* v) {
+  uint32_t packed[N / 2];
+#pragma unroll
+  for (int i = 0; i < N / 2; ++i) {
+    const __nv_bfloat162 b = __floats2bfloat162_rn(v[2 * i], v[2 * i + 1]);
+    packed[i] = *reinterpret_cast<const uint32_t*>(&b);
+  }
+  uint4* d = reinterpret_cast<uint4*>(dst);
+#pragma unroll
+  for (int i = 0; i < N / 8; ++i)
+    d[i] = make_uint4(packed[4 * i], packed[4 * i + 1], packed[4 * i + 2], packed[4 * i + 3]);
+}
 
 // ------------------------------------------------------------------ tile schedule
 struct TcTile {
-  int e;        // expert
-  int m0;       // first row (absolute, in the permuted buffer)
-  int m_end;    // end of the expert's segment
+  int e;        // segment (expert)
+  int m0;       // first row (absolute, in A)
+  int m_end;    // end of the segment
   int nt;       // column tile
 };
 
-// mbp[e] = m-blocks of experts < e (exclusive prefix), mbp[E] = total.
-__device__ __forceinline__ TcTile tc_decode(int t, const int32_t* mbp, int E, int n_tiles, const int32_t* offsets,
-                                            const int32_t* kept) {
-  int lo = 0, hi = E - 1;  // last expert whose first tile index is <= t
+// mbp[e] = m-blocks of segments < e (exclusive prefix), mbp[E] = total.
+__device__ __forceinline__ TcTile tc_decode(int t, const int32_t* mbp, const TcParams& p) {
+  int lo = 0, hi = p.E - 1;  // last segment whose first tile index is <= t
   while (lo < hi) {
     const int mid = (lo + hi + 1) >> 1;
-    if (mbp[mid] * n_tiles <= t) lo = mid; else hi = mid - 1;
+    if (mbp[mid] * p.n_tiles <= t) lo = mid; else hi = mid - 1;
   }
   const int e = lo;
-  const int local = t - mbp[e] * n_tiles;
+  const int local = t - mbp[e] * p.n_tiles;
   const int cnt = mbp[e + 1] - mbp[e];
   TcTile r;
   r.e = e;
   r.nt = local / cnt;
   const int mb = local - r.nt * cnt;
-  r.m0 = offsets[e] + mb * kTcBM;
-  r.m_end = offsets[e] + kept[e];
+  const int seg0 = p.offsets ? p.offsets[e] : 0;
+  r.m0 = seg0 + mb * kTcBM;
+  r.m_end = seg0 + (p.offsets ? p.kept[e] : p.dense_rows);
   return r;
 }
 
-template <int EPI>
+template <int EPI, int BN, int STAGES>
 __global__ void __launch_bounds__(kTcThreads, 1)
-    ffn_tc_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_b, TcParams p) {
+    tc_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_b, TcParams p) {
+  using S = TcShape<BN, STAGES>;
+  constexpr int CH = S::kChunk;
   extern __shared__ uint8_t dyn_smem[];
-  __shared__ __align__(8) uint64_t full_bar[kTcStages], empty_bar[kTcStages];
+  __shared__ __align__(8) uint64_t full_bar[STAGES], empty_bar[STAGES];
   __shared__ __align__(8) uint64_t tmem_full[2], tmem_empty[2], drain_bar;
   __shared__ uint32_t tmem_holder;
   __shared__ volatile uint32_t abort_flag;
@@ -152,15 +203,16 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   uint8_t* tiles = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(dyn_smem) + 1023) & ~uintptr_t(1023));
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
-  // ---- per-expert m-block prefix (every CTA computes it from offsets/kept)
-  for (int e = tid; e < p.E; e += kTcThreads) mbp[e] = (p.kept[e] + kTcBM - 1) / kTcBM;
+  // ---- per-segment m-block prefix (every CTA computes it from offsets/kept)
+  for (int e = tid; e < p.E; e += kTcThreads)
+    mbp[e] = ((p.offsets ? p.kept[e] : p.dense_rows) + kTcBM - 1) / kTcBM;
   __syncthreads();
   const int32_t total_mb = block_exclusive_scan(mbp, p.E, scan_scratch);
   if (tid == 0) mbp[p.E] = total_mb;
   const int total_tiles = total_mb * p.n_tiles;
 
   if (tid == 0) {
-    for (int s = 0; s < kTcStages; ++s) {
+    for (int s = 0; s < STAGES; ++s) {
       mbar_init(&full_bar[s], 1);
       mbar_init(&empty_bar[s], 1);
     }
@@ -174,7 +226,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   }
   if (warp == 1) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(&tmem_holder)),
-                 "r"(kTcTmemCols)
+                 "r"(S::kTmemCols)
                  : "memory");
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
   }
@@ -191,7 +243,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       uint32_t armed = 0;  // bit s: stage s was ever armed; its last arm had parity (phase bit at the time)
       uint32_t armed_parity = 0;
       for (int t = blockIdx.x; t < total_tiles && !abort_flag; t += gridDim.x) {
-        const TcTile tl = tc_decode(t, mbp, p.E, p.n_tiles, p.offsets, p.kept);
+        const TcTile tl = tc_decode(t, mbp, p);
         const int64_t brow = (int64_t)tl.e * p.b_rows;
         for (int kb = 0; kb < p.k_blocks; ++kb) {
           if (!mbar_wait(&empty_bar[stage], phase ^ 1u, &abort_flag)) {
@@ -199,22 +251,22 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             raise_error(kErrTimeout);
             break;
           }
-          uint8_t* sa = tiles + (size_t)stage * kTcStageBytes;
-          uint8_t* sb = sa + kTcABytes;
-          mbar_expect_tx(&full_bar[stage], kTcStageBytes);
+          uint8_t* sa = tiles + (size_t)stage * S::kStageBytes;
+          uint8_t* sb = sa + S::kABytes;
+          mbar_expect_tx(&full_bar[stage], S::kStageBytes);
           const int kx = kb * kTcBK;
           tma_load_2d(sa, &map_a, kx, tl.m0, &full_bar[stage]);
           if (EPI == kTcSwiglu) {
-            const int n0 = tl.nt * (kTcBN / 2);
+            const int n0 = tl.nt * (BN / 2);
             tma_load_2d(sb, &map_b, kx, (int)(brow + n0), &full_bar[stage]);
-            tma_load_2d(sb + kTcBBytes / 2, &map_b, kx, (int)(brow + p.up_rows + n0), &full_bar[stage]);
+            tma_load_2d(sb + S::kBBytes / 2, &map_b, kx, (int)(brow + p.up_rows + n0), &full_bar[stage]);
           } else {
-            const int n0 = tl.nt * kTcBN;
+            const int n0 = tl.nt * BN;
             tma_load_2d(sb, &map_b, kx, (int)(brow + n0), &full_bar[stage]);
           }
           armed |= 1u << stage;
           armed_parity = (armed_parity & ~(1u << stage)) | (phase << stage);
-          if (++stage == kTcStages) {
+          if (++stage == STAGES) {
             stage = 0;
             phase ^= 1u;
           }
@@ -223,14 +275,14 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       if (abort_flag) {
         // let the last load armed on every stage land before the CTA's shared
         // memory is released (bounded like every other wait)
-        for (int s = 0; s < kTcStages; ++s)
+        for (int s = 0; s < STAGES; ++s)
           if ((armed >> s) & 1u) mbar_wait(&full_bar[s], (armed_parity >> s) & 1u);
       }
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
-      constexpr uint32_t idesc = umma_idesc_bf16(kTcBM, kTcBN);
+      constexpr uint32_t idesc = umma_idesc_bf16(kTcBM, BN);
       int stage = 0;
       uint32_t phase = 0;
       int acc = 0;
@@ -242,7 +294,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           break;
         }
         tc_fence_after();
-        const uint32_t d_tmem = tmem_base + (uint32_t)(acc * kTcBN);
+        const uint32_t d_tmem = tmem_base + (uint32_t)(acc * BN);
         bool ok = true;
         for (int kb = 0; kb < p.k_blocks; ++kb) {
           if (!mbar_wait(&full_bar[stage], phase, &abort_flag)) {
@@ -252,15 +304,15 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             break;
           }
           tc_fence_after();
-          const uint32_t sa = smem_u32(tiles + (size_t)stage * kTcStageBytes);
-          const uint32_t sb = sa + kTcABytes;
+          const uint32_t sa = smem_u32(tiles + (size_t)stage * S::kStageBytes);
+          const uint32_t sb = sa + S::kABytes;
 #pragma unroll
           for (int k = 0; k < kTcBK / 16; ++k) {
             umma_bf16(d_tmem, umma_desc_sw128(sa + k * 32), umma_desc_sw128(sb + k * 32), idesc,
                       (kb | k) != 0 ? 1u : 0u);
           }
           umma_commit(&empty_bar[stage]);
-          if (++stage == kTcStages) {
+          if (++stage == STAGES) {
             stage = 0;
             phase ^= 1u;
           }
@@ -288,53 +340,69 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         break;
       }
       tc_fence_after();
-      const TcTile tl = tc_decode(t, mbp, p.E, p.n_tiles, p.offsets, p.kept);
+      const TcTile tl = tc_decode(t, mbp, p);
       const int row = tl.m0 + quarter * 32 + lane;
       const bool valid = row < tl.m_end;
-      const uint32_t taddr = tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(acc * kTcBN);
-      __nv_bfloat16* orow = p.out + (int64_t)row * p.ldo;
+      const uint32_t taddr = tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(acc * BN);
       if (EPI == kTcSwiglu) {
-        const int n0 = tl.nt * (kTcBN / 2);
+        const int n0 = tl.nt * (BN / 2);
+        __nv_bfloat16* orow = static_cast<__nv_bfloat16*>(p.out) + (int64_t)row * p.ldo;
 #pragma unroll 1
-        for (int c = 0; c < kTcBN / 2; c += 32) {
-          uint32_t g[32], u[32];
-          tmem_ld32(taddr + c, g);
-          tmem_ld32(taddr + kTcBN / 2 + c, u);
+        for (int c = 0; c < BN / 2; c += CH) {
+          uint32_t g[CH], u[CH];
+          tmem_ld<CH>(taddr + c, g);
+          tmem_ld<CH>(taddr + BN / 2 + c, u);
           tmem_ld_wait();
-          if (valid && n0 + c + 32 <= p.n_valid) {
-            uint32_t packed[16];
+          if (valid && n0 + c + CH <= p.n_valid) {
+            float a[CH];
 #pragma unroll
-            for (int i = 0; i < 16; ++i) {
-              const float g0 = __uint_as_float(g[2 * i]), g1 = __uint_as_float(g[2 * i + 1]);
-              const float a0 = g0 / (1.0f + expf(-g0)) * __uint_as_float(u[2 * i]);
-              const float a1 = g1 / (1.0f + expf(-g1)) * __uint_as_float(u[2 * i + 1]);
-              const __nv_bfloat162 v = __floats2bfloat162_rn(a0, a1);
-              packed[i] = *reinterpret_cast<const uint32_t*>(&v);
+            for (int i = 0; i < CH; ++i) {
+              const float gi = __uint_as_float(g[i]);
+              a[i] = gi / (1.0f + expf(-gi)) * __uint_as_float(u[i]);
             }
-            uint4* dst = reinterpret_cast<uint4*>(orow + n0 + c);
+            store_bf16_row<CH>(orow + n0 + c, a);
+          }
+        }
+      } else if (EPI == kTcStore) {
+        const int n0 = tl.nt * BN;
+        __nv_bfloat16* orow = static_cast<__nv_bfloat16*>(p.out) + (int64_t)row * p.ldo;
+#pragma unroll 1
+        for (int c = 0; c < BN; c += CH) {
+          uint32_t v[CH];
+          tmem_ld<CH>(taddr + c, v);
+          tmem_ld_wait();
+          if (valid && n0 + c + CH <= p.n_valid) {
+            float a[CH];
 #pragma unroll
-            for (int i = 0; i < 4; ++i)
-              dst[i] = make_uint4(packed[4 * i], packed[4 * i + 1], packed[4 * i + 2], packed[4 * i + 3]);
+            for (int i = 0; i < CH; ++i) a[i] = __uint_as_float(v[i]);
+            store_bf16_row<CH>(orow + n0 + c, a);
           }
         }
       } else {
-        const int n0 = tl.nt * kTcBN;
+        const int n0 = tl.nt * BN;
+        float* orow = static_cast<float*>(p.out) + (int64_t)row * p.ldo;
+        const bool vec = (p.ldo % 4) == 0 && (reinterpret_cast<uintptr_t>(p.out) & 15u) == 0;
 #pragma unroll 1
-        for (int c = 0; c < kTcBN; c += 32) {
-          uint32_t v[32];
-          tmem_ld32(taddr + c, v);
+        for (int c = 0; c < BN; c += CH) {
+          uint32_t v[CH];
+          tmem_ld<CH>(taddr + c, v);
           tmem_ld_wait();
-          if (valid && n0 + c + 32 <= p.n_valid) {
-            uint32_t packed[16];
+          if (valid) {
+            float a[CH];
 #pragma unroll
-            for (int i = 0; i < 16; ++i) {
-              const __nv_bfloat162 b = __floats2bfloat162_rn(__uint_as_float(v[2 * i]), __uint_as_float(v[2 * i + 1]));
-              packed[i] = *reinterpret_cast<const uint32_t*>(&b);
+            for (int i = 0; i < CH; ++i) {
+              const int n = n0 + c + i;
+              a[i] = __uint_as_float(v[i]) + ((p.col_bias != nullptr && n < p.n_valid) ? p.col_bias[n] : 0.0f);
             }
-            uint4* dst = reinterpret_cast<uint4*>(orow + n0 + c);
+            if (vec && n0 + c + CH <= p.n_valid) {
+              float4* d = reinterpret_cast<float4*>(orow + n0 + c);
 #pragma unroll
-            for (int i = 0; i < 4; ++i)
-              dst[i] = make_uint4(packed[4 * i], packed[4 * i + 1], packed[4 * i + 2], packed[4 * i + 3]);
+              for (int i = 0; i < CH / 4; ++i) d[i] = make_float4(a[4 * i], a[4 * i + 1], a[4 * i + 2], a[4 * i + 3]);
+            } else {
+#pragma unroll
+              for (int i = 0; i < CH; ++i)
+                if (n0 + c + i < p.n_valid) orow[n0 + c + i] = a[i];
+            }
           }
         }
       }
@@ -351,7 +419,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   __syncthreads();
   if (warp == 1) {
     tc_fence_after();
-    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base), "r"(kTcTmemCols)
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base), "r"(S::kTmemCols)
                  : "memory");
   }
 }

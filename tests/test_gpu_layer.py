@@ -1,8 +1,8 @@
 """The whole layer on the GPU against the oracle.
 
 Index outputs must equal the oracle's; a token may route differently only at a
-near-tie of the oracle's keys (relative gap < 1e-4 at the top-K or group
-boundary), because the GPU's float32 logits differ from the oracle's float64
+near-tie of the oracle's keys (relative gap < 1e-4 between adjacent keys of the
+top K+1, or at the group boundary), because the GPU's float32 logits differ from the oracle's float64
 sums in the last bits.  Such tokens are counted and excluded from the float
 comparison; so are tokens whose kept set differs as a consequence.
 """
@@ -18,6 +18,20 @@ from gpu_helpers import TOL, dev_of, expert_weights, np_of, rel_err
 
 pytestmark = pytest.mark.gpu
 NEAR_TIE = 1e-4
+
+
+def order_margin(keys, allowed, K):
+    """Smallest relative gap between adjacent keys among a token's K+1 largest
+    allowed keys.  The ids are written in descending key order, so two chosen
+    experts whose keys differ by less than the logits' rounding may swap places
+    just as the K-th and (K+1)-th may; the K-th/(K+1)-th gap is the oracle's
+    topk_margin."""
+    out = np.full(keys.shape[0], np.inf)
+    for t in range(keys.shape[0]):
+        v = sorted(keys[t][allowed[t]].astype(np.float64).tolist(), reverse=True)[:K + 1]
+        for a, b in zip(v, v[1:]):
+            out[t] = min(out[t], abs(a - b) / max(abs(a), 1e-30))
+    return out
 
 
 def run_gpu_layer(w, inp):
@@ -51,19 +65,26 @@ def check_layer(w, sample=None, seed=0):
     gids, gslot = np_of(o["topk_ids"]), np_of(o["slot"])
     assert rel_err(np_of(o["logits"]), L, "f32") < 1e-4
     bad = np.nonzero((gids != ids).any(axis=1))[0]
-    margin = np.minimum(oracle.topk_margin(keys, allowed, w.K), oracle.group_margin(keys, w))
+    margin = np.minimum(order_margin(keys, allowed, w.K), oracle.group_margin(keys, w))
     assert np.all(margin[bad] < NEAR_TIE), f"routing differs away from a near-tie at tokens {bad[:8]}"
-    if len(bad) == 0:
-        assert np.array_equal(gslot, lay["slot"])
-        assert np.array_equal(np_of(o["counts"]), lay["counts"])
-        assert np.array_equal(np_of(o["offsets"]), lay["offsets"])
-        assert np.array_equal(np_of(o["n_ij"]).reshape(w.ep_size, w.ep_size), lay["n_ij"])
+    # every index output of the layout is bit-exact against the oracle's layout
+    # of the ids the GPU chose (identical to the oracle's own ids but for near-ties)
+    lay_g = lay if len(bad) == 0 else oracle.dispatch_layout(gids, w)
+    assert np.array_equal(gslot, lay_g["slot"])
+    assert np.array_equal(np_of(o["counts"]), lay_g["counts"])
+    assert np.array_equal(np_of(o["offsets"]), lay_g["offsets"])
+    assert np.array_equal(np_of(o["row_src"])[:lay_g["rows"]], lay_g["row_src"])
+    assert np.array_equal(np_of(o["n_ij"]).reshape(w.ep_size, w.ep_size), lay_g["n_ij"])
     same = np.ones(w.T, dtype=bool)
     same[bad] = False
     same &= ((gslot >= 0) == (lay["slot"] >= 0)).all(axis=1)
-    # the weights are functions of the logits, which differ from the oracle's
-    # float64 sums by float32 accumulation error (~1e-6 relative)
-    np.testing.assert_allclose(np_of(o["topk_w"])[same], wts[same], rtol=1e-5)
+    # The weights are functions of the logits, which differ from the oracle's
+    # float64 sums by the float32 accumulation error dL.  d log w_k is
+    # dL_k - sum_j w_j dL_j (softmax, renormalised or not; sigmoid renormalised)
+    # or (1 - s_k) dL_k (sigmoid), so |dw/w| <= 2 max|dL|, plus the float32
+    # rounding of the weight itself.
+    dL = float(np.abs(np_of(o["logits"]).astype(np.float64) - L).max())
+    np.testing.assert_allclose(np_of(o["topk_w"])[same], wts[same], rtol=2.0 * dL + 2.0 ** -23)
     tokens = np.nonzero(same)[0]
     if sample is not None:
         rng = np.random.default_rng(seed)

@@ -5,6 +5,7 @@ import torch
 
 import expert_dispatch_bias_b300 as moe
 import oracle
+import synth
 from synth import workloads
 
 from gpu_helpers import dev_of, host_inputs, np_of, oracle_routing, rel_err
@@ -24,6 +25,23 @@ def test_router_logits(name):
     moe.moe_router_logits(cfg, dev_of(h["x"]), dev_of(h["w_r"]), off, L)
     assert moe.moe_check() == 0
     # float32 accumulation of exact bf16/f32 products vs float64 sums
+    assert rel_err(np_of(L), ref, "f32") < 1e-4
+
+
+@pytest.mark.parametrize("T,h,E", [(1, 64, 8), (130, 128, 5), (300, 192, 33), (129, 64, 1000), (1200, 128, 256),
+                                   (2500, 64, 1000), (40, 768, 128)])
+@pytest.mark.parametrize("offset", [False, True])
+def test_router_logits_ragged(T, h, E, offset):
+    """bf16 logits on the tensor cores: partial row blocks, expert counts that do
+    not fill a column tile, every column-tile width, with and without offsets."""
+    w = workloads.Workload("logits_case", T=T, h=h, E=E, K=1, I=64, dtype="bf16", score="softmax")
+    x = synth.normal(3, synth.TID_TEST + 20, (T, h), 1.0, "bf16")
+    wr = synth.normal(3, synth.TID_TEST + 21, (E, h), 1.0 / np.sqrt(h), "bf16")
+    off = synth.uniform(3, synth.TID_TEST + 22, E, -2.0, 2.0) if offset else None
+    ref = oracle.router_logits(x, wr, "bf16", off)
+    L = torch.full((T, E), float("nan"), dtype=torch.float32, device="cuda")
+    moe.moe_router_logits(moe.config_from(w), dev_of(x), dev_of(wr), dev_of(off) if offset else None, L)
+    assert moe.moe_check() == 0
     assert rel_err(np_of(L), ref, "f32") < 1e-4
 
 
