@@ -1,0 +1,356 @@
+// Grouped SwiGLU FFN over ragged expert segments on the tcgen05 tensor cores,
+// with the expert's WEIGHT rows as the MMA's M operand and its TOKEN rows as N.
+//
+// An expert of an MoE layer sees few tokens (DeepSeek-V3 at 4096 tokens: ~128
+// rows per expert; decode: 0-32), far fewer than its weight rows.  With tokens
+// as M (128-row tiles) an expert of 130 rows costs two full 128-row MMA
+// blocks; with tokens as N the MMA width only rounds up to 16.  So a tile is
+//   (expert e, feature tile ft, token tile tt)
+// and computes, for two 128-row weight sub-tiles A0 and A1,
+//   D0[f, r] = sum_k A0[f, k] X[r, k],   D1[f, r] = sum_k A1[f, k] X[r, k]
+// over the tile's token rows r:
+//   gate/up (SwiGLU epilogue): A0 = gate rows 128ft.., A1 = the matching up
+//     rows I+128ft..; out[r, 128ft + f] = bf16(silu(D0) * D1) (the intermediate);
+//   down (store epilogue): A0 = rows 256ft.., A1 = rows 256ft+128..;
+//     out[r, 256ft + f] = bf16(D0), out[r, 256ft + 128 + f] = bf16(D1).
+// A token tile holds up to BT rows (128 <= BT <= 256); both MMAs of a k-step
+// take all of them at once (N = rows rounded up to 16).  TMEM holds two
+// 256-column slots: a tile of at most 128 rows keeps D0 and D1 in one slot
+// (columns 0..127 and 128..255 of it), so such tiles alternate slots and one
+// tile's epilogue overlaps the next tile's MMAs; a longer tile keeps D0 in slot
+// 0 and D1 in slot 1.  An expert with more than BT rows is split into equal
+// token tiles.
+//
+// Roles (192 threads), one persistent CTA per SM over a static round-robin of
+// tiles ordered (expert, feature tile, token tile), so the token tiles sharing
+// a weight tile run on neighbouring SMs and the second read hits L2:
+//   warp 0      one thread issues TMA loads: the two 128x64 weight boxes and the
+//               tile's token rows (boxes of 128, 64, 32 and 16 rows) into a
+//               STAGES-deep ring;
+//   warp 1      allocates 512 TMEM columns; one thread issues tcgen05.mma
+//               (M=128, N = the tile's rows rounded up to 16, K=16), two per
+//               k-step, from descriptors computed once per stage;
+//   warps 2..5  drain the accumulators with tcgen05.ld (warp w reads TMEM lanes
+//               32*(w%4).. = 32 features), transpose 32 features x 32 tokens
+//               through shared memory and store 64-byte row pieces.
+// Rows past a tile's end are computed and masked on store.  Every wait is
+// bounded; a wait that runs out raises the sticky error, and the CTA drains its
+// copies and MMAs, frees TMEM and exits.
+#pragma once
+
+#include "tc_gemm.cuh"
+
+namespace moe {
+
+constexpr int kFgThreads = 192;
+constexpr int kFgXsStride = 40;  // bf16 per row of a warp's 32x32 transpose buffer (80 B: conflict-free 16-B reads)
+
+template <int BT, int STAGES>
+struct FgShape {
+  static_assert(BT % 16 == 0 && BT >= 128 && BT <= 256, "token tiles of 128..256 rows");
+  static constexpr uint32_t kWBytes = 128 * kTcBK * 2;            // one 128-row weight box: 16 KB
+  static constexpr uint32_t kStageBytes = 2 * kWBytes + BT * kTcBK * 2;
+  static constexpr size_t kXsBytes = 4 * 32 * kFgXsStride * 2;    // transpose buffers of the 4 epilogue warps
+  static constexpr size_t kDynSmem = (size_t)STAGES * kStageBytes + kXsBytes + 1024;
+};
+
+struct FgParams {
+  const int32_t* offsets;   // [E+1]
+  const int32_t* kept;      // [E]
+  int E;
+  int f_tiles;              // feature tiles per expert: ceil(I/128) (gate/up) or ceil(h/256) (down)
+  int k_blocks;             // reduction length / 64
+  int64_t a_rows;           // weight rows per expert: 2I (gate/up) or h (down)
+  int up_rows;              // gate/up: I
+  int n_valid;              // output features: I or h
+  __nv_bfloat16* out;       // [R, ldo]
+  int64_t ldo;
+};
+
+// Tensor maps of the token rows with boxes of 128, 64, 32 and 16 rows.
+struct FgTokenMaps {
+  CUtensorMap m[4];
+};
+
+struct FgTile {
+  int e, ft;
+  int r0;          // first token row (absolute, in the permuted buffer)
+  int n;           // token rows (1..BT)
+};
+
+// mbp[e] = token tiles of experts < e, mbp[E] = total.
+template <int BT>
+__device__ __forceinline__ FgTile fg_decode(int t, const int32_t* mbp, const FgParams& p) {
+  int lo = 0, hi = p.E - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (mbp[mid] * p.f_tiles <= t) lo = mid; else hi = mid - 1;
+  }
+  const int e = lo;
+  const int local = t - mbp[e] * p.f_tiles;
+  const int cnt = mbp[e + 1] - mbp[e];
+  const int tt = local % cnt;
+  const int kept = p.kept[e];
+  const int base = kept / cnt, rem = kept % cnt;   // equal split: rows differ by at most one
+  FgTile r;
+  r.e = e;
+  r.ft = local / cnt;
+  r.r0 = p.offsets[e] + tt * base + min(tt, rem);
+  r.n = base + (tt < rem ? 1 : 0);
+  return r;
+}
+
+__device__ __forceinline__ uint32_t round16(int n) { return (uint32_t)((n + 15) & ~15); }
+
+// Drains 32 features (this warp's TMEM lanes) x n tokens of one accumulator
+// half at TMEM column `col0`, applies the epilogue and stores the features'
+// 64-byte pieces of each token row r0 + j.
+template <int EPI>
+__device__ __forceinline__ void fg_drain(uint32_t t_lane, uint32_t col0, uint32_t col_up, int n, int r0,
+                                         int feat0, bool feat_ok, const FgParams& p, __nv_bfloat16* xs) {
+  const int lane = threadIdx.x & 31;
+#pragma unroll 1
+  for (int c = 0; c < n; c += 32) {
+    uint32_t v[32];
+    tmem_ld<32>(t_lane + col0 + c, v);
+    if (EPI == kTcSwiglu) {
+      uint32_t u[32];
+      tmem_ld<32>(t_lane + col_up + c, u);
+      tmem_ld_wait();
+#pragma unroll
+      for (int i = 0; i < 32; ++i) {
+        const float g = __uint_as_float(v[i]);
+        xs[i * kFgXsStride + lane] = __float2bfloat16_rn(g / (1.0f + expf(-g)) * __uint_as_float(u[i]));
+      }
+    } else {
+      tmem_ld_wait();
+#pragma unroll
+      for (int i = 0; i < 32; ++i) xs[i * kFgXsStride + lane] = __float2bfloat16_rn(__uint_as_float(v[i]));
+    }
+    __syncwarp();
+    if (feat_ok && c + lane < n) {
+      const uint4* src = reinterpret_cast<const uint4*>(xs + lane * kFgXsStride);
+      uint4* dst = reinterpret_cast<uint4*>(p.out + (int64_t)(r0 + c + lane) * p.ldo + feat0);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) dst[i] = src[i];
+    }
+    __syncwarp();
+  }
+}
+
+template <int EPI, int BT, int STAGES>
+__global__ void __launch_bounds__(kFgThreads, 1)
+    ffn_grouped_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_constant__ FgTokenMaps maps,
+                       FgParams p) {
+  const CUtensorMap* map_x = maps.m;
+  using S = FgShape<BT, STAGES>;
+  extern __shared__ uint8_t dyn_smem[];
+  __shared__ __align__(8) uint64_t full_bar[STAGES], empty_bar[STAGES];
+  __shared__ __align__(8) uint64_t tmem_full[2], tmem_empty[2], drain_bar;
+  __shared__ uint32_t tmem_holder;
+  __shared__ volatile uint32_t abort_flag;
+  __shared__ int32_t mbp[1025];
+  __shared__ int32_t scan_scratch[33];
+
+  uint8_t* ring = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(dyn_smem) + 1023) & ~uintptr_t(1023));
+  __nv_bfloat16* xs_all = reinterpret_cast<__nv_bfloat16*>(ring + (size_t)STAGES * S::kStageBytes);
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+
+  // ---- per-expert token-tile prefix (every CTA computes it from kept)
+  for (int e = tid; e < p.E; e += kFgThreads) mbp[e] = (p.kept[e] + BT - 1) / BT;
+  __syncthreads();
+  const int32_t total_tt = block_exclusive_scan(mbp, p.E, scan_scratch);
+  if (tid == 0) mbp[p.E] = total_tt;
+  const int total_tiles = total_tt * p.f_tiles;
+
+  if (tid == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(&full_bar[s], 1);
+      mbar_init(&empty_bar[s], 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(&tmem_full[a], 1);
+      mbar_init(&tmem_empty[a], 128);
+    }
+    mbar_init(&drain_bar, 1);
+    abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(&tmem_holder)),
+                 "r"(512)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = tmem_holder;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      uint32_t armed = 0, armed_parity = 0;
+      // weight rows of the two 128-row boxes of a tile
+      auto weight_rows = [&](const FgTile& tl, int64_t& a0, int64_t& a1) {
+        if (EPI == kTcSwiglu) {
+          a0 = (int64_t)tl.e * p.a_rows + 128 * tl.ft;
+          a1 = a0 + p.up_rows;
+        } else {
+          a0 = (int64_t)tl.e * p.a_rows + 256 * tl.ft;
+          a1 = a0 + 128;
+        }
+      };
+      for (int t = blockIdx.x; t < total_tiles && !abort_flag; t += gridDim.x) {
+        const FgTile tl = fg_decode<BT>(t, mbp, p);
+        int64_t a0, a1;
+        weight_rows(tl, a0, a1);
+        const uint32_t x_bytes = round16(tl.n) * (uint32_t)(kTcBK * 2);
+        for (int kb = 0; kb < p.k_blocks; ++kb) {
+          if (!mbar_wait(&empty_bar[stage], phase ^ 1u, &abort_flag)) {
+            abort_flag = 1;
+            raise_error(kErrTimeout);
+            break;
+          }
+          uint8_t* sw = ring + (size_t)stage * S::kStageBytes;
+          uint8_t* sx = sw + 2 * S::kWBytes;
+          mbar_expect_tx(&full_bar[stage], 2 * S::kWBytes + x_bytes);
+          const int kx = kb * kTcBK;
+          tma_load_2d(sw, &map_w, kx, (int)a0, &full_bar[stage]);
+          tma_load_2d(sw + S::kWBytes, &map_w, kx, (int)a1, &full_bar[stage]);
+          {
+            // round16(n) rows as boxes of 128 rows, then at most one each of 64, 32 and 16
+            const int n16 = (int)round16(tl.n);
+            int b = 0;
+            for (; b + 128 <= n16; b += 128) tma_load_2d(sx + b * (kTcBK * 2), &map_x[0], kx, tl.r0 + b, &full_bar[stage]);
+            if ((n16 - b) & 64) { tma_load_2d(sx + b * (kTcBK * 2), &map_x[1], kx, tl.r0 + b, &full_bar[stage]); b += 64; }
+            if ((n16 - b) & 32) { tma_load_2d(sx + b * (kTcBK * 2), &map_x[2], kx, tl.r0 + b, &full_bar[stage]); b += 32; }
+            if ((n16 - b) & 16) tma_load_2d(sx + b * (kTcBK * 2), &map_x[3], kx, tl.r0 + b, &full_bar[stage]);
+          }
+          armed |= 1u << stage;
+          armed_parity = (armed_parity & ~(1u << stage)) | (phase << stage);
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+      if (abort_flag) {
+        for (int s = 0; s < STAGES; ++s)
+          if ((armed >> s) & 1u) mbar_wait(&full_bar[s], (armed_parity >> s) & 1u);
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      int slot = 0;              // TMEM slot of the next tile of at most 128 rows
+      uint32_t slot_phase = 0;   // bit s: uses of slot s so far, mod 2
+      for (int t = blockIdx.x; t < total_tiles && !abort_flag; t += gridDim.x) {
+        const FgTile tl = fg_decode<BT>(t, mbp, p);
+        const bool big = tl.n > 128;
+        const uint32_t idesc = umma_idesc_bf16(128, (int)round16(tl.n));
+        // big: D0 = slot 0, D1 = slot 1; else D0, D1 = the two halves of `slot`
+        const int s0 = big ? 0 : slot;
+        const uint32_t c0 = tmem_base + (uint32_t)(s0 * 256), c1 = big ? tmem_base + 256u : c0 + 128u;
+        bool ok = mbar_wait(&tmem_empty[s0], ((slot_phase >> s0) & 1u) ^ 1u, &abort_flag);
+        if (ok && big) ok = mbar_wait(&tmem_empty[1], ((slot_phase >> 1) & 1u) ^ 1u, &abort_flag);
+        if (!ok) {
+          abort_flag = 1;
+          raise_error(kErrTimeout);
+          break;
+        }
+        tc_fence_after();
+        for (int kb = 0; kb < p.k_blocks; ++kb) {
+          if (!mbar_wait(&full_bar[stage], phase, &abort_flag)) {
+            abort_flag = 1;
+            raise_error(kErrTimeout);
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          // descriptors of the stage's operands; a K=16 step advances 32 bytes (2 units)
+          const uint64_t dw0 = umma_desc_sw128(smem_u32(ring + (size_t)stage * S::kStageBytes));
+          const uint64_t dw1 = dw0 + (S::kWBytes >> 4), dx = dw0 + ((2 * S::kWBytes) >> 4);
+#pragma unroll
+          for (int k = 0; k < kTcBK / 16; ++k) {
+            const uint32_t acc = (kb | k) != 0 ? 1u : 0u;
+            umma_bf16(c0, dw0 + 2 * k, dx + 2 * k, idesc, acc);
+            umma_bf16(c1, dw1 + 2 * k, dx + 2 * k, idesc, acc);
+          }
+          umma_commit(&empty_bar[stage]);
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+        if (!ok) break;
+        umma_commit(&tmem_full[s0]);
+        slot_phase ^= 1u << s0;
+        if (big) {
+          umma_commit(&tmem_full[1]);
+          slot_phase ^= 2u;
+        } else {
+          slot ^= 1;
+        }
+      }
+      umma_commit(&drain_bar);
+      mbar_wait(&drain_bar, 0u);
+    }
+  } else {
+    // ------------------------------------------------------------ epilogue (warps 2..5)
+    const int quarter = warp & 3;
+    __nv_bfloat16* xs = xs_all + quarter * 32 * kFgXsStride;
+    const uint32_t t_lane = tmem_base + ((uint32_t)(quarter * 32) << 16);
+    int slot = 0;
+    uint32_t slot_phase = 0;
+    for (int t = blockIdx.x; t < total_tiles; t += gridDim.x) {
+      const FgTile tl = fg_decode<BT>(t, mbp, p);
+      const bool big = tl.n > 128;
+      const int s0 = big ? 0 : slot;
+      const uint32_t c0 = (uint32_t)(s0 * 256), c1 = big ? 256u : c0 + 128u;
+      bool ok = mbar_wait(&tmem_full[s0], (slot_phase >> s0) & 1u, &abort_flag);
+      if (ok && big) ok = mbar_wait(&tmem_full[1], (slot_phase >> 1) & 1u, &abort_flag);
+      if (!ok) {
+        abort_flag = 1;
+        raise_error(kErrTimeout);
+        break;
+      }
+      tc_fence_after();
+      if (EPI == kTcSwiglu) {
+        const int f0 = 128 * tl.ft + 32 * quarter;
+        fg_drain<kTcSwiglu>(t_lane, c0, c1, tl.n, tl.r0, f0, f0 + 32 <= p.n_valid, p, xs);
+      } else {
+        const int f0 = 256 * tl.ft + 32 * quarter;
+        fg_drain<kTcStore>(t_lane, c0, 0, tl.n, tl.r0, f0, f0 + 32 <= p.n_valid, p, xs);
+        if (big) {  // D0 alone fills slot 0: hand it back before draining D1
+          tc_fence_before();
+          mbar_arrive(&tmem_empty[0]);
+        }
+        fg_drain<kTcStore>(t_lane, c1, 0, tl.n, tl.r0, f0 + 128, f0 + 160 <= p.n_valid, p, xs);
+      }
+      tc_fence_before();
+      if (big) {
+        if (EPI == kTcSwiglu) mbar_arrive(&tmem_empty[0]);
+        mbar_arrive(&tmem_empty[1]);
+        slot_phase ^= 3u;
+      } else {
+        mbar_arrive(&tmem_empty[s0]);
+        slot_phase ^= 1u << s0;
+        slot ^= 1;
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base), "r"(512) : "memory");
+  }
+}
+
+}  // namespace moe

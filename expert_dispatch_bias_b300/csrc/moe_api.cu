@@ -18,6 +18,7 @@
 #include "route.cuh"
 #include "simt_gemm.cuh"
 #include "tc_gemm.cuh"
+#include "ffn_grouped.cuh"
 
 using namespace moe;
 
@@ -416,13 +417,19 @@ moe_status make_tensor_map(CUtensorMap* map, const void* base, uint64_t inner, u
   return r == CUDA_SUCCESS ? MOE_OK : MOE_ERR_CUDA;
 }
 
-// The grouped FFN: gate/up GEMM with the SwiGLU epilogue into the bf16
-// intermediate, then the down GEMM into yp.  256-column tiles (128 gate + 128
-// up units; 256 output columns), a 4-stage ring of 48 KB stages.
+// Experts expected to see more rows than this use token rows as the MMA's M
+// operand (tc_gemm.cuh); others use weight rows as M (ffn_grouped.cuh).
+#ifndef MOE_FFN_SWAP_MAX_ROWS
+#define MOE_FFN_SWAP_MAX_ROWS 160
+#endif
+
+// The grouped FFN with token rows as M (128-row m-blocks of an expert's
+// segment) and weight rows as N (256 columns: 128 gate + 128 up units, or 256
+// output features): the tensor-bound regime of many rows per expert.
 constexpr int kFfnBN = 256, kFfnStages = 4;
 
-moe_status launch_ffn_tc(const moe_config& c, const void* xp, const int32_t* offsets, const int32_t* kept,
-                         const void* w13, const void* w2, void* yp, void* inter, cudaStream_t st) {
+moe_status launch_ffn_tokens_m(const moe_config& c, const void* xp, const int32_t* offsets, const int32_t* kept,
+                               const void* w13, const void* w2, void* yp, void* inter, cudaStream_t st) {
   using S = TcShape<kFfnBN, kFfnStages>;
   const int64_t R = rows_of(c);
   const int grid = device_info().sms;
@@ -459,6 +466,71 @@ moe_status launch_ffn_tc(const moe_config& c, const void* xp, const int32_t* off
   k2<<<grid, kTcThreads, S::kDynSmem, st>>>(a2, b2, p2);
   CUDA_TRY(cudaGetLastError());
   return MOE_OK;
+}
+
+// The grouped FFN: gate/up GEMM with the SwiGLU epilogue into the bf16
+// intermediate, then the down GEMM into yp, both with the expert weights as
+// the MMA's M operand and the expert's token rows as N (ffn_grouped.cuh).
+// Token tiles of up to 160 rows in a 4-stage ring of 52 KB stages.
+constexpr int kFgTileRows = 160, kFgStages = 4;
+template <int BT, int STAGES>
+moe_status launch_ffn_grouped(const moe_config& c, const void* xp, const int32_t* offsets, const int32_t* kept,
+                              const void* w13, const void* w2, void* yp, void* inter, cudaStream_t st) {
+  using S = FgShape<BT, STAGES>;
+  const int64_t R = rows_of(c);
+  const int grid = device_info().sms;
+  CUtensorMap w1m, w2m;
+  FgTokenMaps x1, x2;
+  MOE_TRY(make_tensor_map(&w1m, w13, c.h, (uint64_t)c.E * 2 * c.I, 128));
+  MOE_TRY(make_tensor_map(&w2m, w2, c.I, (uint64_t)c.E * c.h, 128));
+  for (int i = 0; i < 4; ++i) {
+    MOE_TRY(make_tensor_map(&x1.m[i], xp, c.h, R, 128u >> i));
+    MOE_TRY(make_tensor_map(&x2.m[i], inter, c.I, R, 128u >> i));
+  }
+  FgParams p1{};
+  p1.offsets = offsets;
+  p1.kept = kept;
+  p1.E = c.E;
+  p1.f_tiles = (c.I + 127) / 128;
+  p1.k_blocks = c.h / kTcBK;
+  p1.a_rows = 2LL * c.I;
+  p1.up_rows = c.I;
+  p1.n_valid = c.I;
+  p1.out = static_cast<__nv_bfloat16*>(inter);
+  p1.ldo = c.I;
+  FgParams p2 = p1;
+  p2.f_tiles = (c.h + 255) / 256;
+  p2.k_blocks = c.I / kTcBK;
+  p2.a_rows = c.h;
+  p2.up_rows = 0;
+  p2.n_valid = c.h;
+  p2.out = static_cast<__nv_bfloat16*>(yp);
+  p2.ldo = c.h;
+  auto k1 = ffn_grouped_kernel<kTcSwiglu, BT, STAGES>;
+  auto k2 = ffn_grouped_kernel<kTcStore, BT, STAGES>;
+  CUDA_TRY(allow_smem(k1, S::kDynSmem));
+  CUDA_TRY(allow_smem(k2, S::kDynSmem));
+  k1<<<grid, kFgThreads, S::kDynSmem, st>>>(w1m, x1, p1);
+  CUDA_TRY(cudaGetLastError());
+  k2<<<grid, kFgThreads, S::kDynSmem, st>>>(w2m, x2, p2);
+  CUDA_TRY(cudaGetLastError());
+  return MOE_OK;
+}
+
+// Rows an expert is expected to receive: the capacity when there is one, else
+// the mean T*K/E.
+int64_t expected_rows_per_expert(const moe_config& c) {
+  if (c.capacity > 0) return c.capacity < c.T ? c.capacity : c.T;
+  return ((int64_t)c.T * c.K + c.E - 1) / c.E;
+}
+
+moe_status launch_ffn_tc(const moe_config& c, const void* xp, const int32_t* offsets, const int32_t* kept,
+                         const void* w13, const void* w2, void* yp, void* inter, cudaStream_t st) {
+  // TMA row coordinates are 32-bit
+  if ((int64_t)c.E * 2 * c.I >= INT32_MAX || (int64_t)c.E * c.h >= INT32_MAX) return MOE_ERR_UNSUPPORTED;
+  if (expected_rows_per_expert(c) > MOE_FFN_SWAP_MAX_ROWS)
+    return launch_ffn_tokens_m(c, xp, offsets, kept, w13, w2, yp, inter, st);
+  return launch_ffn_grouped<kFgTileRows, kFgStages>(c, xp, offsets, kept, w13, w2, yp, inter, st);
 }
 
 // Router logits of a bf16 layer on the tensor cores: one segment of T rows

@@ -78,8 +78,12 @@ DECODE = tuple(DSV3.replace(name=f"deepseek_v3_decode_T{t}", T=t) for t in (32, 
 # kernel many times, yet larger than the 126 MB L2.
 PROFILE_DSV3 = DSV3.replace(name="deepseek_v3_e16_T256", T=256, E=16, ep_size=16)
 
+# The same shape with 32 experts and 512 tokens (2.8 GB of weights): enough
+# tiles for several waves of the grouped FFN on 148 SMs.
+PROFILE_DSV3_E32 = DSV3.replace(name="deepseek_v3_e32_T512", T=512, E=32, ep_size=32)
+
 ALL = {w.name: w for w in (TINY, MIXTRAL, DSV3, SWITCH) + DECODE}
-EXTRA = {PROFILE_DSV3.name: PROFILE_DSV3}
+EXTRA = {w.name: w for w in (PROFILE_DSV3, PROFILE_DSV3_E32)}
 
 
 def sigma_in(w: Workload) -> float:

@@ -78,3 +78,26 @@ def test_ffn_full_size_sampled_experts(name):
     experts = sorted({int(nz[0]), int(nz[len(nz) // 2]), int(nz[-1])})
     err = _run_ffn(w, lay, experts=experts, rows_per_expert=6)
     assert err <= TOL[w.dtype], err
+
+
+# Expert row counts straddling every boundary of the token tiles (sub-blocks of
+# at most 128 rows, MMA widths rounded to 16, tiles of 128, 160 or 256 rows
+# chosen from the mean rows per expert, longer segments split evenly).
+BOUNDARY_COUNTS = {
+    "tile128": [0, 1, 15, 16, 17, 33, 64, 127, 128, 129, 200],
+    "tile160": [0, 1, 15, 16, 17, 127, 128, 129, 144, 160, 161, 255, 256, 257, 300, 511],
+    "tile256": [0, 1, 16, 127, 128, 129, 160, 161, 255, 256, 257, 300, 511, 600, 700],
+}
+
+
+@pytest.mark.parametrize("regime", list(BOUNDARY_COUNTS))
+def test_ffn_tile_boundaries(regime):
+    counts = np.array(BOUNDARY_COUNTS[regime])
+    E = len(counts)
+    w = _small(f"bf16_{regime}", T=int(counts.sum()), h=256, E=E, K=1, I=384, dtype="bf16", score="softmax")
+    rng = np.random.default_rng(11)
+    ids = rng.permutation(np.repeat(np.arange(E, dtype=np.int32), counts)).reshape(-1, 1)
+    lay = oracle.dispatch_layout(ids, w)
+    assert np.array_equal(lay["kept"], counts)
+    err = _run_ffn(w, lay)
+    assert err <= TOL[w.dtype], err
