@@ -358,7 +358,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 #pragma unroll
             for (int i = 0; i < CH; ++i) {
               const float gi = __uint_as_float(g[i]);
-              a[i] = gi / (1.0f + expf(-gi)) * __uint_as_float(u[i]);
+              a[i] = __fdividef(gi, 1.0f + __expf(-gi)) * __uint_as_float(u[i]);  // fast forms, as in ffn_grouped.cuh
             }
             store_bf16_row<CH>(orow + n0 + c, a);
           }
