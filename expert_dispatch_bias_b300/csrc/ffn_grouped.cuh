@@ -102,42 +102,62 @@ __device__ __forceinline__ FgTile fg_decode(int t, const int32_t* mbp, const FgP
 
 __device__ __forceinline__ uint32_t round16(int n) { return (uint32_t)((n + 15) & ~15); }
 
+// Epilogue of one 32-token chunk: v (and u, SwiGLU) hold this warp's 32
+// features x 32 tokens; the bf16 results are transposed through the warp's
+// shared buffer and each lane stores the 64-byte piece of token row r0 + c + lane.
+template <int EPI>
+__device__ __forceinline__ void fg_chunk(const uint32_t* v, const uint32_t* u, int c, int n, int r0, int feat0,
+                                         bool feat_ok, const FgParams& p, __nv_bfloat16* xs) {
+  const int lane = threadIdx.x & 31;
+#pragma unroll
+  for (int i = 0; i < 32; ++i) {
+    const float g = __uint_as_float(v[i]);
+    // silu(g) * u with the fast exponential and division (about 2 ulp of
+    // float32, far below the bf16 rounding of the result); the IEEE forms made
+    // this loop the slowest part of the tile
+    const float a = EPI == kTcSwiglu ? __fdividef(g, 1.0f + __expf(-g)) * __uint_as_float(u[i]) : g;
+    xs[i * kFgXsStride + lane] = __float2bfloat16_rn(a);
+  }
+  __syncwarp();
+  if (feat_ok && c + lane < n) {
+    const uint4* src = reinterpret_cast<const uint4*>(xs + lane * kFgXsStride);
+    uint4* dst = reinterpret_cast<uint4*>(p.out + (int64_t)(r0 + c + lane) * p.ldo + feat0);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) dst[i] = src[i];
+  }
+  __syncwarp();
+}
+
 // Drains 32 features (this warp's TMEM lanes) x n tokens of one accumulator
-// half at TMEM column `col0`, applies the epilogue and stores the features'
-// 64-byte pieces of each token row r0 + j.
+// (columns col0.., and col_up.. for the SwiGLU's up half), two chunks in
+// flight: the next chunk's tcgen05.ld runs while this one is transposed and
+// stored.
 template <int EPI>
 __device__ __forceinline__ void fg_drain(uint32_t t_lane, uint32_t col0, uint32_t col_up, int n, int r0,
                                          int feat0, bool feat_ok, const FgParams& p, __nv_bfloat16* xs) {
-  const int lane = threadIdx.x & 31;
+  constexpr bool kUp = EPI == kTcSwiglu;
+  uint32_t va[32], vb[32], ua[kUp ? 32 : 1], ub[kUp ? 32 : 1];
+  tmem_ld<32>(t_lane + col0, va);
+  if (kUp) tmem_ld<32>(t_lane + col_up, ua);
 #pragma unroll 1
-  for (int c = 0; c < n; c += 32) {
-    uint32_t v[32];
-    tmem_ld<32>(t_lane + col0 + c, v);
-    if (EPI == kTcSwiglu) {
-      uint32_t u[32];
-      tmem_ld<32>(t_lane + col_up + c, u);
-      tmem_ld_wait();
-#pragma unroll
-      for (int i = 0; i < 32; ++i) {
-        // silu(g) * u with the fast exponential and division (about 2 ulp of
-        // float32, far below the bf16 rounding of the result); the IEEE forms
-        // made this loop the slowest part of the tile
-        const float g = __uint_as_float(v[i]);
-        xs[i * kFgXsStride + lane] = __float2bfloat16_rn(__fdividef(g, 1.0f + __expf(-g)) * __uint_as_float(u[i]));
-      }
-    } else {
-      tmem_ld_wait();
-#pragma unroll
-      for (int i = 0; i < 32; ++i) xs[i * kFgXsStride + lane] = __float2bfloat16_rn(__uint_as_float(v[i]));
+  for (int c = 0; c < n; c += 64) {
+    tmem_ld_wait();
+    tmem_regs_ready(va);
+    if (kUp) tmem_regs_ready(ua);
+    if (c + 32 < n) {
+      tmem_ld<32>(t_lane + col0 + c + 32, vb);
+      if (kUp) tmem_ld<32>(t_lane + col_up + c + 32, ub);
     }
-    __syncwarp();
-    if (feat_ok && c + lane < n) {
-      const uint4* src = reinterpret_cast<const uint4*>(xs + lane * kFgXsStride);
-      uint4* dst = reinterpret_cast<uint4*>(p.out + (int64_t)(r0 + c + lane) * p.ldo + feat0);
-#pragma unroll
-      for (int i = 0; i < 4; ++i) dst[i] = src[i];
+    fg_chunk<EPI>(va, ua, c, n, r0, feat0, feat_ok, p, xs);
+    if (c + 32 >= n) break;
+    tmem_ld_wait();
+    tmem_regs_ready(vb);
+    if (kUp) tmem_regs_ready(ub);
+    if (c + 64 < n) {
+      tmem_ld<32>(t_lane + col0 + c + 64, va);
+      if (kUp) tmem_ld<32>(t_lane + col_up + c + 64, ua);
     }
-    __syncwarp();
+    fg_chunk<EPI>(vb, ub, c + 32, n, r0, feat0, feat_ok, p, xs);
   }
 }
 

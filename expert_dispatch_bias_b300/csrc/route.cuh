@@ -33,66 +33,35 @@ __device__ __forceinline__ bool beats(float ka, int a, float kb, int b) {
   return ka > kb || (ka == kb && a < b);
 }
 
-// PER = experts held by each lane (contiguous: lane l holds l*PER .. l*PER+PER-1).
+// Error bounds of the float32 sigmoid keys fl32(1/(1+expf(-x)) + b) against
+// the exact keys fl32(sigmoid(x) + b): expf is within 2 ulp, the add and the
+// division within half an ulp each, so the score is within 4 ulp of 1 (s <= 1)
+// and the key within 4 + 1.2 ulp of 1 (|s + b| <= 1.1); 2^-20 (16 ulp of 1)
+// bounds a key, 2n * 2^-20 a group score summed from n keys.
+constexpr float kKeyErr = 9.5367431640625e-07f;  // 2^-20
+
+struct RouteSel {
+  int my_id;        // lane k < K: the k-th chosen expert
+  float min_gap;    // smallest gap between adjacent keys of the K+1 best allowed
+  float group_gap;  // gap between the last kept and the first dropped group score
+};
+
+// Group limit and top-K on the keys held by this warp (lane l: experts
+// l*PER..), with the gaps that decide whether an approximation of the keys
+// selects as the exact keys would.  kk: this warp's [E] shared row.
 template <int PER>
-__global__ void __launch_bounds__(kRouteWarps * 32) route_kernel(RouteParams p) {
-  extern __shared__ float s_keys[];  // [kRouteWarps][E], used with a group limit
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int t = blockIdx.x * kRouteWarps + warp;
-  if (t >= p.T) return;  // uniform across the warp
+__device__ __forceinline__ RouteSel route_select(const float* key, const RouteParams& p, float* kk) {
   const unsigned full = 0xffffffffu;
-  const float* L = p.logits + (size_t)t * p.E;
+  const int lane = threadIdx.x & 31;
   constexpr int NONE = 0x7fffffff;
-
-  float lg[PER];
-#pragma unroll
-  for (int i = 0; i < PER; ++i) {
-    const int e = lane * PER + i;
-    lg[i] = e < p.E ? L[e] : -INFINITY;
-  }
-
-  // ---- scores (float64)
-  double s[PER];
-  if (!p.sigmoid) {
-    float m = -INFINITY;
-#pragma unroll
-    for (int i = 0; i < PER; ++i) m = fmaxf(m, lg[i]);
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(full, m, o));
-    double z = 0.0;
-#pragma unroll
-    for (int i = 0; i < PER; ++i) {
-      const int e = lane * PER + i;
-      s[i] = e < p.E ? exp((double)lg[i] - (double)m) : 0.0;
-      z += s[i];
-    }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) z += __shfl_xor_sync(full, z, o);
-#pragma unroll
-    for (int i = 0; i < PER; ++i) s[i] = s[i] / z;
-  } else {
-#pragma unroll
-    for (int i = 0; i < PER; ++i) s[i] = 1.0 / (1.0 + exp(-(double)lg[i]));
-  }
-
-  // ---- selection keys
-  float key[PER];
-#pragma unroll
-  for (int i = 0; i < PER; ++i) {
-    const int e = lane * PER + i;
-    if (p.key_is_logit) {
-      key[i] = lg[i];
-    } else {
-      const double b = (p.bias != nullptr && e < p.E) ? (double)p.bias[e] : 0.0;
-      key[i] = (float)(s[i] + b);
-    }
-  }
+  RouteSel r;
+  r.group_gap = INFINITY;
 
   // ---- group limit: bit g of gmask set iff group g is allowed
   uint32_t gmask = full;
   int gsize = p.E;
   if (p.n_groups > 0) {
-    float* kk = s_keys + warp * p.E;
+    __syncwarp();
 #pragma unroll
     for (int i = 0; i < PER; ++i) {
       const int e = lane * PER + i;
@@ -127,18 +96,27 @@ __global__ void __launch_bounds__(kRouteWarps * 32) route_kernel(RouteParams p) 
       const float v = __shfl_sync(full, gscore, g);
       if (beats(v, g, gscore, lane)) ++rank;
     }
-    gmask = __ballot_sync(full, lane < p.n_groups && rank < p.topk_groups);
+    const bool in = lane < p.n_groups;
+    gmask = __ballot_sync(full, in && rank < p.topk_groups);
+    if (p.topk_groups < p.n_groups) {
+      const int la = __ffs(__ballot_sync(full, in && rank == p.topk_groups - 1)) - 1;
+      const int lb = __ffs(__ballot_sync(full, in && rank == p.topk_groups)) - 1;
+      r.group_gap = __shfl_sync(full, gscore, la) - __shfl_sync(full, gscore, lb);
+    }
   }
 
-  // ---- top-K by repeated warp arg-max
+  // ---- top-K by repeated warp arg-max; one more round measures the gap to
+  // the first expert left out
   bool avail[PER];
 #pragma unroll
   for (int i = 0; i < PER; ++i) {
     const int e = lane * PER + i;
     avail[i] = e < p.E && ((gmask >> (e / gsize)) & 1u);
   }
-  int my_id = 0;
-  for (int k = 0; k < p.K; ++k) {
+  r.my_id = 0;
+  r.min_gap = INFINITY;
+  float prev = 0.0f;
+  for (int k = 0; k <= p.K; ++k) {
     float bk = -INFINITY;
     int bi = NONE;
 #pragma unroll
@@ -158,28 +136,112 @@ __global__ void __launch_bounds__(kRouteWarps * 32) route_kernel(RouteParams p) 
         bi = oi;
       }
     }
+    if (bi == NONE) break;  // fewer than K+1 experts allowed
+    if (k > 0) r.min_gap = fminf(r.min_gap, prev - bk);
+    prev = bk;
+    if (k == p.K) break;
 #pragma unroll
     for (int i = 0; i < PER; ++i)
       if (lane * PER + i == bi) avail[i] = false;
-    if (lane == k) my_id = bi;
+    if (lane == k) r.my_id = bi;
   }
+  return r;
+}
 
-  // ---- weights from the unbiased scores of the chosen experts (float64)
-  const int src = lane < p.K ? my_id / PER : 0;
-  const int slot = my_id % PER;
-  double mys = 0.0;
+// PER = experts held by each lane (contiguous: lane l holds l*PER .. l*PER+PER-1).
+template <int PER>
+__global__ void __launch_bounds__(kRouteWarps * 32) route_kernel(RouteParams p) {
+  extern __shared__ float s_keys[];  // [kRouteWarps][E], used with a group limit
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int t = blockIdx.x * kRouteWarps + warp;
+  if (t >= p.T) return;  // uniform across the warp
+  const unsigned full = 0xffffffffu;
+  const float* L = p.logits + (size_t)t * p.E;
+  float* kk = s_keys + warp * p.E;
+
+  float lg[PER];
 #pragma unroll
   for (int i = 0; i < PER; ++i) {
-    const double v = __shfl_sync(full, s[i], src);
-    if (i == slot) mys = v;
+    const int e = lane * PER + i;
+    lg[i] = e < p.E ? L[e] : -INFINITY;
   }
-  if (lane >= p.K) mys = 0.0;
+  float m = -INFINITY;  // largest logit (softmax)
+#pragma unroll
+  for (int i = 0; i < PER; ++i) m = fmaxf(m, lg[i]);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(full, m, o));
+
+  // ---- selection keys.  Exact: the logit itself, or fl32(s + b) from
+  // float64 scores.  The sigmoid keys are first taken in float32 (within
+  // kKeyErr of the exact ones); the selection stands if every gap it depends
+  // on exceeds twice the error, else it is redone on the exact keys.
+  float key[PER];
+  bool exact = true;
+  double z = 0.0;  // softmax denominator (float64)
+  if (p.key_is_logit) {
+#pragma unroll
+    for (int i = 0; i < PER; ++i) key[i] = lg[i];
+  } else if (p.sigmoid) {
+#pragma unroll
+    for (int i = 0; i < PER; ++i) {
+      const int e = lane * PER + i;
+      const float b = (p.bias != nullptr && e < p.E) ? p.bias[e] : 0.0f;
+      key[i] = e < p.E ? __fadd_rn(1.0f / (1.0f + expf(-lg[i])), b) : -INFINITY;
+    }
+    exact = false;
+  } else {
+    double s[PER];
+#pragma unroll
+    for (int i = 0; i < PER; ++i) {
+      const int e = lane * PER + i;
+      s[i] = e < p.E ? exp((double)lg[i] - (double)m) : 0.0;
+      z += s[i];
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) z += __shfl_xor_sync(full, z, o);
+#pragma unroll
+    for (int i = 0; i < PER; ++i) {
+      const int e = lane * PER + i;
+      const double b = (p.bias != nullptr && e < p.E) ? (double)p.bias[e] : 0.0;
+      key[i] = e < p.E ? (float)(s[i] / z + b) : -INFINITY;
+    }
+  }
+
+  RouteSel sel = route_select<PER>(key, p, kk);
+  if (!exact) {
+    const float group_tol = 4.0f * (float)p.group_topn * kKeyErr;  // twice 2n * 2^-20
+    if (!(sel.min_gap > 2.0f * kKeyErr && (p.n_groups == 0 || sel.group_gap > group_tol))) {
+#pragma unroll
+      for (int i = 0; i < PER; ++i) {
+        const int e = lane * PER + i;
+        const double b = (p.bias != nullptr && e < p.E) ? (double)p.bias[e] : 0.0;
+        key[i] = e < p.E ? (float)(1.0 / (1.0 + exp(-(double)lg[i])) + b) : -INFINITY;
+      }
+      sel = route_select<PER>(key, p, kk);
+    }
+  }
+
+  // ---- weights from the unbiased float64 scores of the chosen experts
+  if (!p.sigmoid && !p.renorm && p.key_is_logit) {  // the full denominator is needed
+#pragma unroll
+    for (int i = 0; i < PER; ++i) {
+      const int e = lane * PER + i;
+      z += e < p.E ? exp((double)lg[i] - (double)m) : 0.0;
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) z += __shfl_xor_sync(full, z, o);
+  }
+  double mys = 0.0;
+  if (lane < p.K) {
+    const double x = (double)L[sel.my_id];
+    mys = p.sigmoid ? 1.0 / (1.0 + exp(-x)) : exp(x - (double)m);
+  }
   double tot = mys;
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) tot += __shfl_xor_sync(full, tot, o);
   if (lane < p.K) {
-    const double wk = p.renorm ? (mys / tot) : mys;
-    p.ids[(size_t)t * p.K + lane] = my_id;
+    const double wk = p.renorm ? (mys / tot) : (p.sigmoid ? mys : mys / z);
+    p.ids[(size_t)t * p.K + lane] = sel.my_id;
     p.w[(size_t)t * p.K + lane] = (float)(wk * (double)p.scale);
   }
 }

@@ -144,6 +144,19 @@ __device__ __forceinline__ void tmem_ld<16>(uint32_t taddr, uint32_t* r) {
 
 __device__ __forceinline__ void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 
+// Ties 32 registers written by an earlier tmem_ld to a point after a
+// tmem_ld_wait, so the compiler cannot read them before the load completed.
+__device__ __forceinline__ void tmem_regs_ready(uint32_t* r) {
+  asm volatile(""
+               : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]), "+r"(r[6]), "+r"(r[7]),
+                 "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]), "+r"(r[12]), "+r"(r[13]), "+r"(r[14]),
+                 "+r"(r[15]), "+r"(r[16]), "+r"(r[17]), "+r"(r[18]), "+r"(r[19]), "+r"(r[20]), "+r"(r[21]),
+                 "+r"(r[22]), "+r"(r[23]), "+r"(r[24]), "+r"(r[25]), "+r"(r[26]), "+r"(r[27]), "+r"(r[28]),
+                 "+r"(r[29]), "+r"(r[30]), "+r"(r[31])
+               :
+               : "memory");
+}
+
 // Packs 2*n float32 values into n bf16 pairs and stores them as 16-byte vectors.
 template <int N>
 __device__ __forceinline__ void store_bf16_row(__nv_bfloat16* dst, const float* v) {

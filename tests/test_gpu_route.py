@@ -100,3 +100,26 @@ def test_route_empty_batch():
     moe.moe_route(cfg, torch.empty(0, device="cuda"), None, torch.empty(0, dtype=torch.int32, device="cuda"),
                   torch.empty(0, device="cuda"))
     assert moe.moe_check() == 0
+
+
+@pytest.mark.parametrize("E,K,G", [(64, 6, 8), (256, 8, 8), (40, 3, 0)])
+def test_route_sigmoid_near_ties(E, K, G):
+    """Sigmoid routing whose keys sit a few float32 ulps apart: float32 keys may
+    order such experts differently from the exact ones, and the selection must
+    still equal the oracle's (the near-ties have to be recognised and settled
+    on exact keys)."""
+    rng = np.random.default_rng(E + K)
+    T = 512
+    L = rng.standard_normal((T, E)).astype(np.float32)
+    for t in range(T):                      # clusters of logits 1..40 ulps apart
+        base = rng.choice(E, size=6, replace=False)
+        for j, e in enumerate(base[1:]):
+            L[t, e] = np.nextafter(L[t, base[0]], np.float32(np.inf) if j % 2 else np.float32(-np.inf))
+            for _ in range(int(rng.integers(0, 40))):
+                L[t, e] = np.nextafter(L[t, e], np.float32(np.inf))
+    bias = (rng.integers(-3, 4, size=E) / 64.0).astype(np.float32)
+    bias[rng.choice(E, size=E // 4, replace=False)] += np.float32(2.0 ** -22)
+    kw = dict(K=K, score="sigmoid", scale=2.5)
+    if G:
+        kw.update(n_groups=G, topk_groups=G // 2, group_topn=2)
+    _route_case(kw, L, bias)
