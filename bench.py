@@ -56,7 +56,8 @@ def measured_peaks():
 
 
 def workload_config(w):
-    return {"workload": w.name, "T": w.T, "h": w.h, "E": w.E, "K": w.K, "I": w.I, "score": w.score,
+    return {"workload": w.name, "T": w.T, "h": w.h, "E": w.E, "K": w.K, "I": w.I, "shared_I": w.shared_I,
+            "score": w.score,
             "n_groups": w.n_groups, "topk_groups": w.topk_groups, "capacity": w.capacity, "ep_size": w.ep_size,
             "l2": "inputs larger than L2: every step streams all touched expert weights (GBs) through the 126 MB L2",
             "parallelism": "replicas"}
@@ -156,7 +157,12 @@ def run_ours(args, rank, world, local_rank):
     yp = torch.empty(R, w.h, dtype=dt, device="cuda")
     y = torch.empty(T, w.h, dtype=dt, device="cuda")
     stream = torch.cuda.current_stream()
-    stages = ("logits", "route", "layout", "permute", "ffn", "combine")
+    shared = w.shared_I > 0  # the whole block: routed layer plus the shared expert
+    if shared:
+        ys = torch.empty(T, w.h, dtype=dt, device="cuda")
+        ws_shared = moe.alloc_workspace(cfg, moe.MOE_OP_SHARED)
+    stages = ("logits", "route", "layout", "permute", "ffn") + (("shared",) if shared else ()) + ("combine",)
+    n_ev = len(stages) + 1
 
     def step(ev=None):
         rec = (lambda i: ev[i].record(stream)) if ev is not None else (lambda i: None)
@@ -172,15 +178,20 @@ def run_ours(args, rank, world, local_rank):
         rec(4)
         moe.moe_grouped_ffn(cfg, xp, lay.offsets, lay.kept, inp["w13"], inp["w2"], yp, ws_ffn)
         rec(5)
-        moe.moe_combine(cfg, yp, lay.slot, wts, y)
-        rec(6)
+        if shared:
+            moe.moe_shared_ffn(cfg, inp["x"], inp["w13s"], inp["w2s"], ys, ws_shared)
+            rec(6)
+            moe.moe_combine_add(cfg, yp, lay.slot, wts, ys, y)
+        else:
+            moe.moe_combine(cfg, yp, lay.slot, wts, y)
+        rec(n_ev - 1)
 
     for _ in range(args.warmup):
         step()
     st = moe.moe_check()
     if st != 0:
         raise RuntimeError(f"device error during warm-up: {moe.STATUS[st]}")
-    events = [[torch.cuda.Event(enable_timing=True) for _ in range(7)] for _ in range(args.steps)]
+    events = [[torch.cuda.Event(enable_timing=True) for _ in range(n_ev)] for _ in range(args.steps)]
     if world > 1:
         dist.barrier()
     torch.cuda.synchronize()
@@ -193,7 +204,7 @@ def run_ours(args, rank, world, local_rank):
     st = moe.moe_check()
     if st != 0:
         raise RuntimeError(f"device error in the timed region: {moe.STATUS[st]}")
-    total_ms = events[0][0].elapsed_time(events[-1][6])
+    total_ms = events[0][0].elapsed_time(events[-1][n_ev - 1])
     per_stage = {s: statistics.mean(events[i][j].elapsed_time(events[i][j + 1]) for i in range(args.steps))
                  for j, s in enumerate(stages)}
     total_ms = max_over_ranks(total_ms, world, "cuda")
@@ -202,14 +213,19 @@ def run_ours(args, rank, world, local_rank):
     # ---- end to end through the public call with host buffers.  Two streams
     # take alternate steps, each with its own workspace and pinned buffers, so
     # the host<->device copies of one step overlap the compute of the other.
+    op_host = moe.MOE_OP_BLOCK_HOST if shared else moe.MOE_OP_LAYER_HOST
     lanes = [dict(stream=torch.cuda.Stream(), x=inp["x"].cpu().pin_memory(),
-                  y=torch.empty(T, w.h, dtype=dt).pin_memory(), ws=moe.alloc_workspace(cfg, moe.MOE_OP_LAYER_HOST))
+                  y=torch.empty(T, w.h, dtype=dt).pin_memory(), ws=moe.alloc_workspace(cfg, op_host))
              for _ in range(2)]
 
     def e2e_step(i):
         ln = lanes[i % len(lanes)]
-        moe.moe_layer_forward_host(cfg, ln["x"], inp["w_r"], inp["logit_offset"], inp["sel_bias"], inp["w13"],
-                                   inp["w2"], ln["y"], ln["ws"], stream=ln["stream"])
+        if shared:
+            moe.moe_block_forward_host(cfg, ln["x"], inp["w_r"], inp["logit_offset"], inp["sel_bias"], inp["w13"],
+                                       inp["w2"], inp["w13s"], inp["w2s"], ln["y"], ln["ws"], stream=ln["stream"])
+        else:
+            moe.moe_layer_forward_host(cfg, ln["x"], inp["w_r"], inp["logit_offset"], inp["sel_bias"], inp["w13"],
+                                       inp["w2"], ln["y"], ln["ws"], stream=ln["stream"])
 
     for i in range(max(2, args.warmup)):
         e2e_step(i)
@@ -253,7 +269,7 @@ def run_ours(args, rank, world, local_rank):
     tc_peak = float(peaks["bf16_tflops_sustained"])
     ffn_s = per_stage["ffn"] / 1e3
     ffn_gbs = ffn_bytes / ffn_s / 1e9
-    launches_per_step = 8 + (1 if (w.pad and w.capacity > 0) else 0)
+    launches_per_step = 8 + (1 if (w.pad and w.capacity > 0) else 0) + (2 if shared else 0)
     ms = total_ms / args.steps
     out = {
         "metric": METRIC,
@@ -327,6 +343,7 @@ def oracle_sample_time(w, sample_tokens: int, seed: int):
             if s >= 0:
                 need.setdefault(int(ids[t, k]), []).append(int(s))
     weights = {e: (workloads.host_w13(w, e), workloads.host_w2(w, e)) for e in need}  # input generation
+    shared_w = (workloads.host_w13s(w), workloads.host_w2s(w)) if w.shared_I > 0 else None
     t1 = time.perf_counter()
     xp = np.zeros((lay["rows"], w.h), dtype=x.dtype)
     for e, rows in need.items():
@@ -337,7 +354,11 @@ def oracle_sample_time(w, sample_tokens: int, seed: int):
     yp = np.zeros_like(xp)
     for e, (idx, val) in parts.items():
         yp[idx] = val
-    oracle.combine(yp, lay["slot"], wts, w, tokens=list(tokens))
+    if shared_w is not None:
+        ys = oracle.shared_ffn(x[tokens], shared_w[0], shared_w[1], w)
+        oracle.combine(yp, lay["slot"], wts, w, tokens=list(tokens), rounded=False) + oracle.to_f64(ys, w.dtype)
+    else:
+        oracle.combine(yp, lay["slot"], wts, w, tokens=list(tokens))
     t_sample = time.perf_counter() - t1
     total = t_index + t_sample * (w.T / len(tokens))
     return {"value": w.T / total, "index_s": t_index, "sample_s": t_sample, "tokens": len(tokens)}

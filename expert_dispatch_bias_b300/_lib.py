@@ -18,6 +18,7 @@ LIB_PATH = os.path.join(_HERE, "libmoe.so")
 MOE_F32, MOE_BF16 = 0, 1
 MOE_SOFTMAX, MOE_SIGMOID = 0, 1
 MOE_OP_LAYOUT, MOE_OP_FFN, MOE_OP_LAYER, MOE_OP_LAYER_HOST = 0, 1, 2, 3
+MOE_OP_SHARED, MOE_OP_BLOCK, MOE_OP_BLOCK_HOST = 4, 5, 6
 
 STATUS = {
     0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED", 3: "MOE_ERR_ALIGNMENT",
@@ -31,6 +32,7 @@ EXPORTS = (
     "moe_router_logits", "moe_route", "moe_dispatch_layout", "moe_dispatch_layout_static", "moe_permute",
     "moe_grouped_ffn",
     "moe_combine", "moe_layer_forward", "moe_layer_forward_host", "moe_check",
+    "moe_shared_ffn", "moe_combine_add", "moe_block_forward", "moe_block_forward_host",
 )
 
 
@@ -45,7 +47,7 @@ class MoeConfig(ctypes.Structure):
         ("T", c_int32), ("h", c_int32), ("E", c_int32), ("K", c_int32), ("I", c_int32),
         ("dtype", c_int32), ("score", c_int32), ("renormalize", c_int32), ("scale", c_float),
         ("n_groups", c_int32), ("topk_groups", c_int32), ("group_topn", c_int32),
-        ("capacity", c_int32), ("pad", c_int32), ("ep_size", c_int32),
+        ("capacity", c_int32), ("pad", c_int32), ("ep_size", c_int32), ("shared_I", c_int32),
     ]
 
 
@@ -80,6 +82,10 @@ def _load() -> ctypes.CDLL:
         "moe_layer_forward": (c_int32, [cfgp] + [c_void_p] * 9 + [c_size_t, c_void_p]),
         "moe_layer_forward_host": (c_int32, [cfgp] + [c_void_p] * 8 + [c_size_t, c_void_p]),
         "moe_check": (c_int32, [c_void_p]),
+        "moe_shared_ffn": (c_int32, [cfgp] + [c_void_p] * 5 + [c_size_t, c_void_p]),
+        "moe_combine_add": (c_int32, [cfgp] + [c_void_p] * 6),
+        "moe_block_forward": (c_int32, [cfgp] + [c_void_p] * 11 + [c_size_t, c_void_p]),
+        "moe_block_forward_host": (c_int32, [cfgp] + [c_void_p] * 10 + [c_size_t, c_void_p]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -115,16 +121,17 @@ def _check(status: int, where: str) -> None:
 
 
 def make_config(T, h, E, K, I, dtype="bf16", score="softmax", renormalize=1, scale=1.0, n_groups=0,
-                topk_groups=0, group_topn=0, capacity=0, pad=0, ep_size=1) -> MoeConfig:
+                topk_groups=0, group_topn=0, capacity=0, pad=0, ep_size=1, shared_I=0) -> MoeConfig:
     return MoeConfig(T, h, E, K, I, MOE_F32 if dtype in ("f32", MOE_F32) else MOE_BF16,
                      MOE_SIGMOID if score in ("sigmoid", MOE_SIGMOID) else MOE_SOFTMAX,
-                     int(renormalize), float(scale), n_groups, topk_groups, group_topn, capacity, pad, ep_size)
+                     int(renormalize), float(scale), n_groups, topk_groups, group_topn, capacity, pad, ep_size,
+                     shared_I)
 
 
 def config_from(w) -> MoeConfig:
     """MoeConfig from any object with the layer's attributes (e.g. a synth Workload)."""
     return make_config(w.T, w.h, w.E, w.K, w.I, w.dtype, w.score, w.renormalize, w.scale, w.n_groups,
-                       w.topk_groups, w.group_topn, w.capacity, w.pad, w.ep_size)
+                       w.topk_groups, w.group_topn, w.capacity, w.pad, w.ep_size, getattr(w, "shared_I", 0))
 
 
 # ------------------------------------------------------------------ the C entry points
@@ -205,6 +212,32 @@ def moe_layer_forward_host(cfg, x_host, w_r, logit_offset, sel_bias, w13, w2, y_
                                       _ptr(sel_bias), _ptr(w13), _ptr(w2), _ptr(y_host), _ptr(workspace),
                                       workspace.numel() * workspace.element_size(), _stream(stream)),
            "moe_layer_forward_host")
+
+
+def moe_shared_ffn(cfg, x, w13s, w2s, ys, workspace, stream=None) -> None:
+    _check(lib.moe_shared_ffn(ctypes.byref(cfg), _ptr(x), _ptr(w13s), _ptr(w2s), _ptr(ys), _ptr(workspace),
+                              workspace.numel() * workspace.element_size(), _stream(stream)), "moe_shared_ffn")
+
+
+def moe_combine_add(cfg, yp, slot, topk_w, ys, y, stream=None) -> None:
+    _check(lib.moe_combine_add(ctypes.byref(cfg), _ptr(yp), _ptr(slot), _ptr(topk_w), _ptr(ys), _ptr(y),
+                               _stream(stream)), "moe_combine_add")
+
+
+def moe_block_forward(cfg, x, w_r, logit_offset, sel_bias, w13, w2, w13s, w2s, y, out: Optional[MoeLayerOut],
+                      workspace, stream=None) -> None:
+    _check(lib.moe_block_forward(ctypes.byref(cfg), _ptr(x), _ptr(w_r), _ptr(logit_offset), _ptr(sel_bias),
+                                 _ptr(w13), _ptr(w2), _ptr(w13s), _ptr(w2s), _ptr(y),
+                                 ctypes.byref(out) if out is not None else None, _ptr(workspace),
+                                 workspace.numel() * workspace.element_size(), _stream(stream)), "moe_block_forward")
+
+
+def moe_block_forward_host(cfg, x_host, w_r, logit_offset, sel_bias, w13, w2, w13s, w2s, y_host, workspace,
+                           stream=None) -> None:
+    _check(lib.moe_block_forward_host(ctypes.byref(cfg), _ptr(x_host), _ptr(w_r), _ptr(logit_offset),
+                                      _ptr(sel_bias), _ptr(w13), _ptr(w2), _ptr(w13s), _ptr(w2s), _ptr(y_host),
+                                      _ptr(workspace), workspace.numel() * workspace.element_size(),
+                                      _stream(stream)), "moe_block_forward_host")
 
 
 def moe_check(stream=None) -> int:

@@ -69,6 +69,7 @@ moe_status validate(const moe_config* c) {
   if (c->capacity < 0 || (c->pad != 0 && c->pad != 1)) return MOE_ERR_INVALID_ARG;
   if (c->pad && c->capacity == 0) return MOE_ERR_INVALID_ARG;
   if (c->ep_size < 1 || c->E % c->ep_size != 0) return MOE_ERR_INVALID_ARG;
+  if (c->shared_I < 0 || c->shared_I % 64 != 0) return MOE_ERR_INVALID_ARG;
   if ((int64_t)c->T * c->K >= INT32_MAX || rows_of(*c) >= INT32_MAX) return MOE_ERR_INVALID_ARG;
   // one permuted row must fit a shared-memory buffer of the bulk-copy permute
   if ((int64_t)c->h * ds_of(*c) > 200 * 1024) return MOE_ERR_UNSUPPORTED;
@@ -135,10 +136,14 @@ struct LayerBuffers {
   void* inter;
   void* xdev;
   void* ydev;
+  void* ys;            // shared expert output [T, h] (block)
+  void* shared_ws;     // shared expert intermediate [T, shared_I] (block)
   size_t total;
 };
 
-LayerBuffers carve_layer(const moe_config& c, void* ws, bool host_io) {
+size_t shared_ws_bytes(const moe_config& c) { return align_up((size_t)c.T * c.shared_I * ds_of(c), 256) + 256; }
+
+LayerBuffers carve_layer(const moe_config& c, void* ws, bool host_io, bool block = false) {
   Carver cv(ws);
   LayerBuffers b;
   const int64_t A = (int64_t)c.T * c.K, R = rows_of(c);
@@ -161,6 +166,8 @@ LayerBuffers carve_layer(const moe_config& c, void* ws, bool host_io) {
   b.inter = cv.take<char>((size_t)R * c.I * ds);
   b.xdev = host_io ? cv.take<char>((size_t)c.T * c.h * ds) : nullptr;
   b.ydev = host_io ? cv.take<char>((size_t)c.T * c.h * ds) : nullptr;
+  b.ys = block ? cv.take<char>((size_t)c.T * c.h * ds) : nullptr;
+  b.shared_ws = block ? cv.take<char>(shared_ws_bytes(c)) : nullptr;
   b.total = cv.off;
   return b;
 }
@@ -318,13 +325,14 @@ moe_status launch_permute(const moe_config& c, const void* x, const int32_t* slo
   return MOE_OK;
 }
 
-moe_status launch_combine(const moe_config& c, const void* yp, const int32_t* slot, const float* w, void* y,
-                          cudaStream_t st) {
+moe_status launch_combine(const moe_config& c, const void* yp, const int32_t* slot, const float* w, const void* ys,
+                          void* y, cudaStream_t st) {
   if (c.T == 0) return MOE_OK;
   CombineParams p{};
   p.yp = yp;
   p.slot = slot;
   p.w = w;
+  p.ys = ys;
   p.y = y;
   p.T = c.T;
   p.K = c.K;
@@ -595,9 +603,88 @@ moe_status launch_ffn(const moe_config& c, const void* xp, const int32_t* offset
   return MOE_OK;
 }
 
+// The shared expert: one dense segment of all T tokens through the FFN GEMMs
+// (tokens as M on the tensor cores for bf16, CUDA cores for float32); x is read
+// in place, no permutation.
+moe_status launch_shared_ffn(const moe_config& c, const void* x, const void* w13s, const void* w2s, void* ys,
+                             void* inter, cudaStream_t st) {
+  if (c.T == 0) return MOE_OK;
+  const int Is = c.shared_I;
+  if (c.dtype == MOE_F32) {
+    SimtParams p{};
+    p.A = x;
+    p.lda = c.h;
+    p.B = w13s;
+    p.ldb = c.h;
+    p.b_expert_rows = 2LL * Is;
+    p.up_rows = Is;
+    p.C = inter;
+    p.ldc = Is;
+    p.E = 1;
+    p.M = c.T;
+    p.N = Is;
+    p.K = c.h;
+    const unsigned mblocks = (unsigned)((c.T + kSimtBM - 1) / kSimtBM);
+    simt_gemm_kernel<float, kSimtSwiglu><<<dim3((Is + kSimtBN - 1) / kSimtBN, mblocks), kSimtThreads, 0, st>>>(p);
+    CUDA_TRY(cudaGetLastError());
+    SimtParams q = p;
+    q.A = inter;
+    q.lda = Is;
+    q.B = w2s;
+    q.ldb = Is;
+    q.b_expert_rows = c.h;
+    q.up_rows = 0;
+    q.C = ys;
+    q.ldc = c.h;
+    q.N = c.h;
+    q.K = Is;
+    simt_gemm_kernel<float, kSimtPlain><<<dim3((c.h + kSimtBN - 1) / kSimtBN, mblocks), kSimtThreads, 0, st>>>(q);
+    CUDA_TRY(cudaGetLastError());
+    return MOE_OK;
+  }
+  using S = TcShape<kFfnBN, kFfnStages>;
+  CUtensorMap a1, b1, a2, b2;
+  MOE_TRY(make_tensor_map(&a1, x, c.h, c.T, kTcBM));
+  MOE_TRY(make_tensor_map(&b1, w13s, c.h, 2ull * Is, kFfnBN / 2));
+  MOE_TRY(make_tensor_map(&a2, inter, Is, c.T, kTcBM));
+  MOE_TRY(make_tensor_map(&b2, w2s, Is, c.h, kFfnBN));
+  TcParams p1{};
+  p1.offsets = nullptr;
+  p1.kept = nullptr;
+  p1.E = 1;
+  p1.dense_rows = c.T;
+  p1.n_tiles = (Is + kFfnBN / 2 - 1) / (kFfnBN / 2);
+  p1.k_blocks = c.h / kTcBK;
+  p1.b_rows = 0;
+  p1.up_rows = Is;
+  p1.n_valid = Is;
+  p1.out = inter;
+  p1.ldo = Is;
+  TcParams p2 = p1;
+  p2.n_tiles = (c.h + kFfnBN - 1) / kFfnBN;
+  p2.k_blocks = Is / kTcBK;
+  p2.up_rows = 0;
+  p2.n_valid = c.h;
+  p2.out = ys;
+  p2.ldo = c.h;
+  const int sms = device_info().sms;
+  const int64_t mb = (c.T + kTcBM - 1) / kTcBM;
+  const int g1 = (int)(mb * p1.n_tiles < sms ? mb * p1.n_tiles : sms);
+  const int g2 = (int)(mb * p2.n_tiles < sms ? mb * p2.n_tiles : sms);
+  auto k1 = tc_gemm_kernel<kTcSwiglu, kFfnBN, kFfnStages>;
+  auto k2 = tc_gemm_kernel<kTcStore, kFfnBN, kFfnStages>;
+  CUDA_TRY(allow_smem(k1, S::kDynSmem));
+  CUDA_TRY(allow_smem(k2, S::kDynSmem));
+  k1<<<g1, kTcThreads, S::kDynSmem, st>>>(a1, b1, p1);
+  CUDA_TRY(cudaGetLastError());
+  k2<<<g2, kTcThreads, S::kDynSmem, st>>>(a2, b2, p2);
+  CUDA_TRY(cudaGetLastError());
+  return MOE_OK;
+}
+
 moe_status layer_core(const moe_config& c, const void* x, const void* w_r, const float* logit_offset,
-                      const float* sel_bias, const void* w13, const void* w2, void* y, const moe_layer_out* out,
-                      const LayerBuffers& b, cudaStream_t st) {
+                      const float* sel_bias, const void* w13, const void* w2, const void* w13s, const void* w2s,
+                      void* y, const moe_layer_out* out, const LayerBuffers& b, cudaStream_t st) {
   moe_layer_out o{};
   if (out != nullptr) o = *out;
   float* logits = o.logits ? o.logits : b.logits;
@@ -616,7 +703,9 @@ moe_status layer_core(const moe_config& c, const void* x, const void* w_r, const
   MOE_TRY(launch_layout(c, ids, counts, kept, offsets, slot, row_src, n_ij, rank_bytes, stats, b.layout_ws, st));
   MOE_TRY(launch_permute(c, x, slot, row_src, b.xp, st));
   MOE_TRY(launch_ffn(c, b.xp, offsets, kept, w13, w2, b.yp, b.inter, st));
-  MOE_TRY(launch_combine(c, b.yp, slot, w, y, st));
+  if (b.ys != nullptr)
+    MOE_TRY(launch_shared_ffn(c, x, w13s, w2s, b.ys, static_cast<char*>(b.shared_ws) + 256, st));
+  MOE_TRY(launch_combine(c, b.yp, slot, w, b.ys, y, st));
   return MOE_OK;
 }
 
@@ -667,6 +756,9 @@ moe_status moe_workspace_size(const moe_config* cfg, int32_t op, size_t* bytes) 
     case MOE_OP_FFN: *bytes = ffn_ws_bytes(*cfg); return MOE_OK;
     case MOE_OP_LAYER: *bytes = carve_layer(*cfg, nullptr, false).total; return MOE_OK;
     case MOE_OP_LAYER_HOST: *bytes = carve_layer(*cfg, nullptr, true).total; return MOE_OK;
+    case MOE_OP_SHARED: *bytes = shared_ws_bytes(*cfg); return MOE_OK;
+    case MOE_OP_BLOCK: *bytes = carve_layer(*cfg, nullptr, false, true).total; return MOE_OK;
+    case MOE_OP_BLOCK_HOST: *bytes = carve_layer(*cfg, nullptr, true, true).total; return MOE_OK;
   }
   return MOE_ERR_INVALID_ARG;
 }
@@ -788,7 +880,7 @@ moe_status moe_combine(const moe_config* cfg, const void* yp, const int32_t* slo
     MOE_TRY(check_dtype_ptr(y));
     if (rows_of(*cfg) > 0) MOE_TRY(check_dtype_ptr(yp));
   }
-  return launch_combine(*cfg, yp, slot, topk_w, y, as_stream(stream));
+  return launch_combine(*cfg, yp, slot, topk_w, nullptr, y, as_stream(stream));
 }
 
 moe_status moe_layer_forward(const moe_config* cfg, const void* x, const void* w_r, const float* logit_offset,
@@ -803,7 +895,7 @@ moe_status moe_layer_forward(const moe_config* cfg, const void* x, const void* w
   MOE_TRY(check_ptr(workspace, 256));
   const LayerBuffers b = carve_layer(*cfg, workspace, false);
   if (workspace_bytes < b.total) return MOE_ERR_WORKSPACE_TOO_SMALL;
-  return layer_core(*cfg, x, w_r, logit_offset, sel_bias, w13, w2, y, out, b, as_stream(stream));
+  return layer_core(*cfg, x, w_r, logit_offset, sel_bias, w13, w2, nullptr, nullptr, y, out, b, as_stream(stream));
 }
 
 moe_status moe_layer_forward_host(const moe_config* cfg, const void* x_host, const void* w_r,
@@ -818,7 +910,75 @@ moe_status moe_layer_forward_host(const moe_config* cfg, const void* x_host, con
   const cudaStream_t st = as_stream(stream);
   const size_t bytes = (size_t)cfg->T * cfg->h * ds_of(*cfg);
   if (bytes > 0) CUDA_TRY(cudaMemcpyAsync(b.xdev, x_host, bytes, cudaMemcpyHostToDevice, st));
-  MOE_TRY(layer_core(*cfg, b.xdev, w_r, logit_offset, sel_bias, w13, w2, b.ydev, nullptr, b, st));
+  MOE_TRY(layer_core(*cfg, b.xdev, w_r, logit_offset, sel_bias, w13, w2, nullptr, nullptr, b.ydev, nullptr, b, st));
+  if (bytes > 0) CUDA_TRY(cudaMemcpyAsync(y_host, b.ydev, bytes, cudaMemcpyDeviceToHost, st));
+  return MOE_OK;
+}
+
+moe_status moe_shared_ffn(const moe_config* cfg, const void* x, const void* w13s, const void* w2s, void* ys,
+                          void* workspace, size_t workspace_bytes, void* stream) {
+  MOE_TRY(validate(cfg));
+  if (cfg->shared_I <= 0) return MOE_ERR_INVALID_ARG;
+  if (cfg->T > 0) {
+    MOE_TRY(check_dtype_ptr(x));
+    MOE_TRY(check_dtype_ptr(ys));
+  }
+  MOE_TRY(check_dtype_ptr(w13s));
+  MOE_TRY(check_dtype_ptr(w2s));
+  MOE_TRY(check_ptr(workspace, 256));
+  if (workspace_bytes < shared_ws_bytes(*cfg)) return MOE_ERR_WORKSPACE_TOO_SMALL;
+  return launch_shared_ffn(*cfg, x, w13s, w2s, ys, static_cast<char*>(workspace) + 256, as_stream(stream));
+}
+
+moe_status moe_combine_add(const moe_config* cfg, const void* yp, const int32_t* slot, const float* topk_w,
+                           const void* ys, void* y, void* stream) {
+  MOE_TRY(validate(cfg));
+  if (cfg->T > 0) {
+    MOE_TRY(check_ptr(slot, 4));
+    MOE_TRY(check_ptr(topk_w, 4));
+    MOE_TRY(check_dtype_ptr(ys));
+    MOE_TRY(check_dtype_ptr(y));
+    if (rows_of(*cfg) > 0) MOE_TRY(check_dtype_ptr(yp));
+  }
+  return launch_combine(*cfg, yp, slot, topk_w, ys, y, as_stream(stream));
+}
+
+moe_status moe_block_forward(const moe_config* cfg, const void* x, const void* w_r, const float* logit_offset,
+                             const float* sel_bias, const void* w13, const void* w2, const void* w13s,
+                             const void* w2s, void* y, const moe_layer_out* out, void* workspace,
+                             size_t workspace_bytes, void* stream) {
+  MOE_TRY(validate(cfg));
+  if (cfg->shared_I <= 0) return MOE_ERR_INVALID_ARG;
+  if (cfg->T > 0) {
+    MOE_TRY(check_dtype_ptr(x));
+    MOE_TRY(check_dtype_ptr(y));
+  }
+  MOE_TRY(check_layer_ptrs(*cfg, x, w_r, logit_offset, sel_bias, w13, w2));
+  MOE_TRY(check_dtype_ptr(w13s));
+  MOE_TRY(check_dtype_ptr(w2s));
+  MOE_TRY(check_ptr(workspace, 256));
+  const LayerBuffers b = carve_layer(*cfg, workspace, false, true);
+  if (workspace_bytes < b.total) return MOE_ERR_WORKSPACE_TOO_SMALL;
+  return layer_core(*cfg, x, w_r, logit_offset, sel_bias, w13, w2, w13s, w2s, y, out, b, as_stream(stream));
+}
+
+moe_status moe_block_forward_host(const moe_config* cfg, const void* x_host, const void* w_r,
+                                  const float* logit_offset, const float* sel_bias, const void* w13,
+                                  const void* w2, const void* w13s, const void* w2s, void* y_host,
+                                  void* workspace, size_t workspace_bytes, void* stream) {
+  MOE_TRY(validate(cfg));
+  if (cfg->shared_I <= 0) return MOE_ERR_INVALID_ARG;
+  if (cfg->T > 0 && (x_host == nullptr || y_host == nullptr)) return MOE_ERR_INVALID_ARG;
+  MOE_TRY(check_layer_ptrs(*cfg, x_host, w_r, logit_offset, sel_bias, w13, w2));
+  MOE_TRY(check_dtype_ptr(w13s));
+  MOE_TRY(check_dtype_ptr(w2s));
+  MOE_TRY(check_ptr(workspace, 256));
+  const LayerBuffers b = carve_layer(*cfg, workspace, true, true);
+  if (workspace_bytes < b.total) return MOE_ERR_WORKSPACE_TOO_SMALL;
+  const cudaStream_t st = as_stream(stream);
+  const size_t bytes = (size_t)cfg->T * cfg->h * ds_of(*cfg);
+  if (bytes > 0) CUDA_TRY(cudaMemcpyAsync(b.xdev, x_host, bytes, cudaMemcpyHostToDevice, st));
+  MOE_TRY(layer_core(*cfg, b.xdev, w_r, logit_offset, sel_bias, w13, w2, w13s, w2s, b.ydev, nullptr, b, st));
   if (bytes > 0) CUDA_TRY(cudaMemcpyAsync(y_host, b.ydev, bytes, cudaMemcpyDeviceToHost, st));
   return MOE_OK;
 }

@@ -98,6 +98,7 @@ struct CombineParams {
   const void* yp;        // [R, h]
   const int32_t* slot;   // [T, K]
   const float* w;        // [T, K]
+  const void* ys;        // [T, h] per-token term added first (shared expert), or null
   void* y;               // [T, h]
   int64_t T;
   int K, h;
@@ -168,8 +169,12 @@ __global__ void __launch_bounds__(256) combine_kernel(CombineParams p) {
       for (int k = 0; k < KMAX; ++k)
         if (k < p.K && s[k] >= 0) v[k] = __ldg(src + (int64_t)s[k] * vecs + c);
       float acc[V];
+      if (p.ys != nullptr) {
+        unpack(__ldg(static_cast<const uint4*>(p.ys) + t * vecs + c), acc, T());
+      } else {
 #pragma unroll
-      for (int i = 0; i < V; ++i) acc[i] = 0.0f;
+        for (int i = 0; i < V; ++i) acc[i] = 0.0f;
+      }
 #pragma unroll
       for (int k = 0; k < KMAX; ++k) {
         if (k < p.K && s[k] >= 0) {

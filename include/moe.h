@@ -21,8 +21,8 @@
  *
  * Conventions shared by every call:
  *  - All tensor pointers are DEVICE pointers owned by the caller, except the
- *    two host buffers of moe_layer_forward_host.  The library never allocates
- *    or frees memory.
+ *    two host buffers of moe_layer_forward_host and moe_block_forward_host.
+ *    The library never allocates or frees memory.
  *  - Every call is asynchronous on `stream` (a cudaStream_t; NULL = legacy
  *    default stream) and does not synchronise the host, except moe_check.
  *  - Arguments are validated on the host before any launch; a bad argument
@@ -57,7 +57,15 @@ typedef enum {
 
 typedef enum { MOE_F32 = 0, MOE_BF16 = 1 } moe_dtype;
 typedef enum { MOE_SOFTMAX = 0, MOE_SIGMOID = 1 } moe_score;
-typedef enum { MOE_OP_LAYOUT = 0, MOE_OP_FFN = 1, MOE_OP_LAYER = 2, MOE_OP_LAYER_HOST = 3 } moe_op;
+typedef enum {
+  MOE_OP_LAYOUT = 0,      /* moe_dispatch_layout */
+  MOE_OP_FFN = 1,         /* moe_grouped_ffn */
+  MOE_OP_LAYER = 2,       /* moe_layer_forward */
+  MOE_OP_LAYER_HOST = 3,  /* moe_layer_forward_host */
+  MOE_OP_SHARED = 4,      /* moe_shared_ffn */
+  MOE_OP_BLOCK = 5,       /* moe_block_forward */
+  MOE_OP_BLOCK_HOST = 6   /* moe_block_forward_host */
+} moe_op;
 
 /* Layer description.  Limits: T >= 0; h % 64 == 0; I % 64 == 0; 1 <= E <= 1024;
  * 1 <= K <= min(E, 16); T*K and the permuted row count below 2^31. */
@@ -77,6 +85,7 @@ typedef struct moe_config {
   int32_t capacity;     /* 0: dropless; > 0: per-expert cap, overflow dropped in token order */
   int32_t pad;          /* 1 (needs capacity > 0): expert e owns rows [e*cap, (e+1)*cap) */
   int32_t ep_size;      /* virtual expert-parallel group size N_EP; E % ep_size == 0 */
+  int32_t shared_I;     /* intermediate size of the shared expert (0: none); % 64 == 0 */
 } moe_config;
 
 /* Scalar results of moe_dispatch_layout (device memory, 32 bytes). */
@@ -113,8 +122,8 @@ moe_status moe_validate_config(const moe_config* cfg);
 /* Rows R of the permuted buffers: T*K, or E*capacity when pad is set. */
 moe_status moe_rows(const moe_config* cfg, int64_t* rows);
 
-/* Workspace bytes needed by `op` (host only).  MOE_OP_LAYOUT: moe_dispatch_layout;
- * MOE_OP_FFN: moe_grouped_ffn; MOE_OP_LAYER / MOE_OP_LAYER_HOST: the whole layer. */
+/* Workspace bytes needed by `op`, one of moe_op (the call named beside each;
+ * host only). */
 moe_status moe_workspace_size(const moe_config* cfg, int32_t op, size_t* bytes);
 
 /* Zero-fills a workspace.  Must run once after allocation, and again after a call
@@ -225,6 +234,40 @@ moe_status moe_layer_forward(const moe_config* cfg, const void* x, const void* w
 moe_status moe_layer_forward_host(const moe_config* cfg, const void* x_host, const void* w_r,
                                   const float* logit_offset, const float* sel_bias,
                                   const void* w13, const void* w2, void* y_host,
+                                  void* workspace, size_t workspace_bytes, void* stream);
+
+/* Shared expert ([overview] glossary "Expert": DeepSeek-V3 has 256 routed
+ * experts plus 1 shared expert per layer, "MoE 路由机制是什么"): a SwiGLU FFN that
+ * every token passes through, outside the routing.  For every token t:
+ * a = silu(x[t] Wg^T) * (x[t] Wu^T), stored in dtype; ys[t] = a Wd^T, stored in
+ * dtype; float32 accumulation.  Needs cfg->shared_I > 0.
+ * x [T,h] dtype; w13s [2*shared_I, h] dtype (gate rows then up rows); w2s
+ * [h, shared_I] dtype; ys [T,h] dtype; workspace >= moe_workspace_size(MOE_OP_SHARED). */
+moe_status moe_shared_ffn(const moe_config* cfg, const void* x, const void* w13s, const void* w2s, void* ys,
+                          void* workspace, size_t workspace_bytes, void* stream);
+
+/* moe_combine plus a per-token term: y[t] = ys[t] + sum_{k: slot[t,k] >= 0}
+ * topk_w[t,k] * yp[slot[t,k]], float32 sum (ys first, then k order), stored in
+ * dtype.  ys [T,h] dtype (the shared expert's output); other arguments as in
+ * moe_combine. */
+moe_status moe_combine_add(const moe_config* cfg, const void* yp, const int32_t* slot, const float* topk_w,
+                           const void* ys, void* y, void* stream);
+
+/* The DeepSeek-V3 MoE block: moe_layer_forward's routed experts plus the shared
+ * expert, y = ys + routed combine (moe_shared_ffn, then moe_combine_add in place
+ * of moe_combine).  Needs cfg->shared_I > 0.  Arguments as in moe_layer_forward
+ * plus w13s, w2s as in moe_shared_ffn; workspace >= moe_workspace_size(MOE_OP_BLOCK). */
+moe_status moe_block_forward(const moe_config* cfg, const void* x, const void* w_r, const float* logit_offset,
+                             const float* sel_bias, const void* w13, const void* w2, const void* w13s,
+                             const void* w2s, void* y, const moe_layer_out* out, void* workspace,
+                             size_t workspace_bytes, void* stream);
+
+/* moe_block_forward with HOST activations, as moe_layer_forward_host:
+ * x_host [T,h] in, y_host [T,h] out, copies on `stream`;
+ * workspace >= moe_workspace_size(MOE_OP_BLOCK_HOST). */
+moe_status moe_block_forward_host(const moe_config* cfg, const void* x_host, const void* w_r,
+                                  const float* logit_offset, const float* sel_bias, const void* w13,
+                                  const void* w2, const void* w13s, const void* w2s, void* y_host,
                                   void* workspace, size_t workspace_bytes, void* stream);
 
 /* Synchronises `stream`, then reports and clears the sticky device error word of

@@ -417,6 +417,41 @@ def layer_forward(x, w_r, get_w13, get_w2, cfg, sel_bias=None, logit_offset=None
             "layout": lay, "xp": xp, "yp": yp, "y": y, "y_exact": y_exact}
 
 
+# ----------------------------------------------------------------- shared expert, whole block
+
+
+def shared_ffn(x: np.ndarray, w13s: np.ndarray, w2s: np.ndarray, cfg, rounded: bool = True) -> np.ndarray:
+    """The shared expert: an expert that every token passes through, outside the
+    routing ([overview] glossary "Expert" and "MoE 路由机制是什么": DeepSeek-V3
+    has 256 routed experts plus 1 shared expert per layer).  The same SwiGLU
+    FFN as a routed expert (expert_ffn) on all T rows of x, with intermediate
+    size ``cfg.shared_I``; output stored in the data type (READING: like a
+    routed expert's output rows)."""
+    return expert_ffn(x, w13s, w2s, cfg.dtype, cfg.shared_I, rounded)
+
+
+def combine_add(yp: np.ndarray, slot: np.ndarray, w: np.ndarray, ys: np.ndarray, cfg, tokens=None,
+                rounded: bool = True) -> np.ndarray:
+    """y[t] = ys[t] + the routed combine of token t (float64, stored in the data
+    type): the block's output is the shared expert's plus the routed experts'
+    weighted sum."""
+    tok = list(range(slot.shape[0])) if tokens is None else list(tokens)
+    Ys = ys if ys.dtype == np.float64 else to_f64(ys, cfg.dtype)
+    out = combine(yp, slot, w, cfg, tokens=tok, rounded=False) + Ys[tok]
+    return store(out, cfg.dtype) if rounded else out
+
+
+def block_forward(x, w_r, get_w13, get_w2, w13s, w2s, cfg, sel_bias=None, logit_offset=None) -> dict:
+    """The DeepSeek-V3 MoE block: the routed layer (layer_forward) plus the shared
+    expert, y = shared(x) + sum_k w_k expert_k(x)."""
+    r = layer_forward(x, w_r, get_w13, get_w2, cfg, sel_bias, logit_offset)
+    ys = shared_ffn(x, w13s, w2s, cfg)
+    r["ys"] = ys
+    r["y"] = combine_add(r["yp"], r["layout"]["slot"], r["w"], ys, cfg)
+    r["y_exact"] = combine_add(r["yp"], r["layout"]["slot"], r["w"], ys, cfg, rounded=False)
+    return r
+
+
 # ----------------------------------------------------------------- page formulas
 
 

@@ -46,6 +46,8 @@ TID_W13 = 3        # expert gate/up weights [E, 2I, h]
 TID_W2 = 4         # expert down weights [E, h, I]
 TID_SEL_BIAS = 5   # per-expert selection bias [E]
 TID_ZIPF = 6       # surrogate logits used to fit the Zipf logit offsets
+TID_W13S = 7       # shared expert gate/up weights [2*shared_I, h]
+TID_W2S = 8        # shared expert down weights [h, shared_I]
 TID_TEST = 100     # first id free for test-only tensors
 
 

@@ -56,6 +56,10 @@ def layer_inputs(w: workloads.Workload, device="cuda", weights=True) -> dict:
     if weights:
         out["w13"] = fill_normal(torch.empty(w.E, 2 * w.I, w.h, dtype=dt, device=device), w.seed, synth.TID_W13, s)
         out["w2"] = fill_normal(torch.empty(w.E, w.h, w.I, dtype=dt, device=device), w.seed, synth.TID_W2, s)
+    if weights and w.shared_I > 0:
+        out["w13s"] = fill_normal(torch.empty(2 * w.shared_I, w.h, dtype=dt, device=device), w.seed,
+                                  synth.TID_W13S, s)
+        out["w2s"] = fill_normal(torch.empty(w.h, w.shared_I, dtype=dt, device=device), w.seed, synth.TID_W2S, s)
     if w.sel_bias is not None:
         out["sel_bias"] = fill_uniform(torch.empty(w.E, dtype=torch.float32, device=device), w.seed,
                                        synth.TID_SEL_BIAS, *w.sel_bias)

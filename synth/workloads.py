@@ -9,7 +9,8 @@ layer uses one; seed 0.  "N" is the Irwin-Hall normal of :mod:`synth`.
 Layouts (row-major, the last index contiguous):
   x [T, h]; router weight [E, h]; w13 [E, 2I, h] (gate rows 0..I-1 then up rows
   I..2I-1 of each expert); w2 [E, h, I]; selection bias [E] float32; logit
-  offset [E] float32.
+  offset [E] float32; shared expert w13s [2*shared_I, h], w2s [h, shared_I]
+  ~ N(0, 1/h).
 """
 from __future__ import annotations
 
@@ -42,6 +43,7 @@ class Workload:
     ep_size: int = 1
     sel_bias: Optional[Tuple[float, float]] = None   # U(lo, hi) selection bias
     zipf_s: Optional[float] = None                   # Zipf logit offsets
+    shared_I: int = 0                                # shared expert intermediate (0: none)
     seed: int = 0
 
     @property
@@ -72,6 +74,9 @@ SWITCH = Workload("switch_base", T=16384, h=768, E=128, K=1, I=3072, dtype="bf16
                   score="softmax", capacity=capacity_for(1.0, 16384, 1, 128), ep_size=16,
                   zipf_s=1.1)
 DECODE = tuple(DSV3.replace(name=f"deepseek_v3_decode_T{t}", T=t) for t in (32, 256, 1024))
+# The whole DeepSeek-V3 MoE block: the routed layer plus its one shared expert
+# (intermediate 2048, like a routed expert), which every token passes through.
+DSV3_BLOCK = DSV3.replace(name="deepseek_v3_block", shared_I=2048)
 
 # The DeepSeek-V3 expert shape (h=7168, I=2048, ~128 rows per expert) with 16
 # experts: 1.4 GB of weights, small enough for a profiler capture that replays a
@@ -83,7 +88,7 @@ PROFILE_DSV3 = DSV3.replace(name="deepseek_v3_e16_T256", T=256, E=16, ep_size=16
 PROFILE_DSV3_E32 = DSV3.replace(name="deepseek_v3_e32_T512", T=512, E=32, ep_size=32)
 
 ALL = {w.name: w for w in (TINY, MIXTRAL, DSV3, SWITCH) + DECODE}
-EXTRA = {w.name: w for w in (PROFILE_DSV3, PROFILE_DSV3_E32)}
+EXTRA = {w.name: w for w in (PROFILE_DSV3, PROFILE_DSV3_E32, DSV3_BLOCK)}
 
 
 def sigma_in(w: Workload) -> float:
@@ -114,6 +119,16 @@ def host_w2(w: Workload, e: int) -> np.ndarray:
     """Expert e's down weight [h, I]."""
     n = w.h * w.I
     return synth.normal(w.seed, synth.TID_W2, (w.h, w.I), sigma_in(w), w.dtype, start=e * n)
+
+
+def host_w13s(w: Workload) -> np.ndarray:
+    """The shared expert's gate/up weight [2*shared_I, h]."""
+    return synth.normal(w.seed, synth.TID_W13S, (2 * w.shared_I, w.h), sigma_in(w), w.dtype)
+
+
+def host_w2s(w: Workload) -> np.ndarray:
+    """The shared expert's down weight [h, shared_I]."""
+    return synth.normal(w.seed, synth.TID_W2S, (w.h, w.shared_I), sigma_in(w), w.dtype)
 
 
 def host_sel_bias(w: Workload) -> Optional[np.ndarray]:

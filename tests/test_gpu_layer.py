@@ -47,9 +47,14 @@ def run_gpu_layer(w, inp):
              rank_bytes=torch.empty(2 * N, dtype=torch.int64, device="cuda"),
              stats=torch.empty(4, dtype=torch.int64, device="cuda"))
     y = torch.empty(T, w.h, dtype=dt, device="cuda")
-    ws = moe.alloc_workspace(cfg, moe.MOE_OP_LAYER)
-    moe.moe_layer_forward(cfg, inp["x"], inp["w_r"], inp["logit_offset"], inp["sel_bias"], inp["w13"], inp["w2"],
-                          y, moe.layer_out(**o), ws)
+    if w.shared_I > 0:  # the whole block: routed experts plus the shared expert
+        ws = moe.alloc_workspace(cfg, moe.MOE_OP_BLOCK)
+        moe.moe_block_forward(cfg, inp["x"], inp["w_r"], inp["logit_offset"], inp["sel_bias"], inp["w13"],
+                              inp["w2"], inp["w13s"], inp["w2s"], y, moe.layer_out(**o), ws)
+    else:
+        ws = moe.alloc_workspace(cfg, moe.MOE_OP_LAYER)
+        moe.moe_layer_forward(cfg, inp["x"], inp["w_r"], inp["logit_offset"], inp["sel_bias"], inp["w13"],
+                              inp["w2"], y, moe.layer_out(**o), ws)
     assert moe.moe_check() == 0
     return y, o, ws
 
@@ -109,6 +114,9 @@ def check_layer(w, sample=None, seed=0):
     for e, (idx, val) in parts.items():
         yp[idx] = val
     ref = oracle.combine(yp, lay["slot"], wts, w, tokens=list(tokens), rounded=False)
+    if w.shared_I > 0:
+        ys = oracle.shared_ffn(h["x"][tokens], np_of(inp["w13s"]), np_of(inp["w2s"]), w)
+        ref = ref + oracle.to_f64(ys, w.dtype)
     err = rel_err(np_of(y)[tokens], ref, w.dtype)
     assert err <= TOL[w.dtype], err
     return len(bad), len(tokens), err

@@ -379,3 +379,71 @@ def test_bf16_rounding(golden_dir):
     v = np.array(vals, dtype=np.float64)
     assert oracle.round_to_bf16_bits(v).tolist() == bits
     assert synth.f32_to_bf16_bits(v.astype(np.float32)).tolist() == bits
+
+
+# --------------------------------------------------------------------------- shared expert
+def _block_case(dtype, seed=4):
+    cfg = _cfg(T=20, h=16, E=4, K=2, I=12, dtype=dtype, score="sigmoid", scale=2.5, ep_size=2, shared_I=12)
+    rng = np.random.default_rng(seed)
+    mk = (lambda shape, s: synth.f32_to_bf16_bits((rng.normal(size=shape) * s).astype(np.float32))) \
+        if dtype == "bf16" else (lambda shape, s: (rng.normal(size=shape) * s).astype(np.float32))
+    x = mk((cfg.T, cfg.h), 1.0)
+    wr = mk((cfg.E, cfg.h), 0.3)
+    W13 = [mk((2 * cfg.I, cfg.h), 0.3) for _ in range(cfg.E)]
+    W2 = [mk((cfg.h, cfg.I), 0.3) for _ in range(cfg.E)]
+    w13s, w2s = mk((2 * cfg.shared_I, cfg.h), 0.3), mk((cfg.h, cfg.shared_I), 0.3)
+    return cfg, x, wr, W13, W2, w13s, w2s
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_block_is_routed_layer_plus_an_always_chosen_expert(dtype):
+    """The shared expert is an expert that every token uses outside the routing:
+    the block must equal a routed layer with one more expert, forced into every
+    token's choice with weight 1 (computed through the layout, permutation,
+    grouped FFN and combine of the routed path)."""
+    cfg, x, wr, W13, W2, w13s, w2s = _block_case(dtype)
+    blk = oracle.block_forward(x, wr, lambda e: W13[e], lambda e: W2[e], w13s, w2s, cfg)
+    aug = cfg.replace(E=cfg.E + 1, K=cfg.K + 1, ep_size=1)
+    ids = np.concatenate([blk["ids"], np.full((cfg.T, 1), cfg.E, dtype=np.int32)], axis=1)
+    w = np.concatenate([blk["w"], np.ones((cfg.T, 1), dtype=np.float32)], axis=1)
+    lay = oracle.dispatch_layout(ids, aug)
+    xp = oracle.permute(x, lay["row_src"])
+    W13a, W2a = W13 + [w13s], W2 + [w2s]
+    parts = oracle.grouped_ffn(xp, lay["offsets"], lay["kept"], lambda e: W13a[e], lambda e: W2a[e], aug)
+    yp = np.zeros_like(xp)
+    for e, (idx, rows) in parts.items():
+        yp[idx] = rows
+    y_aug = oracle.combine(yp, lay["slot"], w, aug, rounded=False)
+    np.testing.assert_allclose(blk["y_exact"], y_aug, rtol=1e-12, atol=1e-12)
+
+
+def test_block_without_shared_weights_is_the_layer():
+    """Zero shared-expert weights leave exactly the routed layer; doubling the
+    down weight (an exact scaling in bf16) doubles the shared expert's output."""
+    cfg, x, wr, W13, W2, w13s, w2s = _block_case("bf16", seed=5)
+    lay = oracle.layer_forward(x, wr, lambda e: W13[e], lambda e: W2[e], cfg)
+    zero = np.zeros_like(w13s)
+    blk = oracle.block_forward(x, wr, lambda e: W13[e], lambda e: W2[e], zero, np.zeros_like(w2s), cfg)
+    assert np.array_equal(blk["y"], lay["y"])
+    ys1 = oracle.to_f64(oracle.shared_ffn(x, w13s, w2s, cfg), "bf16")
+    w2x2 = synth.f32_to_bf16_bits((oracle.to_f64(w2s, "bf16") * 2).astype(np.float32))
+    ys2 = oracle.to_f64(oracle.shared_ffn(x, w13s, w2x2, cfg), "bf16")
+    assert np.array_equal(ys2, 2 * ys1)
+
+
+def test_shared_ffn_library_other_width():
+    """A shared expert narrower than the routed ones (shared_I != I) against
+    torch's linear and silu in float64, intermediate rounded to bf16."""
+    cfg, x, wr, W13, W2, _, _ = _block_case("bf16", seed=6)
+    cfg = cfg.replace(shared_I=8)
+    rng = np.random.default_rng(7)
+    w13s = synth.f32_to_bf16_bits((rng.normal(size=(16, cfg.h)) * 0.3).astype(np.float32))
+    w2s = synth.f32_to_bf16_bits((rng.normal(size=(cfg.h, 8)) * 0.3).astype(np.float32))
+    F = torch.nn.functional
+    X = torch.from_numpy(oracle.to_f64(x, "bf16"))
+    A = torch.from_numpy(oracle.to_f64(w13s, "bf16"))
+    a = F.silu(F.linear(X, A[:8])) * F.linear(X, A[8:])
+    a = torch.from_numpy(oracle.to_f64(oracle.round_to_bf16_bits(a.numpy()), "bf16"))
+    ref = F.linear(a, torch.from_numpy(oracle.to_f64(w2s, "bf16"))).numpy()
+    got = oracle.shared_ffn(x, w13s, w2s, cfg, rounded=False)
+    np.testing.assert_allclose(got, ref, rtol=1e-12, atol=1e-12)
