@@ -452,6 +452,102 @@ def block_forward(x, w_r, get_w13, get_w2, w13s, w2s, cfg, sel_bias=None, logit_
     return r
 
 
+# ----------------------------------------------------------------- EPLB: logical and physical experts
+
+
+def eplb_plan(counts, n_ep: int, n_redundant: int) -> dict:
+    """Replica plan of expert-parallel load balancing ([overview] glossary
+    "Logical expert", "Physical expert / Replica", "Redundant expert": a placement
+    algorithm copies hot logical experts so that E + R physical experts, a
+    multiple of the number of GPUs, flatten the load; e.g. 256 logical + 32
+    redundant = 288 physical).
+
+    READINGS (the pages define the terms and the goal, not the algorithm):
+    * replication: each of the R redundant replicas goes, one at a time, to the
+      logical expert with the largest load per replica counts[e] / n_rep[e]
+      (exact integer comparison; ties to the lower id);
+    * a logical expert's load is split over its replicas as evenly as possible:
+      replica r gets counts // n + (1 if r < counts % n else 0);
+    * placement: replicas in order of load descending (ties: lower logical id,
+      then lower replica index) each go to the rank with the least load among
+      ranks with a free slot (ties to the lower rank); every rank has
+      (E + R) / N_EP slots, and physical ids are rank-major in placement order.
+    Returns n_rep [E], rep_offsets [E+1], rep_phys [E+R] (physical ids of the
+    replicas of e at rep_offsets[e]..), phys_to_log [E+R], rank_load [N_EP]."""
+    counts = [int(c) for c in counts]
+    E = len(counts)
+    P = E + n_redundant
+    assert P % n_ep == 0
+    n_rep = [1] * E
+    for _ in range(n_redundant):
+        best = 0
+        for e in range(1, E):
+            if counts[e] * n_rep[best] > counts[best] * n_rep[e]:
+                best = e
+        n_rep[best] += 1
+    reps = []
+    for e in range(E):
+        q, m = divmod(counts[e], n_rep[e])
+        for r in range(n_rep[e]):
+            reps.append((q + (1 if r < m else 0), e, r))
+    reps.sort(key=lambda x: (-x[0], x[1], x[2]))
+    slots = P // n_ep
+    load, fill = [0] * n_ep, [0] * n_ep
+    phys = {}
+    for ld, e, r in reps:
+        j = min((j for j in range(n_ep) if fill[j] < slots), key=lambda j: (load[j], j))
+        phys[(e, r)] = j * slots + fill[j]
+        fill[j] += 1
+        load[j] += ld
+    rep_offsets = np.zeros(E + 1, dtype=np.int32)
+    rep_offsets[1:] = np.cumsum(n_rep)
+    rep_phys = np.zeros(P, dtype=np.int32)
+    phys_to_log = np.zeros(P, dtype=np.int32)
+    for e in range(E):
+        for r in range(n_rep[e]):
+            rep_phys[rep_offsets[e] + r] = phys[(e, r)]
+            phys_to_log[phys[(e, r)]] = e
+    return {"n_rep": np.array(n_rep, dtype=np.int32), "rep_offsets": rep_offsets, "rep_phys": rep_phys,
+            "phys_to_log": phys_to_log, "rank_load": np.array(load, dtype=np.int64)}
+
+
+def eplb_map(ids: np.ndarray, rep_offsets: np.ndarray, rep_phys: np.ndarray) -> np.ndarray:
+    """Physical expert of every routed (t, k): replica t mod n_rep(e) of its
+    logical expert e (READING: the pages leave the choice among replicas open;
+    token order round robin keeps it a function of (t, e) alone)."""
+    T, K = ids.shape
+    out = np.zeros_like(ids)
+    for t in range(T):
+        for k in range(K):
+            e = int(ids[t, k])
+            n = int(rep_offsets[e + 1] - rep_offsets[e])
+            out[t, k] = rep_phys[rep_offsets[e] + t % n]
+    return out
+
+
+def layer_forward_eplb(x, w_r, get_w13, get_w2, cfg, plan: dict, sel_bias=None, logit_offset=None) -> dict:
+    """The routed layer with replicas: route over the E logical experts, map each
+    choice to a physical replica, then layout (capacity, n_ij and Balancedness
+    over the E + R physical experts on their ranks), permutation, the FFN of
+    each replica with its logical expert's weights, and combine."""
+    L = router_logits(x, w_r, cfg.dtype, logit_offset)
+    ids, w, keys, allowed = route(L, cfg, sel_bias)
+    pids = eplb_map(ids, plan["rep_offsets"], plan["rep_phys"])
+    pcfg = cfg.replace(E=cfg.E + cfg.n_redundant, n_groups=0, topk_groups=0, group_topn=0)
+    lay = dispatch_layout(pids, pcfg)
+    xp = permute(x, lay["row_src"])
+    p2l = plan["phys_to_log"]
+    parts = grouped_ffn(xp, lay["offsets"], lay["kept"], lambda p: get_w13(int(p2l[p])),
+                        lambda p: get_w2(int(p2l[p])), pcfg, rounded=False)
+    yp_exact = np.zeros(xp.shape, dtype=np.float64)
+    for e, (idx, rows) in parts.items():
+        yp_exact[idx] = rows
+    yp = store(yp_exact, cfg.dtype)
+    return {"logits": L, "ids": ids, "phys_ids": pids, "w": w, "keys": keys, "allowed": allowed, "layout": lay,
+            "yp": yp, "y": combine(yp, lay["slot"], w, pcfg), "y_exact": combine(yp, lay["slot"], w, pcfg,
+                                                                                   rounded=False)}
+
+
 # ----------------------------------------------------------------- page formulas
 
 

@@ -44,6 +44,7 @@ class Workload:
     sel_bias: Optional[Tuple[float, float]] = None   # U(lo, hi) selection bias
     zipf_s: Optional[float] = None                   # Zipf logit offsets
     shared_I: int = 0                                # shared expert intermediate (0: none)
+    n_redundant: int = 0                             # EPLB: physical replicas beyond E (0: none)
     seed: int = 0
 
     @property

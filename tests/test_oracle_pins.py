@@ -447,3 +447,83 @@ def test_shared_ffn_library_other_width():
     ref = F.linear(a, torch.from_numpy(oracle.to_f64(w2s, "bf16"))).numpy()
     got = oracle.shared_ffn(x, w13s, w2s, cfg, rounded=False)
     np.testing.assert_allclose(got, ref, rtol=1e-12, atol=1e-12)
+
+
+# --------------------------------------------------------------------------- EPLB
+def test_eplb_hand_worked(golden_dir):
+    g = {}
+    for line in open(os.path.join(golden_dir, "eplb_case.txt")):
+        line = line.split("#")[0].split()
+        if line:
+            g[line[0]] = [int(v) for v in line[1:]]
+    p = oracle.eplb_plan(g["counts"], g["n_ep"][0], g["n_redundant"][0])
+    for k in ("n_rep", "rep_offsets", "rep_phys", "phys_to_log", "rank_load"):
+        assert p[k].tolist() == g[k], k
+
+
+@pytest.mark.parametrize("seed", range(6))
+def test_eplb_replication_minimises_the_largest_replica_load(seed):
+    """Brute force over every way to hand out R redundant replicas: the plan's
+    largest load per replica (count / replicas) is the smallest possible."""
+    from fractions import Fraction
+    rng = np.random.default_rng(seed)
+    E, R = int(rng.integers(2, 5)), int(rng.integers(1, 5))
+    counts = rng.integers(0, 40, size=E).tolist()
+    p = oracle.eplb_plan(counts, 1, R)
+    worst = max(Fraction(c, n) for c, n in zip(counts, p["n_rep"].tolist()))
+    best = min(max(Fraction(c, n) for c, n in zip(counts, reps))
+               for reps in itertools.product(range(1, R + 2), repeat=E) if sum(reps) == E + R)
+    assert worst == best
+    assert p["n_rep"].sum() == E + R and p["n_rep"].min() >= 1
+
+
+@pytest.mark.parametrize("seed", range(6))
+def test_eplb_placement(seed):
+    """Every replica on exactly one slot, every rank full, loads adding up; the
+    most loaded rank within one replica's load of the best possible placement
+    (brute force over all placements with equal slot counts)."""
+    rng = np.random.default_rng(100 + seed)
+    n_ep = int(rng.integers(2, 4))
+    E = n_ep * int(rng.integers(1, 3))
+    R = n_ep * int(rng.integers(0, 2))
+    counts = rng.integers(0, 30, size=E).tolist()
+    p = oracle.eplb_plan(counts, n_ep, R)
+    P, slots = E + R, (E + R) // n_ep
+    assert sorted(p["rep_phys"].tolist()) == list(range(P))
+    assert p["rank_load"].sum() == sum(counts)
+    loads = []
+    for e in range(E):
+        n = int(p["n_rep"][e])
+        q, m = divmod(counts[e], n)
+        loads += [q + (1 if r < m else 0) for r in range(n)]
+    best = min(max(sum(loads[i] for i in range(P) if assign[i] == j) for j in range(n_ep))
+               for assign in itertools.product(range(n_ep), repeat=P)
+               if all(assign.count(j) == slots for j in range(n_ep)))
+    assert p["rank_load"].max() <= best + max(loads)
+
+
+def test_eplb_map_round_robin_and_layer_unchanged():
+    """Tokens of a logical expert go to its replicas by t mod n_rep; relabelling
+    experts into replicas leaves a dropless layer's output bit for bit as it
+    was, while the per-rank load becomes more even."""
+    cfg = _cfg(T=48, h=16, E=8, K=1, I=8, dtype="f32", score="softmax", ep_size=4, n_redundant=4)
+    rng = np.random.default_rng(9)
+    x = rng.normal(size=(cfg.T, cfg.h)).astype(np.float32)
+    wr = rng.normal(size=(cfg.E, cfg.h)).astype(np.float32) * 0.2
+    off = np.zeros(cfg.E, dtype=np.float32)
+    off[0] = 2.0                                     # expert 0 takes most tokens
+    W13 = [rng.normal(size=(2 * cfg.I, cfg.h)).astype(np.float32) for _ in range(cfg.E)]
+    W2 = [rng.normal(size=(cfg.h, cfg.I)).astype(np.float32) for _ in range(cfg.E)]
+    base = oracle.layer_forward(x, wr, lambda e: W13[e], lambda e: W2[e], cfg.replace(n_redundant=0),
+                                logit_offset=off)
+    plan = oracle.eplb_plan(base["layout"]["counts"], cfg.ep_size, cfg.n_redundant)
+    r = oracle.layer_forward_eplb(x, wr, lambda e: W13[e], lambda e: W2[e], cfg, plan, logit_offset=off)
+    assert base["layout"]["counts"][0] > cfg.T // 2
+    assert np.array_equal(r["ids"], base["ids"])
+    for t in range(cfg.T):
+        for k in range(cfg.K):
+            e = base["ids"][t, k]
+            reps = plan["rep_phys"][plan["rep_offsets"][e]:plan["rep_offsets"][e + 1]]
+            assert r["phys_ids"][t, k] == reps[t % len(reps)]
+    assert np.array_equal(r["y"], base["y"])
+    assert r["layout"]["balancedness"] > base["layout"]["balancedness"] + 0.2
