@@ -57,6 +57,7 @@ def measured_peaks():
 
 def workload_config(w):
     return {"workload": w.name, "T": w.T, "h": w.h, "E": w.E, "K": w.K, "I": w.I, "shared_I": w.shared_I,
+            "n_redundant": w.n_redundant,
             "score": w.score,
             "n_groups": w.n_groups, "topk_groups": w.topk_groups, "capacity": w.capacity, "ep_size": w.ep_size,
             "l2": "inputs larger than L2: every step streams all touched expert weights (GBs) through the 126 MB L2",
@@ -161,30 +162,54 @@ def run_ours(args, rank, world, local_rank):
     if shared:
         ys = torch.empty(T, w.h, dtype=dt, device="cuda")
         ws_shared = moe.alloc_workspace(cfg, moe.MOE_OP_SHARED)
-    stages = ("logits", "route", "layout", "permute", "ffn") + (("shared",) if shared else ()) + ("combine",)
+    eplb = w.n_redundant > 0  # replicas: plan once from this batch's logical expert loads (not timed)
+    if eplb:
+        moe.moe_router_logits(cfg, inp["x"], inp["w_r"], inp["logit_offset"], logits)
+        moe.moe_route(cfg, logits, inp["sel_bias"], ids, wts)
+        counts = torch.bincount(ids.view(-1).long(), minlength=E).cpu().numpy()
+        plan_h = moe.moe_eplb_plan(E, N, w.n_redundant, counts)
+        plan = {k: torch.from_numpy(v).cuda() for k, v in plan_h.items() if k != "rank_load"}
+        pids = torch.empty(T, K, **i32)
+    stages = (("logits", "route") + (("eplb_map",) if eplb else ()) + ("layout", "permute", "ffn")
+              + (("shared",) if shared else ()) + ("combine",))
     n_ev = len(stages) + 1
 
     def step(ev=None):
-        rec = (lambda i: ev[i].record(stream)) if ev is not None else (lambda i: None)
-        rec(0)
+        n = [0]
+
+        def rec():
+            if ev is not None:
+                ev[n[0]].record(stream)
+            n[0] += 1
+
+        rec()
         moe.moe_router_logits(cfg, inp["x"], inp["w_r"], inp["logit_offset"], logits)
-        rec(1)
+        rec()
         moe.moe_route(cfg, logits, inp["sel_bias"], ids, wts)
-        rec(2)
-        moe.moe_dispatch_layout(cfg, ids, lay.counts, lay.kept, lay.offsets, lay.slot, lay.row_src, lay.n_ij,
+        rec()
+        lids = ids
+        if eplb:
+            moe.moe_eplb_map(cfg, ids, plan["rep_offsets"], plan["rep_phys"], pids)
+            rec()
+            lids = pids
+        moe.moe_dispatch_layout(cfg, lids, lay.counts, lay.kept, lay.offsets, lay.slot, lay.row_src, lay.n_ij,
                                 lay.rank_bytes, lay.stats, ws_layout)
-        rec(3)
+        rec()
         moe.moe_permute(cfg, inp["x"], lay.slot, lay.row_src, xp)
-        rec(4)
-        moe.moe_grouped_ffn(cfg, xp, lay.offsets, lay.kept, inp["w13"], inp["w2"], yp, ws_ffn)
-        rec(5)
+        rec()
+        if eplb:
+            moe.moe_grouped_ffn_mapped(cfg, xp, lay.offsets, lay.kept, plan["phys_to_log"], inp["w13"], inp["w2"],
+                                       yp, ws_ffn)
+        else:
+            moe.moe_grouped_ffn(cfg, xp, lay.offsets, lay.kept, inp["w13"], inp["w2"], yp, ws_ffn)
+        rec()
         if shared:
             moe.moe_shared_ffn(cfg, inp["x"], inp["w13s"], inp["w2s"], ys, ws_shared)
-            rec(6)
+            rec()
             moe.moe_combine_add(cfg, yp, lay.slot, wts, ys, y)
         else:
             moe.moe_combine(cfg, yp, lay.slot, wts, y)
-        rec(n_ev - 1)
+        rec()
 
     for _ in range(args.warmup):
         step()
@@ -213,14 +238,22 @@ def run_ours(args, rank, world, local_rank):
     # ---- end to end through the public call with host buffers.  Two streams
     # take alternate steps, each with its own workspace and pinned buffers, so
     # the host<->device copies of one step overlap the compute of the other.
-    op_host = moe.MOE_OP_BLOCK_HOST if shared else moe.MOE_OP_LAYER_HOST
+    op_host = moe.MOE_OP_BLOCK_HOST if shared else (moe.MOE_OP_LAYER if eplb else moe.MOE_OP_LAYER_HOST)
     lanes = [dict(stream=torch.cuda.Stream(), x=inp["x"].cpu().pin_memory(),
-                  y=torch.empty(T, w.h, dtype=dt).pin_memory(), ws=moe.alloc_workspace(cfg, op_host))
+                  y=torch.empty(T, w.h, dtype=dt).pin_memory(), ws=moe.alloc_workspace(cfg, op_host),
+                  xd=torch.empty_like(inp["x"]) if eplb else None, yd=torch.empty_like(y) if eplb else None)
              for _ in range(2)]
 
     def e2e_step(i):
         ln = lanes[i % len(lanes)]
-        if shared:
+        if eplb:  # the layer call takes device activations: copies on the lane's stream around it
+            with torch.cuda.stream(ln["stream"]):
+                ln["xd"].copy_(ln["x"], non_blocking=True)
+                moe.moe_layer_forward_eplb(cfg, ln["xd"], inp["w_r"], inp["logit_offset"], inp["sel_bias"],
+                                           inp["w13"], inp["w2"], plan["rep_offsets"], plan["rep_phys"],
+                                           plan["phys_to_log"], ln["yd"], None, ln["ws"], stream=ln["stream"])
+                ln["y"].copy_(ln["yd"], non_blocking=True)
+        elif shared:
             moe.moe_block_forward_host(cfg, ln["x"], inp["w_r"], inp["logit_offset"], inp["sel_bias"], inp["w13"],
                                        inp["w2"], inp["w13s"], inp["w2s"], ln["y"], ln["ws"], stream=ln["stream"])
         else:
@@ -258,6 +291,8 @@ def run_ours(args, rank, world, local_rank):
     rows_kept = int(kept.sum())
     ds = 2 if w.dtype == "bf16" else 4
     touched = int((kept > 0).sum())
+    if eplb:  # replicas share their logical expert's weights: count each touched logical expert once
+        touched = len(set(plan_h["phys_to_log"][kept > 0].tolist()))
     weight_bytes = touched * 3 * w.h * w.I * ds
     ffn_bytes = weight_bytes + rows_kept * (2 * w.h + 2 * w.I) * ds
     ffn_flops = 6.0 * w.h * w.I * rows_kept
@@ -269,7 +304,7 @@ def run_ours(args, rank, world, local_rank):
     tc_peak = float(peaks["bf16_tflops_sustained"])
     ffn_s = per_stage["ffn"] / 1e3
     ffn_gbs = ffn_bytes / ffn_s / 1e9
-    launches_per_step = 8 + (1 if (w.pad and w.capacity > 0) else 0) + (2 if shared else 0)
+    launches_per_step = 8 + (1 if (w.pad and w.capacity > 0) else 0) + (2 if shared else 0) + (1 if eplb else 0)
     ms = total_ms / args.steps
     out = {
         "metric": METRIC,

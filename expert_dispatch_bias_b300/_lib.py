@@ -33,6 +33,7 @@ EXPORTS = (
     "moe_grouped_ffn",
     "moe_combine", "moe_layer_forward", "moe_layer_forward_host", "moe_check",
     "moe_shared_ffn", "moe_combine_add", "moe_block_forward", "moe_block_forward_host",
+    "moe_eplb_plan", "moe_eplb_map", "moe_grouped_ffn_mapped", "moe_layer_forward_eplb",
 )
 
 
@@ -48,6 +49,7 @@ class MoeConfig(ctypes.Structure):
         ("dtype", c_int32), ("score", c_int32), ("renormalize", c_int32), ("scale", c_float),
         ("n_groups", c_int32), ("topk_groups", c_int32), ("group_topn", c_int32),
         ("capacity", c_int32), ("pad", c_int32), ("ep_size", c_int32), ("shared_I", c_int32),
+        ("n_redundant", c_int32),
     ]
 
 
@@ -86,6 +88,10 @@ def _load() -> ctypes.CDLL:
         "moe_combine_add": (c_int32, [cfgp] + [c_void_p] * 6),
         "moe_block_forward": (c_int32, [cfgp] + [c_void_p] * 11 + [c_size_t, c_void_p]),
         "moe_block_forward_host": (c_int32, [cfgp] + [c_void_p] * 10 + [c_size_t, c_void_p]),
+        "moe_eplb_plan": (c_int32, [c_int32, c_int32, c_int32] + [c_void_p] * 5),
+        "moe_eplb_map": (c_int32, [cfgp] + [c_void_p] * 5),
+        "moe_grouped_ffn_mapped": (c_int32, [cfgp] + [c_void_p] * 8 + [c_size_t, c_void_p]),
+        "moe_layer_forward_eplb": (c_int32, [cfgp] + [c_void_p] * 11 + [c_size_t, c_void_p]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -121,17 +127,18 @@ def _check(status: int, where: str) -> None:
 
 
 def make_config(T, h, E, K, I, dtype="bf16", score="softmax", renormalize=1, scale=1.0, n_groups=0,
-                topk_groups=0, group_topn=0, capacity=0, pad=0, ep_size=1, shared_I=0) -> MoeConfig:
+                topk_groups=0, group_topn=0, capacity=0, pad=0, ep_size=1, shared_I=0, n_redundant=0) -> MoeConfig:
     return MoeConfig(T, h, E, K, I, MOE_F32 if dtype in ("f32", MOE_F32) else MOE_BF16,
                      MOE_SIGMOID if score in ("sigmoid", MOE_SIGMOID) else MOE_SOFTMAX,
                      int(renormalize), float(scale), n_groups, topk_groups, group_topn, capacity, pad, ep_size,
-                     shared_I)
+                     shared_I, n_redundant)
 
 
 def config_from(w) -> MoeConfig:
     """MoeConfig from any object with the layer's attributes (e.g. a synth Workload)."""
     return make_config(w.T, w.h, w.E, w.K, w.I, w.dtype, w.score, w.renormalize, w.scale, w.n_groups,
-                       w.topk_groups, w.group_topn, w.capacity, w.pad, w.ep_size, getattr(w, "shared_I", 0))
+                       w.topk_groups, w.group_topn, w.capacity, w.pad, w.ep_size, getattr(w, "shared_I", 0),
+                       getattr(w, "n_redundant", 0))
 
 
 # ------------------------------------------------------------------ the C entry points
@@ -238,6 +245,41 @@ def moe_block_forward_host(cfg, x_host, w_r, logit_offset, sel_bias, w13, w2, w1
                                       _ptr(sel_bias), _ptr(w13), _ptr(w2), _ptr(w13s), _ptr(w2s), _ptr(y_host),
                                       _ptr(workspace), workspace.numel() * workspace.element_size(),
                                       _stream(stream)), "moe_block_forward_host")
+
+
+def moe_eplb_plan(E: int, ep_size: int, n_redundant: int, counts) -> dict:
+    """Host-only replica plan (see include/moe.h); counts: a sequence of E ints.
+    Returns numpy arrays rep_offsets, rep_phys, phys_to_log, rank_load."""
+    import numpy as np
+    c = np.ascontiguousarray(np.asarray(counts, dtype=np.int64))
+    P = E + n_redundant
+    out = {"rep_offsets": np.zeros(E + 1, np.int32), "rep_phys": np.zeros(P, np.int32),
+           "phys_to_log": np.zeros(P, np.int32), "rank_load": np.zeros(ep_size, np.int64)}
+    _check(lib.moe_eplb_plan(E, ep_size, n_redundant, c.ctypes.data, out["rep_offsets"].ctypes.data,
+                             out["rep_phys"].ctypes.data, out["phys_to_log"].ctypes.data,
+                             out["rank_load"].ctypes.data), "moe_eplb_plan")
+    return out
+
+
+def moe_eplb_map(cfg, topk_ids, rep_offsets, rep_phys, phys_ids, stream=None) -> None:
+    _check(lib.moe_eplb_map(ctypes.byref(cfg), _ptr(topk_ids), _ptr(rep_offsets), _ptr(rep_phys), _ptr(phys_ids),
+                            _stream(stream)), "moe_eplb_map")
+
+
+def moe_grouped_ffn_mapped(cfg, xp, offsets, kept, phys_to_log, w13, w2, yp, workspace, stream=None) -> None:
+    _check(lib.moe_grouped_ffn_mapped(ctypes.byref(cfg), _ptr(xp), _ptr(offsets), _ptr(kept), _ptr(phys_to_log),
+                                      _ptr(w13), _ptr(w2), _ptr(yp), _ptr(workspace),
+                                      workspace.numel() * workspace.element_size(), _stream(stream)),
+           "moe_grouped_ffn_mapped")
+
+
+def moe_layer_forward_eplb(cfg, x, w_r, logit_offset, sel_bias, w13, w2, rep_offsets, rep_phys, phys_to_log, y,
+                           out: Optional[MoeLayerOut], workspace, stream=None) -> None:
+    _check(lib.moe_layer_forward_eplb(ctypes.byref(cfg), _ptr(x), _ptr(w_r), _ptr(logit_offset), _ptr(sel_bias),
+                                      _ptr(w13), _ptr(w2), _ptr(rep_offsets), _ptr(rep_phys), _ptr(phys_to_log),
+                                      _ptr(y), ctypes.byref(out) if out is not None else None, _ptr(workspace),
+                                      workspace.numel() * workspace.element_size(), _stream(stream)),
+           "moe_layer_forward_eplb")
 
 
 def moe_check(stream=None) -> int:

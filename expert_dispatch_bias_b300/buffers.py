@@ -37,8 +37,9 @@ def alloc_layout(cfg: _lib.MoeConfig, device="cuda") -> LayoutBuffers:
     R = _lib.moe_rows(cfg)
     N = cfg.ep_size
     i32 = dict(dtype=torch.int32, device=device)
+    P = cfg.E + cfg.n_redundant  # physical experts (E without replicas)
     return LayoutBuffers(
-        counts=torch.empty(cfg.E, **i32), kept=torch.empty(cfg.E, **i32), offsets=torch.empty(cfg.E + 1, **i32),
+        counts=torch.empty(P, **i32), kept=torch.empty(P, **i32), offsets=torch.empty(P + 1, **i32),
         slot=torch.empty(max(cfg.T * cfg.K, 1), **i32), row_src=torch.empty(max(R, 1), **i32),
         n_ij=torch.empty(N * N, dtype=torch.int64, device=device),
         rank_bytes=torch.empty(2 * N, dtype=torch.int64, device=device),

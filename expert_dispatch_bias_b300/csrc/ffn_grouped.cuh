@@ -65,6 +65,7 @@ struct FgParams {
   int n_valid;              // output features: I or h
   __nv_bfloat16* out;       // [R, ldo]
   int64_t ldo;
+  const int32_t* w_map;     // expert -> its weight matrices (replicas share a logical expert's), or null
 };
 
 // Tensor maps of the token rows with boxes of 128, 64, 32 and 16 rows.
@@ -218,11 +219,12 @@ __global__ void __launch_bounds__(kFgThreads, 1)
       uint32_t armed = 0, armed_parity = 0;
       // weight rows of the two 128-row boxes of a tile
       auto weight_rows = [&](const FgTile& tl, int64_t& a0, int64_t& a1) {
+        const int64_t we = p.w_map != nullptr ? p.w_map[tl.e] : tl.e;
         if (EPI == kTcSwiglu) {
-          a0 = (int64_t)tl.e * p.a_rows + 128 * tl.ft;
+          a0 = we * p.a_rows + 128 * tl.ft;
           a1 = a0 + p.up_rows;
         } else {
-          a0 = (int64_t)tl.e * p.a_rows + 256 * tl.ft;
+          a0 = we * p.a_rows + 256 * tl.ft;
           a1 = a0 + 128;
         }
       };

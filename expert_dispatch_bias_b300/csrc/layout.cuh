@@ -301,4 +301,26 @@ __global__ void __launch_bounds__(kFinalizeThreads) layout_finalize_kernel(Layou
   for (int t = tid; t < p.num_tiles; t += kFinalizeThreads) p.ws.flags[t] = kTileEmpty;
 }
 
+// Replica map of expert-parallel load balancing: the physical expert of every
+// routed (t, k) is replica t mod n_rep(e) of its logical expert e, where the
+// replicas of e are rep_phys[rep_offsets[e] .. rep_offsets[e+1]).  An id outside
+// [0, E) or a plan entry outside [0, P) raises the bad-index error and writes -1.
+__global__ void eplb_map_kernel(const int32_t* ids, int64_t A, int K, int E, int P, const int32_t* rep_offsets,
+                                const int32_t* rep_phys, int32_t* out) {
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < A; i += (int64_t)gridDim.x * blockDim.x) {
+    const int e = ids[i];
+    int32_t v = -1;
+    if (e >= 0 && e < E) {
+      const int32_t r0 = rep_offsets[e], n = rep_offsets[e + 1] - r0;
+      const int64_t j = n > 0 ? r0 + (i / K) % n : -1;
+      if (n > 0 && r0 >= 0 && j < P) v = rep_phys[j];
+    }
+    if (v < 0 || v >= P) {
+      raise_error(kErrBadIndex);
+      v = -1;
+    }
+    out[i] = v;
+  }
+}
+
 }  // namespace moe

@@ -9,6 +9,9 @@
 #include <stdint.h>
 #include <string.h>
 
+#include <algorithm>
+#include <vector>
+
 #include <cudaTypedefs.h>
 
 #include "moe.h"
@@ -44,8 +47,12 @@ namespace {
 
 inline bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 inline int ds_of(const moe_config& c) { return c.dtype == MOE_F32 ? 4 : 2; }
+// Experts after routing: the E logical experts plus the redundant replicas
+// (expert-parallel load balancing); layout, permutation, FFN and combine
+// work on these physical experts.
+inline int nphys(const moe_config& c) { return c.E + c.n_redundant; }
 inline int64_t rows_of(const moe_config& c) {
-  return (c.pad && c.capacity > 0) ? (int64_t)c.E * c.capacity : (int64_t)c.T * c.K;
+  return (c.pad && c.capacity > 0) ? (int64_t)nphys(c) * c.capacity : (int64_t)c.T * c.K;
 }
 inline cudaStream_t as_stream(void* s) { return static_cast<cudaStream_t>(s); }
 
@@ -68,7 +75,8 @@ moe_status validate(const moe_config* c) {
   }
   if (c->capacity < 0 || (c->pad != 0 && c->pad != 1)) return MOE_ERR_INVALID_ARG;
   if (c->pad && c->capacity == 0) return MOE_ERR_INVALID_ARG;
-  if (c->ep_size < 1 || c->E % c->ep_size != 0) return MOE_ERR_INVALID_ARG;
+  if (c->n_redundant < 0 || (int64_t)c->E + c->n_redundant > 1024) return MOE_ERR_INVALID_ARG;
+  if (c->ep_size < 1 || (c->E + c->n_redundant) % c->ep_size != 0) return MOE_ERR_INVALID_ARG;
   if (c->shared_I < 0 || c->shared_I % 64 != 0) return MOE_ERR_INVALID_ARG;
   if ((int64_t)c->T * c->K >= INT32_MAX || rows_of(*c) >= INT32_MAX) return MOE_ERR_INVALID_ARG;
   // one permuted row must fit a shared-memory buffer of the bulk-copy permute
@@ -136,6 +144,7 @@ struct LayerBuffers {
   void* inter;
   void* xdev;
   void* ydev;
+  int32_t* phys_ids;   // physical expert of every (t, k) (replicas)
   void* ys;            // shared expert output [T, h] (block)
   void* shared_ws;     // shared expert intermediate [T, shared_I] (block)
   size_t total;
@@ -148,14 +157,15 @@ LayerBuffers carve_layer(const moe_config& c, void* ws, bool host_io, bool block
   LayerBuffers b;
   const int64_t A = (int64_t)c.T * c.K, R = rows_of(c);
   const int N = c.ep_size, ds = ds_of(c);
-  b.layout_ws_bytes = layout_scratch_bytes(A, c.E);
+  b.layout_ws_bytes = layout_scratch_bytes(A, nphys(c));
   b.layout_ws = cv.take<char>(b.layout_ws_bytes);
   b.logits = cv.take<float>((size_t)c.T * c.E);
   b.ids = cv.take<int32_t>(A);
   b.w = cv.take<float>(A);
-  b.counts = cv.take<int32_t>(c.E);
-  b.kept = cv.take<int32_t>(c.E);
-  b.offsets = cv.take<int32_t>(c.E + 1);
+  b.counts = cv.take<int32_t>(nphys(c));
+  b.kept = cv.take<int32_t>(nphys(c));
+  b.offsets = cv.take<int32_t>(nphys(c) + 1);
+  b.phys_ids = c.n_redundant > 0 ? cv.take<int32_t>(A) : nullptr;
   b.slot = cv.take<int32_t>(A);
   b.row_src = cv.take<int32_t>(R);
   b.n_ij = cv.take<int64_t>((size_t)N * N);
@@ -262,7 +272,7 @@ moe_status launch_layout(const moe_config& c, const int32_t* ids, int32_t* count
   p.A = (int64_t)c.T * c.K;
   p.T = c.T;
   p.K = c.K;
-  p.E = c.E;
+  p.E = nphys(c);
   p.cap = c.capacity;
   p.pad = c.pad;
   p.n_ep = c.ep_size;
@@ -278,14 +288,14 @@ moe_status launch_layout(const moe_config& c, const int32_t* ids, int32_t* count
   p.n_ij = n_ij;
   p.rank_bytes = rank_bytes;
   p.stats = stats;
-  p.ws = layout_scratch_at(ws, p.A, c.E);
-  const size_t smem1 = (size_t)(kLayoutWarps + 2) * c.E * sizeof(int32_t);
+  p.ws = layout_scratch_at(ws, p.A, nphys(c));
+  const size_t smem1 = (size_t)(kLayoutWarps + 2) * nphys(c) * sizeof(int32_t);
   CUDA_TRY(allow_smem(layout_rank_kernel, smem1));
   layout_rank_kernel<<<p.num_tiles, kLayoutThreads, smem1, st>>>(p);
   CUDA_TRY(cudaGetLastError());
   const int64_t per_block = kFinalizeThreads * kFinalizeItems;
   const int blocks2 = (int)((p.A + per_block - 1) / per_block) > 0 ? (int)((p.A + per_block - 1) / per_block) : 1;
-  layout_finalize_kernel<<<blocks2, kFinalizeThreads, (c.E + 1) * sizeof(int32_t), st>>>(p);
+  layout_finalize_kernel<<<blocks2, kFinalizeThreads, (nphys(c) + 1) * sizeof(int32_t), st>>>(p);
   CUDA_TRY(cudaGetLastError());
   return MOE_OK;
 }
@@ -361,9 +371,10 @@ moe_status launch_combine(const moe_config& c, const void* yp, const int32_t* sl
 
 template <typename T>
 cudaError_t launch_ffn_simt(const moe_config& c, const void* xp, const int32_t* offsets, const int32_t* kept,
-                            const void* w13, const void* w2, void* yp, void* inter, cudaStream_t st) {
+                            const int32_t* w_map, const void* w13, const void* w2, void* yp, void* inter,
+                            cudaStream_t st) {
   const int64_t R = rows_of(c);
-  const unsigned mblocks = (unsigned)((R + kSimtBM - 1) / kSimtBM + c.E);
+  const unsigned mblocks = (unsigned)((R + kSimtBM - 1) / kSimtBM + nphys(c));
   SimtParams p{};
   p.A = xp;
   p.lda = c.h;
@@ -375,7 +386,9 @@ cudaError_t launch_ffn_simt(const moe_config& c, const void* xp, const int32_t* 
   p.ldc = c.I;
   p.offsets = offsets;
   p.kept = kept;
-  p.E = c.E;
+  p.E = nphys(c);
+  p.w_map = w_map;
+  p.n_w = w_map != nullptr ? c.E : nphys(c);
   p.N = c.I;
   p.K = c.h;
   simt_gemm_kernel<T, kSimtSwiglu><<<dim3((c.I + kSimtBN - 1) / kSimtBN, mblocks), kSimtThreads, 0, st>>>(p);
@@ -437,19 +450,21 @@ moe_status make_tensor_map(CUtensorMap* map, const void* base, uint64_t inner, u
 constexpr int kFfnBN = 256, kFfnStages = 4;
 
 moe_status launch_ffn_tokens_m(const moe_config& c, const void* xp, const int32_t* offsets, const int32_t* kept,
-                               const void* w13, const void* w2, void* yp, void* inter, cudaStream_t st) {
+                               const int32_t* w_map, int n_w, const void* w13, const void* w2, void* yp, void* inter,
+                               cudaStream_t st) {
   using S = TcShape<kFfnBN, kFfnStages>;
   const int64_t R = rows_of(c);
   const int grid = device_info().sms;
   CUtensorMap a1, b1, a2, b2;
   MOE_TRY(make_tensor_map(&a1, xp, c.h, R, kTcBM));
-  MOE_TRY(make_tensor_map(&b1, w13, c.h, (uint64_t)c.E * 2 * c.I, kFfnBN / 2));
+  MOE_TRY(make_tensor_map(&b1, w13, c.h, (uint64_t)n_w * 2 * c.I, kFfnBN / 2));
   MOE_TRY(make_tensor_map(&a2, inter, c.I, R, kTcBM));
-  MOE_TRY(make_tensor_map(&b2, w2, c.I, (uint64_t)c.E * c.h, kFfnBN));
+  MOE_TRY(make_tensor_map(&b2, w2, c.I, (uint64_t)n_w * c.h, kFfnBN));
   TcParams p1{};
   p1.offsets = offsets;
   p1.kept = kept;
-  p1.E = c.E;
+  p1.E = nphys(c);
+  p1.w_map = w_map;
   p1.n_tiles = (c.I + kFfnBN / 2 - 1) / (kFfnBN / 2);
   p1.k_blocks = c.h / kTcBK;
   p1.b_rows = 2LL * c.I;
@@ -483,14 +498,15 @@ moe_status launch_ffn_tokens_m(const moe_config& c, const void* xp, const int32_
 constexpr int kFgTileRows = 160, kFgStages = 4;
 template <int BT, int STAGES>
 moe_status launch_ffn_grouped(const moe_config& c, const void* xp, const int32_t* offsets, const int32_t* kept,
-                              const void* w13, const void* w2, void* yp, void* inter, cudaStream_t st) {
+                              const int32_t* w_map, int n_w, const void* w13, const void* w2, void* yp, void* inter,
+                              cudaStream_t st) {
   using S = FgShape<BT, STAGES>;
   const int64_t R = rows_of(c);
   const int grid = device_info().sms;
   CUtensorMap w1m, w2m;
   FgTokenMaps x1, x2;
-  MOE_TRY(make_tensor_map(&w1m, w13, c.h, (uint64_t)c.E * 2 * c.I, 128));
-  MOE_TRY(make_tensor_map(&w2m, w2, c.I, (uint64_t)c.E * c.h, 128));
+  MOE_TRY(make_tensor_map(&w1m, w13, c.h, (uint64_t)n_w * 2 * c.I, 128));
+  MOE_TRY(make_tensor_map(&w2m, w2, c.I, (uint64_t)n_w * c.h, 128));
   for (int i = 0; i < 4; ++i) {
     MOE_TRY(make_tensor_map(&x1.m[i], xp, c.h, R, 128u >> i));
     MOE_TRY(make_tensor_map(&x2.m[i], inter, c.I, R, 128u >> i));
@@ -498,7 +514,8 @@ moe_status launch_ffn_grouped(const moe_config& c, const void* xp, const int32_t
   FgParams p1{};
   p1.offsets = offsets;
   p1.kept = kept;
-  p1.E = c.E;
+  p1.E = nphys(c);
+  p1.w_map = w_map;
   p1.f_tiles = (c.I + 127) / 128;
   p1.k_blocks = c.h / kTcBK;
   p1.a_rows = 2LL * c.I;
@@ -529,16 +546,19 @@ moe_status launch_ffn_grouped(const moe_config& c, const void* xp, const int32_t
 // the mean T*K/E.
 int64_t expected_rows_per_expert(const moe_config& c) {
   if (c.capacity > 0) return c.capacity < c.T ? c.capacity : c.T;
-  return ((int64_t)c.T * c.K + c.E - 1) / c.E;
+  return ((int64_t)c.T * c.K + nphys(c) - 1) / nphys(c);
 }
 
+// n_w: experts held by w13/w2; w_map: physical expert -> its weights (null:
+// the identity, n_w == physical experts).
 moe_status launch_ffn_tc(const moe_config& c, const void* xp, const int32_t* offsets, const int32_t* kept,
-                         const void* w13, const void* w2, void* yp, void* inter, cudaStream_t st) {
+                         const int32_t* w_map, int n_w, const void* w13, const void* w2, void* yp, void* inter,
+                         cudaStream_t st) {
   // TMA row coordinates are 32-bit
-  if ((int64_t)c.E * 2 * c.I >= INT32_MAX || (int64_t)c.E * c.h >= INT32_MAX) return MOE_ERR_UNSUPPORTED;
+  if ((int64_t)n_w * 2 * c.I >= INT32_MAX || (int64_t)n_w * c.h >= INT32_MAX) return MOE_ERR_UNSUPPORTED;
   if (expected_rows_per_expert(c) > MOE_FFN_SWAP_MAX_ROWS)
-    return launch_ffn_tokens_m(c, xp, offsets, kept, w13, w2, yp, inter, st);
-  return launch_ffn_grouped<kFgTileRows, kFgStages>(c, xp, offsets, kept, w13, w2, yp, inter, st);
+    return launch_ffn_tokens_m(c, xp, offsets, kept, w_map, n_w, w13, w2, yp, inter, st);
+  return launch_ffn_grouped<kFgTileRows, kFgStages>(c, xp, offsets, kept, w_map, n_w, w13, w2, yp, inter, st);
 }
 
 // Router logits of a bf16 layer on the tensor cores: one segment of T rows
@@ -596,10 +616,11 @@ moe_status launch_logits(const moe_config& c, const void* x, const void* w_r, co
 }
 
 moe_status launch_ffn(const moe_config& c, const void* xp, const int32_t* offsets, const int32_t* kept,
-                      const void* w13, const void* w2, void* yp, void* inter, cudaStream_t st) {
+                      const int32_t* w_map, int n_w, const void* w13, const void* w2, void* yp, void* inter,
+                      cudaStream_t st) {
   if (rows_of(c) == 0) return MOE_OK;
-  if (c.dtype == MOE_BF16) return launch_ffn_tc(c, xp, offsets, kept, w13, w2, yp, inter, st);
-  CUDA_TRY(launch_ffn_simt<float>(c, xp, offsets, kept, w13, w2, yp, inter, st));
+  if (c.dtype == MOE_BF16) return launch_ffn_tc(c, xp, offsets, kept, w_map, n_w, w13, w2, yp, inter, st);
+  CUDA_TRY(launch_ffn_simt<float>(c, xp, offsets, kept, w_map, w13, w2, yp, inter, st));
   return MOE_OK;
 }
 
@@ -682,9 +703,29 @@ moe_status launch_shared_ffn(const moe_config& c, const void* x, const void* w13
   return MOE_OK;
 }
 
+// Device copy of an EPLB plan (moe_eplb_plan's outputs), or all null.
+struct EplbDev {
+  const int32_t* rep_offsets = nullptr;
+  const int32_t* rep_phys = nullptr;
+  const int32_t* phys_to_log = nullptr;
+};
+
+moe_status launch_eplb_map(const moe_config& c, const int32_t* ids, const EplbDev& plan, int32_t* phys,
+                           cudaStream_t st) {
+  const int64_t A = (int64_t)c.T * c.K;
+  if (A == 0) return MOE_OK;
+  int64_t blocks = (A + 255) / 256;
+  if (blocks > (int64_t)device_info().sms * 8) blocks = (int64_t)device_info().sms * 8;
+  eplb_map_kernel<<<(unsigned)blocks, 256, 0, st>>>(ids, A, c.K, c.E, nphys(c), plan.rep_offsets, plan.rep_phys,
+                                                      phys);
+  CUDA_TRY(cudaGetLastError());
+  return MOE_OK;
+}
+
 moe_status layer_core(const moe_config& c, const void* x, const void* w_r, const float* logit_offset,
                       const float* sel_bias, const void* w13, const void* w2, const void* w13s, const void* w2s,
-                      void* y, const moe_layer_out* out, const LayerBuffers& b, cudaStream_t st) {
+                      void* y, const moe_layer_out* out, const LayerBuffers& b, cudaStream_t st,
+                      const EplbDev& plan = EplbDev()) {
   moe_layer_out o{};
   if (out != nullptr) o = *out;
   float* logits = o.logits ? o.logits : b.logits;
@@ -700,9 +741,15 @@ moe_status layer_core(const moe_config& c, const void* x, const void* w_r, const
   moe_layout_stats* stats = o.stats ? o.stats : b.stats;
   MOE_TRY(launch_logits(c, x, w_r, logit_offset, logits, st));
   MOE_TRY(launch_route(c, logits, sel_bias, ids, w, st));
-  MOE_TRY(launch_layout(c, ids, counts, kept, offsets, slot, row_src, n_ij, rank_bytes, stats, b.layout_ws, st));
+  const int32_t* lids = ids;  // expert ids the layout sees: physical replicas when the plan has any
+  if (c.n_redundant > 0) {
+    MOE_TRY(launch_eplb_map(c, ids, plan, b.phys_ids, st));
+    lids = b.phys_ids;
+  }
+  MOE_TRY(launch_layout(c, lids, counts, kept, offsets, slot, row_src, n_ij, rank_bytes, stats, b.layout_ws, st));
   MOE_TRY(launch_permute(c, x, slot, row_src, b.xp, st));
-  MOE_TRY(launch_ffn(c, b.xp, offsets, kept, w13, w2, b.yp, b.inter, st));
+  MOE_TRY(launch_ffn(c, b.xp, offsets, kept, plan.phys_to_log, plan.phys_to_log ? c.E : nphys(c), w13, w2, b.yp,
+                     b.inter, st));
   if (b.ys != nullptr)
     MOE_TRY(launch_shared_ffn(c, x, w13s, w2s, b.ys, static_cast<char*>(b.shared_ws) + 256, st));
   MOE_TRY(launch_combine(c, b.yp, slot, w, b.ys, y, st));
@@ -752,7 +799,7 @@ moe_status moe_workspace_size(const moe_config* cfg, int32_t op, size_t* bytes) 
   MOE_TRY(validate(cfg));
   if (bytes == nullptr) return MOE_ERR_INVALID_ARG;
   switch (op) {
-    case MOE_OP_LAYOUT: *bytes = layout_scratch_bytes((int64_t)cfg->T * cfg->K, cfg->E); return MOE_OK;
+    case MOE_OP_LAYOUT: *bytes = layout_scratch_bytes((int64_t)cfg->T * cfg->K, nphys(*cfg)); return MOE_OK;
     case MOE_OP_FFN: *bytes = ffn_ws_bytes(*cfg); return MOE_OK;
     case MOE_OP_LAYER: *bytes = carve_layer(*cfg, nullptr, false).total; return MOE_OK;
     case MOE_OP_LAYER_HOST: *bytes = carve_layer(*cfg, nullptr, true).total; return MOE_OK;
@@ -810,7 +857,7 @@ moe_status moe_dispatch_layout(const moe_config* cfg, const int32_t* topk_ids, i
   MOE_TRY(check_ptr(rank_bytes, 8));
   MOE_TRY(check_ptr(stats, 8));
   MOE_TRY(check_ptr(workspace, 256));
-  if (workspace_bytes < layout_scratch_bytes((int64_t)cfg->T * cfg->K, cfg->E)) return MOE_ERR_WORKSPACE_TOO_SMALL;
+  if (workspace_bytes < layout_scratch_bytes((int64_t)cfg->T * cfg->K, nphys(*cfg))) return MOE_ERR_WORKSPACE_TOO_SMALL;
   return launch_layout(*cfg, topk_ids, counts, kept, offsets, slot, row_src, n_ij, rank_bytes, stats, workspace,
                        as_stream(stream));
 }
@@ -831,7 +878,7 @@ moe_status moe_dispatch_layout_static(const moe_config* cfg, const int32_t* topk
   MOE_TRY(check_ptr(rank_bytes, 8));
   MOE_TRY(check_ptr(stats, 8));
   const int64_t A = (int64_t)cfg->T * cfg->K;
-  if (layout_scratch_bytes(A, cfg->E) > MOE_LAYOUT_STATIC_SCRATCH_BYTES) return MOE_ERR_WORKSPACE_TOO_SMALL;
+  if (layout_scratch_bytes(A, nphys(*cfg)) > MOE_LAYOUT_STATIC_SCRATCH_BYTES) return MOE_ERR_WORKSPACE_TOO_SMALL;
   void* scratch = nullptr;
   MOE_TRY(static_layout_scratch(&scratch));
   // the counters and tile flags must start at zero; the per-tile sums are
@@ -868,7 +915,8 @@ moe_status moe_grouped_ffn(const moe_config* cfg, const void* xp, const int32_t*
   MOE_TRY(check_dtype_ptr(w2));
   MOE_TRY(check_ptr(workspace, 256));
   if (workspace_bytes < ffn_ws_bytes(*cfg)) return MOE_ERR_WORKSPACE_TOO_SMALL;
-  return launch_ffn(*cfg, xp, offsets, kept, w13, w2, yp, static_cast<char*>(workspace) + 256, as_stream(stream));
+  return launch_ffn(*cfg, xp, offsets, kept, nullptr, nphys(*cfg), w13, w2, yp, static_cast<char*>(workspace) + 256,
+                    as_stream(stream));
 }
 
 moe_status moe_combine(const moe_config* cfg, const void* yp, const int32_t* slot, const float* topk_w, void* y,
@@ -893,6 +941,7 @@ moe_status moe_layer_forward(const moe_config* cfg, const void* x, const void* w
   }
   MOE_TRY(check_layer_ptrs(*cfg, x, w_r, logit_offset, sel_bias, w13, w2));
   MOE_TRY(check_ptr(workspace, 256));
+  if (cfg->n_redundant > 0) return MOE_ERR_INVALID_ARG;  // replicas need a plan: moe_layer_forward_eplb
   const LayerBuffers b = carve_layer(*cfg, workspace, false);
   if (workspace_bytes < b.total) return MOE_ERR_WORKSPACE_TOO_SMALL;
   return layer_core(*cfg, x, w_r, logit_offset, sel_bias, w13, w2, nullptr, nullptr, y, out, b, as_stream(stream));
@@ -903,6 +952,7 @@ moe_status moe_layer_forward_host(const moe_config* cfg, const void* x_host, con
                                   void* y_host, void* workspace, size_t workspace_bytes, void* stream) {
   MOE_TRY(validate(cfg));
   if (cfg->T > 0 && (x_host == nullptr || y_host == nullptr)) return MOE_ERR_INVALID_ARG;
+  if (cfg->n_redundant > 0) return MOE_ERR_INVALID_ARG;  // replicas need a plan: moe_layer_forward_eplb
   MOE_TRY(check_layer_ptrs(*cfg, x_host, w_r, logit_offset, sel_bias, w13, w2));
   MOE_TRY(check_ptr(workspace, 256));
   const LayerBuffers b = carve_layer(*cfg, workspace, true);
@@ -948,7 +998,7 @@ moe_status moe_block_forward(const moe_config* cfg, const void* x, const void* w
                              const void* w2s, void* y, const moe_layer_out* out, void* workspace,
                              size_t workspace_bytes, void* stream) {
   MOE_TRY(validate(cfg));
-  if (cfg->shared_I <= 0) return MOE_ERR_INVALID_ARG;
+  if (cfg->shared_I <= 0 || cfg->n_redundant > 0) return MOE_ERR_INVALID_ARG;
   if (cfg->T > 0) {
     MOE_TRY(check_dtype_ptr(x));
     MOE_TRY(check_dtype_ptr(y));
@@ -967,7 +1017,7 @@ moe_status moe_block_forward_host(const moe_config* cfg, const void* x_host, con
                                   const void* w2, const void* w13s, const void* w2s, void* y_host,
                                   void* workspace, size_t workspace_bytes, void* stream) {
   MOE_TRY(validate(cfg));
-  if (cfg->shared_I <= 0) return MOE_ERR_INVALID_ARG;
+  if (cfg->shared_I <= 0 || cfg->n_redundant > 0) return MOE_ERR_INVALID_ARG;
   if (cfg->T > 0 && (x_host == nullptr || y_host == nullptr)) return MOE_ERR_INVALID_ARG;
   MOE_TRY(check_layer_ptrs(*cfg, x_host, w_r, logit_offset, sel_bias, w13, w2));
   MOE_TRY(check_dtype_ptr(w13s));
@@ -981,6 +1031,116 @@ moe_status moe_block_forward_host(const moe_config* cfg, const void* x_host, con
   MOE_TRY(layer_core(*cfg, b.xdev, w_r, logit_offset, sel_bias, w13, w2, w13s, w2s, b.ydev, nullptr, b, st));
   if (bytes > 0) CUDA_TRY(cudaMemcpyAsync(y_host, b.ydev, bytes, cudaMemcpyDeviceToHost, st));
   return MOE_OK;
+}
+
+moe_status moe_eplb_plan(int32_t E, int32_t ep_size, int32_t n_redundant, const int64_t* counts,
+                         int32_t* rep_offsets, int32_t* rep_phys, int32_t* phys_to_log, int64_t* rank_load) {
+  if (E < 1 || ep_size < 1 || n_redundant < 0 || (int64_t)E + n_redundant > 1024) return MOE_ERR_INVALID_ARG;
+  if ((E + n_redundant) % ep_size != 0) return MOE_ERR_INVALID_ARG;
+  if (counts == nullptr || rep_offsets == nullptr || rep_phys == nullptr || phys_to_log == nullptr)
+    return MOE_ERR_INVALID_ARG;
+  for (int e = 0; e < E; ++e)
+    if (counts[e] < 0 || counts[e] > ((int64_t)1 << 40)) return MOE_ERR_INVALID_ARG;
+  const int P = E + n_redundant, slots = P / ep_size;
+  // replication: each redundant replica to the largest load per replica
+  std::vector<int64_t> n_rep(E, 1);
+  for (int i = 0; i < n_redundant; ++i) {
+    int best = 0;
+    for (int e = 1; e < E; ++e)
+      if (counts[e] * n_rep[best] > counts[best] * n_rep[e]) best = e;
+    ++n_rep[best];
+  }
+  // replicas with the even split of their expert's count; heaviest first
+  struct Rep {
+    int64_t load;
+    int e, r;
+  };
+  std::vector<Rep> reps;
+  reps.reserve(P);
+  for (int e = 0; e < E; ++e)
+    for (int r = 0; r < n_rep[e]; ++r)
+      reps.push_back({counts[e] / n_rep[e] + (r < counts[e] % n_rep[e] ? 1 : 0), e, r});
+  std::sort(reps.begin(), reps.end(), [](const Rep& a, const Rep& b) {
+    if (a.load != b.load) return a.load > b.load;
+    if (a.e != b.e) return a.e < b.e;
+    return a.r < b.r;
+  });
+  // placement: least loaded rank with a free slot, ties to the lower rank
+  std::vector<int64_t> load(ep_size, 0);
+  std::vector<int> fill(ep_size, 0);
+  rep_offsets[0] = 0;
+  for (int e = 0; e < E; ++e) rep_offsets[e + 1] = rep_offsets[e] + (int32_t)n_rep[e];
+  for (const Rep& rp : reps) {
+    int best = -1;
+    for (int j = 0; j < ep_size; ++j)
+      if (fill[j] < slots && (best < 0 || load[j] < load[best])) best = j;
+    const int phys = best * slots + fill[best];
+    ++fill[best];
+    load[best] += rp.load;
+    rep_phys[rep_offsets[rp.e] + rp.r] = phys;
+    phys_to_log[phys] = rp.e;
+  }
+  if (rank_load != nullptr)
+    for (int j = 0; j < ep_size; ++j) rank_load[j] = load[j];
+  return MOE_OK;
+}
+
+moe_status moe_eplb_map(const moe_config* cfg, const int32_t* topk_ids, const int32_t* rep_offsets,
+                        const int32_t* rep_phys, int32_t* phys_ids, void* stream) {
+  MOE_TRY(validate(cfg));
+  if (cfg->T > 0) {
+    MOE_TRY(check_ptr(topk_ids, 4));
+    MOE_TRY(check_ptr(phys_ids, 4));
+  }
+  MOE_TRY(check_ptr(rep_offsets, 4));
+  MOE_TRY(check_ptr(rep_phys, 4));
+  EplbDev plan;
+  plan.rep_offsets = rep_offsets;
+  plan.rep_phys = rep_phys;
+  return launch_eplb_map(*cfg, topk_ids, plan, phys_ids, as_stream(stream));
+}
+
+moe_status moe_grouped_ffn_mapped(const moe_config* cfg, const void* xp, const int32_t* offsets, const int32_t* kept,
+                                  const int32_t* phys_to_log, const void* w13, const void* w2, void* yp,
+                                  void* workspace, size_t workspace_bytes, void* stream) {
+  MOE_TRY(validate(cfg));
+  if (rows_of(*cfg) > 0) {
+    MOE_TRY(check_dtype_ptr(xp));
+    MOE_TRY(check_dtype_ptr(yp));
+  }
+  MOE_TRY(check_ptr(offsets, 4));
+  MOE_TRY(check_ptr(kept, 4));
+  MOE_TRY(check_ptr(phys_to_log, 4));
+  MOE_TRY(check_dtype_ptr(w13));
+  MOE_TRY(check_dtype_ptr(w2));
+  MOE_TRY(check_ptr(workspace, 256));
+  if (workspace_bytes < ffn_ws_bytes(*cfg)) return MOE_ERR_WORKSPACE_TOO_SMALL;
+  return launch_ffn(*cfg, xp, offsets, kept, phys_to_log, cfg->E, w13, w2, yp, static_cast<char*>(workspace) + 256,
+                    as_stream(stream));
+}
+
+moe_status moe_layer_forward_eplb(const moe_config* cfg, const void* x, const void* w_r, const float* logit_offset,
+                                  const float* sel_bias, const void* w13, const void* w2, const int32_t* rep_offsets,
+                                  const int32_t* rep_phys, const int32_t* phys_to_log, void* y,
+                                  const moe_layer_out* out, void* workspace, size_t workspace_bytes, void* stream) {
+  MOE_TRY(validate(cfg));
+  if (cfg->T > 0) {
+    MOE_TRY(check_dtype_ptr(x));
+    MOE_TRY(check_dtype_ptr(y));
+  }
+  MOE_TRY(check_layer_ptrs(*cfg, x, w_r, logit_offset, sel_bias, w13, w2));
+  MOE_TRY(check_ptr(rep_offsets, 4));
+  MOE_TRY(check_ptr(rep_phys, 4));
+  MOE_TRY(check_ptr(phys_to_log, 4));
+  MOE_TRY(check_ptr(workspace, 256));
+  const LayerBuffers b = carve_layer(*cfg, workspace, false);
+  if (workspace_bytes < b.total) return MOE_ERR_WORKSPACE_TOO_SMALL;
+  EplbDev plan;
+  plan.rep_offsets = rep_offsets;
+  plan.rep_phys = rep_phys;
+  plan.phys_to_log = phys_to_log;
+  return layer_core(*cfg, x, w_r, logit_offset, sel_bias, w13, w2, nullptr, nullptr, y, out, b, as_stream(stream),
+                    plan);
 }
 
 moe_status moe_check(void* stream) {

@@ -33,6 +33,8 @@ struct SimtParams {
   int E;
   int M, N, K;
   const float* col_bias;    // logits offset [N] or null
+  const int32_t* w_map;     // segment -> its B matrix, or null: segment e uses B_e
+  int n_w;                  // B matrices available (bounds w_map's entries)
 };
 
 // Loads 4 consecutive K-elements of a row as floats (zeros when out of range).
@@ -97,7 +99,12 @@ __global__ void __launch_bounds__(kSimtThreads) simt_gemm_kernel(SimtParams p) {
   }
   const int n0 = blockIdx.x * kSimtBN;
   const T* A = static_cast<const T*>(p.A);
-  const T* B = static_cast<const T*>(p.B) + (int64_t)e * p.b_expert_rows * p.ldb;
+  const int we = p.w_map != nullptr ? p.w_map[e] : e;
+  if (we < 0 || (p.w_map != nullptr && we >= p.n_w)) {  // uniform across the block
+    if (threadIdx.x == 0) raise_error(kErrBadIndex);
+    return;
+  }
+  const T* B = static_cast<const T*>(p.B) + (int64_t)we * p.b_expert_rows * p.ldb;
 
   float acc[4][4] = {};
   float acc_up[4][4] = {};

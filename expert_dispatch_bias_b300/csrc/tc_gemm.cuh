@@ -68,6 +68,7 @@ struct TcParams {
   void* out;                // [rows, ldo] bf16 (SwiGLU, store) or float32 (logits)
   int64_t ldo;
   const float* col_bias;    // logits: per-column offset [n_valid] or null
+  const int32_t* w_map;     // segment -> its B (weight) matrix, or null: segment e uses B_e
 };
 
 // ------------------------------------------------------------------ PTX wrappers
@@ -257,7 +258,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       uint32_t armed_parity = 0;
       for (int t = blockIdx.x; t < total_tiles && !abort_flag; t += gridDim.x) {
         const TcTile tl = tc_decode(t, mbp, p);
-        const int64_t brow = (int64_t)tl.e * p.b_rows;
+        const int64_t brow = (int64_t)(p.w_map != nullptr ? p.w_map[tl.e] : tl.e) * p.b_rows;
         for (int kb = 0; kb < p.k_blocks; ++kb) {
           if (!mbar_wait(&empty_bar[stage], phase ^ 1u, &abort_flag)) {
             abort_flag = 1;

@@ -68,7 +68,9 @@ typedef enum {
 } moe_op;
 
 /* Layer description.  Limits: T >= 0; h % 64 == 0; I % 64 == 0; 1 <= E <= 1024;
- * 1 <= K <= min(E, 16); T*K and the permuted row count below 2^31. */
+ * 1 <= K <= min(E, 16); T*K and the permuted row count below 2^31.  "Experts"
+ * below means the P = E + n_redundant physical experts wherever the call works
+ * after routing (counts, kept, offsets, capacity, n_ij, the FFN's segments). */
 typedef struct moe_config {
   int32_t T;            /* tokens (the pages' B) */
   int32_t h;            /* hidden size */
@@ -86,6 +88,10 @@ typedef struct moe_config {
   int32_t pad;          /* 1 (needs capacity > 0): expert e owns rows [e*cap, (e+1)*cap) */
   int32_t ep_size;      /* virtual expert-parallel group size N_EP; E % ep_size == 0 */
   int32_t shared_I;     /* intermediate size of the shared expert (0: none); % 64 == 0 */
+  int32_t n_redundant;  /* replicas beyond the E logical experts (load balancing, 0: none);
+                         * E + n_redundant <= 1024 physical experts, a multiple of ep_size.
+                         * Routing chooses among the E logical experts; layout, permute,
+                         * FFN and combine work on the E + n_redundant physical ones. */
 } moe_config;
 
 /* Scalar results of moe_dispatch_layout (device memory, 32 bytes). */
@@ -269,6 +275,50 @@ moe_status moe_block_forward_host(const moe_config* cfg, const void* x_host, con
                                   const float* logit_offset, const float* sel_bias, const void* w13,
                                   const void* w2, const void* w13s, const void* w2s, void* y_host,
                                   void* workspace, size_t workspace_bytes, void* stream);
+
+/* Replica plan for expert-parallel load balancing ([overview] glossary "Logical
+ * expert", "Physical expert / Replica", "Redundant expert": hot logical experts
+ * are copied so that E + n_redundant physical experts, a multiple of the GPU
+ * count, flatten the load).  Host only, integer arithmetic:
+ *  - each of the n_redundant replicas goes, one at a time, to the logical expert
+ *    with the largest counts[e] / n_rep[e] (ties to the lower id);
+ *  - a logical expert's count is split over its replicas as evenly as possible
+ *    (replica r gets counts/n + (r < counts % n));
+ *  - replicas, heaviest first (ties: lower expert, lower replica), go to the
+ *    rank with the least load among ranks with a free slot (ties to the lower
+ *    rank); each of the ep_size ranks has (E + n_redundant) / ep_size slots and
+ *    physical ids are rank-major in placement order.
+ * counts [E] int64 (tokens per logical expert, e.g. from a previous batch);
+ * outputs, host memory: rep_offsets [E+1] and rep_phys [E+n_redundant] (the
+ * physical ids of e's replicas are rep_phys[rep_offsets[e] .. rep_offsets[e+1])),
+ * phys_to_log [E+n_redundant], rank_load [ep_size] (may be NULL). */
+moe_status moe_eplb_plan(int32_t E, int32_t ep_size, int32_t n_redundant, const int64_t* counts,
+                         int32_t* rep_offsets, int32_t* rep_phys, int32_t* phys_to_log, int64_t* rank_load);
+
+/* Physical expert of every routed (t, k): replica t mod n_rep(e) of its logical
+ * expert e = topk_ids[t,k] (a function of (t, e) only).  topk_ids, phys_ids
+ * [T,K] int32 device; rep_offsets, rep_phys device copies of moe_eplb_plan's. */
+moe_status moe_eplb_map(const moe_config* cfg, const int32_t* topk_ids, const int32_t* rep_offsets,
+                        const int32_t* rep_phys, int32_t* phys_ids, void* stream);
+
+/* moe_grouped_ffn over physical experts whose weights are their logical
+ * experts': segment p uses w13[phys_to_log[p]], w2[phys_to_log[p]], so
+ * replicas share one copy.  w13 [E,2I,h], w2 [E,h,I]; phys_to_log
+ * [E+n_redundant] int32 device; other arguments as in moe_grouped_ffn. */
+moe_status moe_grouped_ffn_mapped(const moe_config* cfg, const void* xp, const int32_t* offsets, const int32_t* kept,
+                                  const int32_t* phys_to_log, const void* w13, const void* w2, void* yp,
+                                  void* workspace, size_t workspace_bytes, void* stream);
+
+/* moe_layer_forward with replicas: route over the E logical experts,
+ * moe_eplb_map, then layout / permute / mapped FFN / combine over the physical
+ * experts (n_ij, rank bytes and Balancedness per physical placement).  The plan
+ * arrays are device copies of moe_eplb_plan's; out->topk_ids receives logical
+ * ids, out->counts/kept/offsets physical ones.  moe_layer_forward and the
+ * block calls refuse n_redundant > 0.  workspace >= moe_workspace_size(MOE_OP_LAYER). */
+moe_status moe_layer_forward_eplb(const moe_config* cfg, const void* x, const void* w_r, const float* logit_offset,
+                                  const float* sel_bias, const void* w13, const void* w2, const int32_t* rep_offsets,
+                                  const int32_t* rep_phys, const int32_t* phys_to_log, void* y,
+                                  const moe_layer_out* out, void* workspace, size_t workspace_bytes, void* stream);
 
 /* Synchronises `stream`, then reports and clears the sticky device error word of
  * the current device: MOE_ERR_DEVICE_TIMEOUT, MOE_ERR_DEVICE_BAD_INDEX,

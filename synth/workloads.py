@@ -89,7 +89,13 @@ PROFILE_DSV3 = DSV3.replace(name="deepseek_v3_e16_T256", T=256, E=16, ep_size=16
 PROFILE_DSV3_E32 = DSV3.replace(name="deepseek_v3_e32_T512", T=512, E=32, ep_size=32)
 
 ALL = {w.name: w for w in (TINY, MIXTRAL, DSV3, SWITCH) + DECODE}
-EXTRA = {w.name: w for w in (PROFILE_DSV3, PROFILE_DSV3_E32, DSV3_BLOCK)}
+# Expert-parallel load balancing: redundant replicas so that the physical
+# experts fill every rank evenly (16 per 16 ranks for the Zipf-skewed Switch
+# layer: 144 physical, 9 per rank; 64 for DeepSeek-V3: 320 physical, 5 per rank).
+SWITCH_EPLB = SWITCH.replace(name="switch_base_eplb", n_redundant=16)
+DSV3_EPLB = DSV3.replace(name="deepseek_v3_eplb", n_redundant=64)
+
+EXTRA = {w.name: w for w in (PROFILE_DSV3, PROFILE_DSV3_E32, DSV3_BLOCK, SWITCH_EPLB, DSV3_EPLB)}
 
 
 def sigma_in(w: Workload) -> float:
