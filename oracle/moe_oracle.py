@@ -548,6 +548,104 @@ def layer_forward_eplb(x, w_r, get_w13, get_w2, cfg, plan: dict, sel_bias=None, 
                                                                                    rounded=False)}
 
 
+# ----------------------------------------------------------------- FP8 experts
+
+
+def _e4m3_magnitudes() -> np.ndarray:
+    """Magnitudes of the non-negative E4M3 codes 0x00..0x7E (OCP FP8 E4M3: 1 sign,
+    4 exponent bits with bias 7, 3 mantissa bits; exponent 0 is subnormal,
+    m/8 * 2^-6; 0x7F is NaN and there is no infinity; largest finite 448).
+    Increasing with the code."""
+    out = np.zeros(0x7F, dtype=np.float64)
+    for c in range(0x7F):
+        e, m = c >> 3, c & 7
+        out[c] = (m / 8.0) * 2.0 ** -6 if e == 0 else (1.0 + m / 8.0) * 2.0 ** (e - 7)
+    return out
+
+
+_E4M3 = _e4m3_magnitudes()
+
+
+def e4m3_decode(codes: np.ndarray) -> np.ndarray:
+    """E4M3 codes (uint8) to float64 values (codes 0x7F/0xFF never occur here)."""
+    c = np.asarray(codes, dtype=np.uint8)
+    v = _E4M3[np.minimum(c & 0x7F, 0x7E)]
+    return np.where(c & 0x80, -v, v)
+
+
+def round_to_e4m3(v: np.ndarray) -> np.ndarray:
+    """float32 values to E4M3 codes: round to nearest, ties to the even code
+    (the one whose mantissa ends in 0), magnitudes above 448 saturate to 448;
+    the sign is kept (negative values that round to zero give 0x80)."""
+    v = np.asarray(v, dtype=np.float64)
+    a = np.minimum(np.abs(v), _E4M3[-1])
+    hi = np.clip(np.searchsorted(_E4M3, a, side="left"), 0, 0x7E)
+    lo = np.maximum(hi - 1, 0)
+    dlo, dhi = a - _E4M3[lo], _E4M3[hi] - a
+    pick_hi = (dhi < dlo) | ((dhi == dlo) & (hi % 2 == 0))
+    code = np.where(pick_hi, hi, lo).astype(np.uint8)
+    return np.where(np.signbit(v), code | np.uint8(0x80), code).astype(np.uint8)
+
+
+def quantize_rows_e4m3(v: np.ndarray):
+    """Row-wise FP8 quantisation (READING: the pages name FP8 MoE without a
+    format; E4M3 with one float32 scale per row is used).  Per row: amax =
+    max |v|, scale = fl32(amax / 448) (1 for an all-zero row), codes =
+    round_to_e4m3(fl32(v / scale)); both divisions in float32, correctly
+    rounded.  v holds float32-representable values (bf16 or float32 data).
+    Returns (codes uint8 [rows, cols], scales float32 [rows])."""
+    v32 = np.asarray(v, dtype=np.float64).astype(np.float32)
+    amax = np.abs(v32).max(axis=1) if v32.shape[1] else np.zeros(v32.shape[0], np.float32)
+    scale = np.where(amax > 0, amax / np.float32(448.0), np.float32(1.0)).astype(np.float32)
+    q = (v32 / scale[:, None]).astype(np.float32)
+    return round_to_e4m3(q), scale
+
+
+def expert_ffn_fp8(xq, sx, w13q, s13, w2q, s2, I: int, rounded: bool = True) -> np.ndarray:
+    """One expert's SwiGLU FFN with FP8 operands: g = (Xq Wq_gate^T) * sx[row] *
+    s13[unit] in float64 from the decoded codes (and u likewise); a =
+    silu(g) * u stored in bf16 (the intermediate buffer), then quantised per
+    row like the inputs; y = (Aq W2q^T) * sa[row] * s2[feature], stored in
+    bf16 (READING: FP8 is the storage of weights and expert inputs; the
+    intermediate keeps the layer's bf16 and is re-quantised for the down
+    projection)."""
+    X, W = e4m3_decode(xq), e4m3_decode(w13q)
+    sx = np.asarray(sx, dtype=np.float64)[:, None]
+    s13 = np.asarray(s13, dtype=np.float64)[None, :]
+    g = (X @ W[:I].T) * sx * s13[:, :I]
+    u = (X @ W[I:].T) * sx * s13[:, I:]
+    a = to_f64(store(silu(g) * u, "bf16"), "bf16")
+    aq, sa = quantize_rows_e4m3(a)
+    y = (e4m3_decode(aq) @ e4m3_decode(w2q).T) * sa.astype(np.float64)[:, None] * \
+        np.asarray(s2, dtype=np.float64)[None, :]
+    return store(y, "bf16") if rounded else y
+
+
+def layer_forward_fp8(x, w_r, get_w13q, get_w2q, cfg, sel_bias=None, logit_offset=None) -> dict:
+    """The routed layer with FP8 experts: routing and layout as layer_forward (bf16
+    router); x quantised per token (quantize_rows_e4m3) and permuted with its
+    scale; each expert's FFN by expert_ffn_fp8 with its quantised weights
+    get_w13q(e) = (codes [2I, h], scales [2I]) and get_w2q(e) = (codes [h, I],
+    scales [h]); combine as before."""
+    L = router_logits(x, w_r, cfg.dtype, logit_offset)
+    ids, w, keys, allowed = route(L, cfg, sel_bias)
+    lay = dispatch_layout(ids, cfg)
+    xq, sx = quantize_rows_e4m3(to_f64(x, cfg.dtype))
+    R = lay["rows"]
+    yp = np.zeros((R, cfg.h), dtype=np.float64)
+    for e in range(cfg.E):
+        r0, n = int(lay["offsets"][e]), int(lay["kept"][e])
+        if n == 0:
+            continue
+        src = lay["row_src"][r0:r0 + n]
+        (w13q, s13), (w2q, s2) = get_w13q(e), get_w2q(e)
+        yp[r0:r0 + n] = expert_ffn_fp8(xq[src], sx[src], w13q, s13, w2q, s2, cfg.I, rounded=False)
+    yp = store(yp, "bf16")
+    return {"logits": L, "ids": ids, "w": w, "keys": keys, "allowed": allowed, "layout": lay, "xq": xq, "sx": sx,
+            "yp": yp, "y": combine(yp, lay["slot"], w, cfg), "y_exact": combine(yp, lay["slot"], w, cfg,
+                                                                              rounded=False)}
+
+
 # ----------------------------------------------------------------- page formulas
 
 

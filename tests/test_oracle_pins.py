@@ -527,3 +527,88 @@ def test_eplb_map_round_robin_and_layer_unchanged():
             assert r["phys_ids"][t, k] == reps[t % len(reps)]
     assert np.array_equal(r["y"], base["y"])
     assert r["layout"]["balancedness"] > base["layout"]["balancedness"] + 0.2
+
+
+# --------------------------------------------------------------------------- FP8 experts
+def test_e4m3_rounding_matches_torch():
+    """Round-to-nearest-even E4M3 with saturation against torch's float8_e4m3fn
+    cast: random values over the whole range, subnormals, every tie between two
+    neighbouring codes, signed zeros, the largest finite value."""
+    rng = np.random.default_rng(0)
+    mags = oracle.moe_oracle._E4M3
+    mid = (mags[1:] + mags[:-1]) / 2
+    v = np.concatenate([rng.normal(size=20000) * 10, rng.normal(size=5000) * 1e-3, rng.uniform(-448, 448, 5000),
+                        mid, -mid, [0.0, -0.0, 448.0, -448.0, 1e-12, -1e-12]]).astype(np.float32)
+    ref = torch.from_numpy(v).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    assert np.array_equal(oracle.round_to_e4m3(v), ref)
+    codes = np.arange(256, dtype=np.uint8)
+    codes = codes[(codes & 0x7F) != 0x7F]
+    assert np.array_equal(oracle.e4m3_decode(codes),
+                          torch.from_numpy(codes).view(torch.float8_e4m3fn).double().numpy())
+
+
+def test_quantize_rows_definition():
+    """The largest magnitude of a row maps to 448 times its scale; an all-zero
+    row has scale 1 and zero codes; every value comes back within half a step
+    of E4M3 (1/16 relative in the normal range, half the smallest subnormal
+    step below it)."""
+    rng = np.random.default_rng(1)
+    v = (rng.normal(size=(50, 300)) * np.exp(rng.normal(size=(50, 1)) * 3)).astype(np.float32)
+    v[7] = 0
+    q, s = oracle.quantize_rows_e4m3(v)
+    assert s[7] == 1.0 and not q[7].any()
+    dec = oracle.e4m3_decode(q)
+    for r in range(50):
+        if r == 7:
+            continue
+        j = np.argmax(np.abs(v[r]))
+        assert abs(dec[r, j]) == 448.0
+        assert s[r] == np.float32(np.abs(v[r]).max() / np.float32(448))
+        err = np.abs(dec[r] * float(s[r]) - v[r].astype(np.float64))
+        bound = np.maximum(np.abs(v[r]) / 16 * (1 + 1e-6), float(s[r]) * 2.0 ** -10)
+        assert np.all(err <= bound)
+
+
+def test_fp8_expert_ffn_against_torch_float8():
+    """One FP8 expert against a path built from torch: float8_e4m3fn casts of
+    the scaled rows, float64 F.linear and F.silu, the intermediate rounded to
+    bf16 and re-quantised by the same torch casts."""
+    rng = np.random.default_rng(2)
+    h, I, n = 64, 32, 9
+    F = torch.nn.functional
+
+    def tq(a):  # torch-side row quantisation: float32 scale, float8 cast
+        a32 = torch.from_numpy(np.asarray(a, dtype=np.float32))
+        s = a32.abs().amax(dim=1) / 448.0
+        s = torch.where(s > 0, s, torch.ones_like(s))
+        return (a32 / s[:, None]).to(torch.float8_e4m3fn), s
+
+    bf = lambda a: oracle.to_f64(synth.f32_to_bf16_bits(np.asarray(a, np.float32)), "bf16")  # noqa: E731
+    x, w13, w2 = bf(rng.normal(size=(n, h))), bf(rng.normal(size=(2 * I, h)) / 8), bf(rng.normal(size=(h, I)) / 6)
+    (xt, sxt), (wt, swt), (w2t, sw2t) = tq(x), tq(w13), tq(w2)
+    g = F.linear(xt.double(), wt.double()[:I]) * sxt.double()[:, None] * swt.double()[None, :I]
+    u = F.linear(xt.double(), wt.double()[I:]) * sxt.double()[:, None] * swt.double()[None, I:]
+    a = bf((F.silu(g) * u).numpy())
+    at, sat = tq(a)
+    ref = (F.linear(at.double(), w2t.double()) * sat.double()[:, None] * sw2t.double()[None, :]).numpy()
+    u8 = lambda t: t.view(torch.uint8).numpy()  # noqa: E731
+    got = oracle.expert_ffn_fp8(u8(xt), sxt.numpy(), u8(wt), swt.numpy(), u8(w2t), sw2t.numpy(), I, rounded=False)
+    np.testing.assert_allclose(got, ref, rtol=1e-12, atol=1e-12)
+    xq, sx = oracle.quantize_rows_e4m3(x)
+    assert np.array_equal(xq, u8(xt)) and np.array_equal(sx, sxt.numpy())
+
+
+def test_fp8_layer_routes_like_the_bf16_layer():
+    """FP8 experts leave routing and layout untouched, and the output stays
+    close to the bf16 layer's (E4M3 carries 3 mantissa bits)."""
+    cfg, x, wr, W13, W2, _, _ = _block_case("bf16", seed=8)
+    cfg = cfg.replace(shared_I=0)
+    Q13 = [oracle.quantize_rows_e4m3(oracle.to_f64(w, "bf16")) for w in W13]
+    Q2 = [oracle.quantize_rows_e4m3(oracle.to_f64(w, "bf16")) for w in W2]
+    a = oracle.layer_forward(x, wr, lambda e: W13[e], lambda e: W2[e], cfg)
+    b = oracle.layer_forward_fp8(x, wr, lambda e: Q13[e], lambda e: Q2[e], cfg)
+    assert np.array_equal(a["ids"], b["ids"]) and np.array_equal(a["layout"]["slot"], b["layout"]["slot"])
+    ya, yb = oracle.to_f64(a["y"], "bf16"), oracle.to_f64(b["y"], "bf16")
+    # E4M3 steps are at most 1/16 relative: a few quantised stages stay within
+    # a few percent of the output's RMS
+    assert np.sqrt(np.mean((ya - yb) ** 2)) <= 0.1 * np.sqrt(np.mean(ya ** 2))
