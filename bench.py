@@ -57,7 +57,7 @@ def measured_peaks():
 
 def workload_config(w):
     return {"workload": w.name, "T": w.T, "h": w.h, "E": w.E, "K": w.K, "I": w.I, "shared_I": w.shared_I,
-            "n_redundant": w.n_redundant,
+            "n_redundant": w.n_redundant, "fp8": w.fp8,
             "score": w.score,
             "n_groups": w.n_groups, "topk_groups": w.topk_groups, "capacity": w.capacity, "ep_size": w.ep_size,
             "l2": "inputs larger than L2: every step streams all touched expert weights (GBs) through the 126 MB L2",
@@ -170,6 +170,19 @@ def run_ours(args, rank, world, local_rank):
         plan_h = moe.moe_eplb_plan(E, N, w.n_redundant, counts)
         plan = {k: torch.from_numpy(v).cuda() for k, v in plan_h.items() if k != "rank_load"}
         pids = torch.empty(T, K, **i32)
+    fp8 = w.fp8  # FP8 experts: weights quantised once here (not timed)
+    if fp8:
+        q13 = torch.empty(inp["w13"].shape, dtype=torch.uint8, device="cuda")
+        s13 = torch.empty(E, 2 * w.I, dtype=torch.float32, device="cuda")
+        q2 = torch.empty(inp["w2"].shape, dtype=torch.uint8, device="cuda")
+        s2 = torch.empty(E, w.h, dtype=torch.float32, device="cuda")
+        moe.moe_quantize_fp8(inp["w13"].view(-1, w.h), q13.view(-1, w.h), s13.view(-1))
+        moe.moe_quantize_fp8(inp["w2"].view(-1, w.I), q2.view(-1, w.I), s2.view(-1))
+        del inp["w13"], inp["w2"]
+        torch.cuda.synchronize()
+        xq = torch.empty(R, w.h, dtype=torch.uint8, device="cuda")
+        sxp = torch.empty(R, dtype=torch.float32, device="cuda")
+        ws_ffn = moe.alloc_workspace(cfg, moe.MOE_OP_FFN_FP8)
     stages = (("logits", "route") + (("eplb_map",) if eplb else ()) + ("layout", "permute", "ffn")
               + (("shared",) if shared else ()) + ("combine",))
     n_ev = len(stages) + 1
@@ -195,9 +208,14 @@ def run_ours(args, rank, world, local_rank):
         moe.moe_dispatch_layout(cfg, lids, lay.counts, lay.kept, lay.offsets, lay.slot, lay.row_src, lay.n_ij,
                                 lay.rank_bytes, lay.stats, ws_layout)
         rec()
-        moe.moe_permute(cfg, inp["x"], lay.slot, lay.row_src, xp)
+        if fp8:
+            moe.moe_permute_fp8(cfg, inp["x"], lay.slot, xq, sxp)
+        else:
+            moe.moe_permute(cfg, inp["x"], lay.slot, lay.row_src, xp)
         rec()
-        if eplb:
+        if fp8:
+            moe.moe_grouped_ffn_fp8(cfg, xq, sxp, lay.offsets, lay.kept, q13, s13, q2, s2, yp, ws_ffn)
+        elif eplb:
             moe.moe_grouped_ffn_mapped(cfg, xp, lay.offsets, lay.kept, plan["phys_to_log"], inp["w13"], inp["w2"],
                                        yp, ws_ffn)
         else:
@@ -238,15 +256,23 @@ def run_ours(args, rank, world, local_rank):
     # ---- end to end through the public call with host buffers.  Two streams
     # take alternate steps, each with its own workspace and pinned buffers, so
     # the host<->device copies of one step overlap the compute of the other.
-    op_host = moe.MOE_OP_BLOCK_HOST if shared else (moe.MOE_OP_LAYER if eplb else moe.MOE_OP_LAYER_HOST)
+    op_host = (moe.MOE_OP_BLOCK_HOST if shared else moe.MOE_OP_LAYER if eplb else moe.MOE_OP_LAYER_FP8 if fp8
+               else moe.MOE_OP_LAYER_HOST)
+    dev_io = eplb or fp8  # layer calls that take device activations: copies on the lane's stream around them
     lanes = [dict(stream=torch.cuda.Stream(), x=inp["x"].cpu().pin_memory(),
                   y=torch.empty(T, w.h, dtype=dt).pin_memory(), ws=moe.alloc_workspace(cfg, op_host),
-                  xd=torch.empty_like(inp["x"]) if eplb else None, yd=torch.empty_like(y) if eplb else None)
+                  xd=torch.empty_like(inp["x"]) if dev_io else None, yd=torch.empty_like(y) if dev_io else None)
              for _ in range(2)]
 
     def e2e_step(i):
         ln = lanes[i % len(lanes)]
-        if eplb:  # the layer call takes device activations: copies on the lane's stream around it
+        if fp8:
+            with torch.cuda.stream(ln["stream"]):
+                ln["xd"].copy_(ln["x"], non_blocking=True)
+                moe.moe_layer_forward_fp8(cfg, ln["xd"], inp["w_r"], inp["logit_offset"], inp["sel_bias"], q13, s13,
+                                          q2, s2, ln["yd"], None, ln["ws"], stream=ln["stream"])
+                ln["y"].copy_(ln["yd"], non_blocking=True)
+        elif eplb:
             with torch.cuda.stream(ln["stream"]):
                 ln["xd"].copy_(ln["x"], non_blocking=True)
                 moe.moe_layer_forward_eplb(cfg, ln["xd"], inp["w_r"], inp["logit_offset"], inp["sel_bias"],
@@ -293,15 +319,20 @@ def run_ours(args, rank, world, local_rank):
     touched = int((kept > 0).sum())
     if eplb:  # replicas share their logical expert's weights: count each touched logical expert once
         touched = len(set(plan_h["phys_to_log"][kept > 0].tolist()))
-    weight_bytes = touched * 3 * w.h * w.I * ds
-    ffn_bytes = weight_bytes + rows_kept * (2 * w.h + 2 * w.I) * ds
+    if fp8:  # E4M3 weights (+ float32 row scales); E4M3 rows in, bf16 intermediate out, re-quantised, bf16 out
+        weight_bytes = touched * (3 * w.h * w.I + 4 * (2 * w.I + w.h))
+        ffn_bytes = weight_bytes + rows_kept * (w.h + 4 + 2 * w.I * 2 + w.I * 2 + 4 + 2 * w.h)
+    else:
+        weight_bytes = touched * 3 * w.h * w.I * ds
+        ffn_bytes = weight_bytes + rows_kept * (2 * w.h + 2 * w.I) * ds
     ffn_flops = 6.0 * w.h * w.I * rows_kept
     tokens_with_rows = int((lay.slot.view(T, K) >= 0).any(dim=1).sum().item())
     permute_bytes = (tokens_with_rows + rows_kept) * w.h * ds
     combine_bytes = (rows_kept + T) * w.h * ds
     peaks, peak_kind = measured_peaks()
     hbm = float(peaks["hbm_gbs"])
-    tc_peak = float(peaks["bf16_tflops_sustained"])
+    # FP8 dense tensor peak taken as twice the measured bf16 one (the nominal ratio)
+    tc_peak = float(peaks["bf16_tflops_sustained"]) * (2.0 if fp8 else 1.0)
     ffn_s = per_stage["ffn"] / 1e3
     ffn_gbs = ffn_bytes / ffn_s / 1e9
     launches_per_step = 8 + (1 if (w.pad and w.capacity > 0) else 0) + (2 if shared else 0) + (1 if eplb else 0)
@@ -317,7 +348,7 @@ def run_ours(args, rank, world, local_rank):
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
-        "dtype": w.dtype,
+        "dtype": "e4m3" if fp8 else w.dtype,
         "data": "synthetic: seeded counter-based generator (x~N(0,1), weights~N(0,1/h)), no dataset",
         "config": workload_config(w),
         "e2e": {"value": job_throughput(T, world, args.steps, e2e_ms), "unit": "tokens/s",

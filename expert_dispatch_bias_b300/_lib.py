@@ -19,6 +19,7 @@ MOE_F32, MOE_BF16 = 0, 1
 MOE_SOFTMAX, MOE_SIGMOID = 0, 1
 MOE_OP_LAYOUT, MOE_OP_FFN, MOE_OP_LAYER, MOE_OP_LAYER_HOST = 0, 1, 2, 3
 MOE_OP_SHARED, MOE_OP_BLOCK, MOE_OP_BLOCK_HOST = 4, 5, 6
+MOE_OP_FFN_FP8, MOE_OP_LAYER_FP8 = 7, 8
 
 STATUS = {
     0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED", 3: "MOE_ERR_ALIGNMENT",
@@ -34,6 +35,7 @@ EXPORTS = (
     "moe_combine", "moe_layer_forward", "moe_layer_forward_host", "moe_check",
     "moe_shared_ffn", "moe_combine_add", "moe_block_forward", "moe_block_forward_host",
     "moe_eplb_plan", "moe_eplb_map", "moe_grouped_ffn_mapped", "moe_layer_forward_eplb",
+    "moe_quantize_fp8", "moe_permute_fp8", "moe_grouped_ffn_fp8", "moe_layer_forward_fp8",
 )
 
 
@@ -92,6 +94,10 @@ def _load() -> ctypes.CDLL:
         "moe_eplb_map": (c_int32, [cfgp] + [c_void_p] * 5),
         "moe_grouped_ffn_mapped": (c_int32, [cfgp] + [c_void_p] * 8 + [c_size_t, c_void_p]),
         "moe_layer_forward_eplb": (c_int32, [cfgp] + [c_void_p] * 11 + [c_size_t, c_void_p]),
+        "moe_quantize_fp8": (c_int32, [c_int64, c_int32, c_int32, c_void_p, c_void_p, c_void_p, c_void_p]),
+        "moe_permute_fp8": (c_int32, [cfgp] + [c_void_p] * 5),
+        "moe_grouped_ffn_fp8": (c_int32, [cfgp] + [c_void_p] * 10 + [c_size_t, c_void_p]),
+        "moe_layer_forward_fp8": (c_int32, [cfgp] + [c_void_p] * 11 + [c_size_t, c_void_p]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -280,6 +286,37 @@ def moe_layer_forward_eplb(cfg, x, w_r, logit_offset, sel_bias, w13, w2, rep_off
                                       _ptr(y), ctypes.byref(out) if out is not None else None, _ptr(workspace),
                                       workspace.numel() * workspace.element_size(), _stream(stream)),
            "moe_layer_forward_eplb")
+
+
+def moe_quantize_fp8(src, codes, scales, stream=None) -> None:
+    """Row quantisation of a 2-D bf16/float32 tensor into E4M3 codes (uint8) and
+    float32 row scales (see include/moe.h)."""
+    rows, cols = src.shape[0], src.numel() // max(src.shape[0], 1)
+    import torch
+    dt = MOE_BF16 if src.dtype == torch.bfloat16 else MOE_F32
+    _check(lib.moe_quantize_fp8(rows, cols, dt, _ptr(src), _ptr(codes), _ptr(scales), _stream(stream)),
+           "moe_quantize_fp8")
+
+
+def moe_permute_fp8(cfg, x, slot, xq, sx, stream=None) -> None:
+    _check(lib.moe_permute_fp8(ctypes.byref(cfg), _ptr(x), _ptr(slot), _ptr(xq), _ptr(sx), _stream(stream)),
+           "moe_permute_fp8")
+
+
+def moe_grouped_ffn_fp8(cfg, xq, sx, offsets, kept, w13q, s13, w2q, s2, yp, workspace, stream=None) -> None:
+    _check(lib.moe_grouped_ffn_fp8(ctypes.byref(cfg), _ptr(xq), _ptr(sx), _ptr(offsets), _ptr(kept), _ptr(w13q),
+                                   _ptr(s13), _ptr(w2q), _ptr(s2), _ptr(yp), _ptr(workspace),
+                                   workspace.numel() * workspace.element_size(), _stream(stream)),
+           "moe_grouped_ffn_fp8")
+
+
+def moe_layer_forward_fp8(cfg, x, w_r, logit_offset, sel_bias, w13q, s13, w2q, s2, y, out: Optional[MoeLayerOut],
+                          workspace, stream=None) -> None:
+    _check(lib.moe_layer_forward_fp8(ctypes.byref(cfg), _ptr(x), _ptr(w_r), _ptr(logit_offset), _ptr(sel_bias),
+                                     _ptr(w13q), _ptr(s13), _ptr(w2q), _ptr(s2), _ptr(y),
+                                     ctypes.byref(out) if out is not None else None, _ptr(workspace),
+                                     workspace.numel() * workspace.element_size(), _stream(stream)),
+           "moe_layer_forward_fp8")
 
 
 def moe_check(stream=None) -> int:

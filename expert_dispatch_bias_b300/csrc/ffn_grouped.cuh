@@ -66,6 +66,8 @@ struct FgParams {
   __nv_bfloat16* out;       // [R, ldo]
   int64_t ldo;
   const int32_t* w_map;     // expert -> its weight matrices (replicas share a logical expert's), or null
+  const float* w_scale;     // FP8: scale of every weight row [experts * a_rows]
+  const float* x_scale;     // FP8: scale of every token row [R]
 };
 
 // Tensor maps of the token rows with boxes of 128, 64, 32 and 16 rows.
@@ -106,17 +108,25 @@ __device__ __forceinline__ uint32_t round16(int n) { return (uint32_t)((n + 15) 
 // Epilogue of one 32-token chunk: v (and u, SwiGLU) hold this warp's 32
 // features x 32 tokens; the bf16 results are transposed through the warp's
 // shared buffer and each lane stores the 64-byte piece of token row r0 + c + lane.
-template <int EPI>
+template <int EPI, bool FP8>
 __device__ __forceinline__ void fg_chunk(const uint32_t* v, const uint32_t* u, int c, int n, int r0, int feat0,
-                                         bool feat_ok, const FgParams& p, __nv_bfloat16* xs) {
+                                         bool feat_ok, const FgParams& p, __nv_bfloat16* xs, float wsg, float wsu) {
   const int lane = threadIdx.x & 31;
+  // FP8: token i's scale (lane i loads it; shuffled to every feature lane)
+  const float xsc = (FP8 && c + lane < n) ? p.x_scale[r0 + c + lane] : 0.0f;
 #pragma unroll
   for (int i = 0; i < 32; ++i) {
-    const float g = __uint_as_float(v[i]);
+    float g = __uint_as_float(v[i]);
+    float uu = EPI == kTcSwiglu ? __uint_as_float(u[i]) : 0.0f;
+    if (FP8) {
+      const float xi = __shfl_sync(0xffffffffu, xsc, i);
+      g = g * wsg * xi;
+      uu = uu * wsu * xi;
+    }
     // silu(g) * u with the fast exponential and division (about 2 ulp of
     // float32, far below the bf16 rounding of the result); the IEEE forms made
     // this loop the slowest part of the tile
-    const float a = EPI == kTcSwiglu ? __fdividef(g, 1.0f + __expf(-g)) * __uint_as_float(u[i]) : g;
+    const float a = EPI == kTcSwiglu ? __fdividef(g, 1.0f + __expf(-g)) * uu : g;
     xs[i * kFgXsStride + lane] = __float2bfloat16_rn(a);
   }
   __syncwarp();
@@ -133,9 +143,10 @@ __device__ __forceinline__ void fg_chunk(const uint32_t* v, const uint32_t* u, i
 // (columns col0.., and col_up.. for the SwiGLU's up half), two chunks in
 // flight: the next chunk's tcgen05.ld runs while this one is transposed and
 // stored.
-template <int EPI>
+template <int EPI, bool FP8>
 __device__ __forceinline__ void fg_drain(uint32_t t_lane, uint32_t col0, uint32_t col_up, int n, int r0,
-                                         int feat0, bool feat_ok, const FgParams& p, __nv_bfloat16* xs) {
+                                         int feat0, bool feat_ok, const FgParams& p, __nv_bfloat16* xs,
+                                         float wsg = 1.0f, float wsu = 1.0f) {
   constexpr bool kUp = EPI == kTcSwiglu;
   uint32_t va[32], vb[32], ua[kUp ? 32 : 1], ub[kUp ? 32 : 1];
   tmem_ld<32>(t_lane + col0, va);
@@ -149,7 +160,7 @@ __device__ __forceinline__ void fg_drain(uint32_t t_lane, uint32_t col0, uint32_
       tmem_ld<32>(t_lane + col0 + c + 32, vb);
       if (kUp) tmem_ld<32>(t_lane + col_up + c + 32, ub);
     }
-    fg_chunk<EPI>(va, ua, c, n, r0, feat0, feat_ok, p, xs);
+    fg_chunk<EPI, FP8>(va, ua, c, n, r0, feat0, feat_ok, p, xs, wsg, wsu);
     if (c + 32 >= n) break;
     tmem_ld_wait();
     tmem_regs_ready(vb);
@@ -158,11 +169,13 @@ __device__ __forceinline__ void fg_drain(uint32_t t_lane, uint32_t col0, uint32_
       tmem_ld<32>(t_lane + col0 + c + 64, va);
       if (kUp) tmem_ld<32>(t_lane + col_up + c + 64, ua);
     }
-    fg_chunk<EPI>(vb, ub, c + 32, n, r0, feat0, feat_ok, p, xs);
+    fg_chunk<EPI, FP8>(vb, ub, c + 32, n, r0, feat0, feat_ok, p, xs, wsg, wsu);
   }
 }
 
-template <int EPI, int BT, int STAGES>
+// FP8: E4M3 operands (tcgen05.mma kind::f8f6f4), 128-element k-blocks (the
+// same 128-byte rows), results scaled by weight-row and token scales.
+template <int EPI, int BT, int STAGES, bool FP8 = false>
 __global__ void __launch_bounds__(kFgThreads, 1)
     ffn_grouped_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_constant__ FgTokenMaps maps,
                        FgParams p) {
@@ -242,7 +255,7 @@ __global__ void __launch_bounds__(kFgThreads, 1)
           uint8_t* sw = ring + (size_t)stage * S::kStageBytes;
           uint8_t* sx = sw + 2 * S::kWBytes;
           mbar_expect_tx(&full_bar[stage], 2 * S::kWBytes + x_bytes);
-          const int kx = kb * kTcBK;
+          const int kx = kb * (FP8 ? 128 : kTcBK);
           tma_load_2d(sw, &map_w, kx, (int)a0, &full_bar[stage]);
           tma_load_2d(sw + S::kWBytes, &map_w, kx, (int)a1, &full_bar[stage]);
           {
@@ -277,7 +290,7 @@ __global__ void __launch_bounds__(kFgThreads, 1)
       for (int t = blockIdx.x; t < total_tiles && !abort_flag; t += gridDim.x) {
         const FgTile tl = fg_decode<BT>(t, mbp, p);
         const bool big = tl.n > 128;
-        const uint32_t idesc = umma_idesc_bf16(128, (int)round16(tl.n));
+        const uint32_t idesc = FP8 ? umma_idesc_e4m3(128, (int)round16(tl.n)) : umma_idesc_bf16(128, (int)round16(tl.n));
         // big: D0 = slot 0, D1 = slot 1; else D0, D1 = the two halves of `slot`
         const int s0 = big ? 0 : slot;
         const uint32_t c0 = tmem_base + (uint32_t)(s0 * 256), c1 = big ? tmem_base + 256u : c0 + 128u;
@@ -303,8 +316,13 @@ __global__ void __launch_bounds__(kFgThreads, 1)
 #pragma unroll
           for (int k = 0; k < kTcBK / 16; ++k) {
             const uint32_t acc = (kb | k) != 0 ? 1u : 0u;
-            umma_bf16(c0, dw0 + 2 * k, dx + 2 * k, idesc, acc);
-            umma_bf16(c1, dw1 + 2 * k, dx + 2 * k, idesc, acc);
+            if (FP8) {
+              umma_e4m3(c0, dw0 + 2 * k, dx + 2 * k, idesc, acc);
+              umma_e4m3(c1, dw1 + 2 * k, dx + 2 * k, idesc, acc);
+            } else {
+              umma_bf16(c0, dw0 + 2 * k, dx + 2 * k, idesc, acc);
+              umma_bf16(c1, dw1 + 2 * k, dx + 2 * k, idesc, acc);
+            }
           }
           umma_commit(&empty_bar[stage]);
           if (++stage == STAGES) {
@@ -345,17 +363,25 @@ __global__ void __launch_bounds__(kFgThreads, 1)
         break;
       }
       tc_fence_after();
+      const int64_t wrow = FP8 ? (int64_t)(p.w_map != nullptr ? p.w_map[tl.e] : tl.e) * p.a_rows : 0;
       if (EPI == kTcSwiglu) {
         const int f0 = 128 * tl.ft + 32 * quarter;
-        fg_drain<kTcSwiglu>(t_lane, c0, c1, tl.n, tl.r0, f0, f0 + 32 <= p.n_valid, p, xs);
+        float wsg = 1.0f, wsu = 1.0f;
+        if (FP8 && f0 + 32 <= p.n_valid) {
+          wsg = p.w_scale[wrow + f0 + lane];
+          wsu = p.w_scale[wrow + p.up_rows + f0 + lane];
+        }
+        fg_drain<kTcSwiglu, FP8>(t_lane, c0, c1, tl.n, tl.r0, f0, f0 + 32 <= p.n_valid, p, xs, wsg, wsu);
       } else {
         const int f0 = 256 * tl.ft + 32 * quarter;
-        fg_drain<kTcStore>(t_lane, c0, 0, tl.n, tl.r0, f0, f0 + 32 <= p.n_valid, p, xs);
+        const float ws0 = (FP8 && f0 + 32 <= p.n_valid) ? p.w_scale[wrow + f0 + lane] : 1.0f;
+        const float ws1 = (FP8 && f0 + 160 <= p.n_valid) ? p.w_scale[wrow + f0 + 128 + lane] : 1.0f;
+        fg_drain<kTcStore, FP8>(t_lane, c0, 0, tl.n, tl.r0, f0, f0 + 32 <= p.n_valid, p, xs, ws0);
         if (big) {  // D0 alone fills slot 0: hand it back before draining D1
           tc_fence_before();
           mbar_arrive(&tmem_empty[0]);
         }
-        fg_drain<kTcStore>(t_lane, c1, 0, tl.n, tl.r0, f0 + 128, f0 + 160 <= p.n_valid, p, xs);
+        fg_drain<kTcStore, FP8>(t_lane, c1, 0, tl.n, tl.r0, f0 + 128, f0 + 160 <= p.n_valid, p, xs, ws1);
       }
       tc_fence_before();
       if (big) {

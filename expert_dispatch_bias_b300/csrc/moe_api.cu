@@ -22,6 +22,7 @@
 #include "simt_gemm.cuh"
 #include "tc_gemm.cuh"
 #include "ffn_grouped.cuh"
+#include "fp8.cuh"
 
 using namespace moe;
 
@@ -145,6 +146,7 @@ struct LayerBuffers {
   void* xdev;
   void* ydev;
   int32_t* phys_ids;   // physical expert of every (t, k) (replicas)
+  float* xscale;       // FP8: scale of every permuted row [R]
   void* ys;            // shared expert output [T, h] (block)
   void* shared_ws;     // shared expert intermediate [T, shared_I] (block)
   size_t total;
@@ -152,7 +154,9 @@ struct LayerBuffers {
 
 size_t shared_ws_bytes(const moe_config& c) { return align_up((size_t)c.T * c.shared_I * ds_of(c), 256) + 256; }
 
-LayerBuffers carve_layer(const moe_config& c, void* ws, bool host_io, bool block = false) {
+size_t ffn_fp8_ws_bytes(const moe_config& c);
+
+LayerBuffers carve_layer(const moe_config& c, void* ws, bool host_io, bool block = false, bool fp8 = false) {
   Carver cv(ws);
   LayerBuffers b;
   const int64_t A = (int64_t)c.T * c.K, R = rows_of(c);
@@ -173,7 +177,8 @@ LayerBuffers carve_layer(const moe_config& c, void* ws, bool host_io, bool block
   b.stats = cv.take<moe_layout_stats>(1);
   b.xp = cv.take<char>((size_t)R * c.h * ds);
   b.yp = cv.take<char>((size_t)R * c.h * ds);
-  b.inter = cv.take<char>((size_t)R * c.I * ds);
+  b.inter = cv.take<char>(fp8 ? ffn_fp8_ws_bytes(c) : (size_t)R * c.I * ds);
+  b.xscale = fp8 ? cv.take<float>(R) : nullptr;
   b.xdev = host_io ? cv.take<char>((size_t)c.T * c.h * ds) : nullptr;
   b.ydev = host_io ? cv.take<char>((size_t)c.T * c.h * ds) : nullptr;
   b.ys = block ? cv.take<char>((size_t)c.T * c.h * ds) : nullptr;
@@ -425,16 +430,19 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
 
 // 2-D bf16 K-major tensor [rows, inner] read in boxes of box_rows x 64 elements
 // with the 128-byte swizzle the MMA descriptors expect.
-moe_status make_tensor_map(CUtensorMap* map, const void* base, uint64_t inner, uint64_t rows, uint32_t box_rows) {
+moe_status make_tensor_map(CUtensorMap* map, const void* base, uint64_t inner, uint64_t rows, uint32_t box_rows,
+                           bool bytes = false) {
   PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
   if (enc == nullptr) return MOE_ERR_CUDA;
+  // bf16 elements, or (bytes) 8-bit codes; either way 128-byte box rows
   const cuuint64_t dims[2] = {inner, rows};
-  const cuuint64_t strides[1] = {inner * 2};
-  const cuuint32_t box[2] = {(cuuint32_t)kTcBK, box_rows};
+  const cuuint64_t strides[1] = {inner * (bytes ? 1 : 2)};
+  const cuuint32_t box[2] = {(cuuint32_t)(bytes ? 128 : kTcBK), box_rows};
   const cuuint32_t estr[2] = {1, 1};
-  const CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
-                         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  const CUresult r = enc(map, bytes ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
+                         const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                         CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? MOE_OK : MOE_ERR_CUDA;
 }
 
@@ -615,6 +623,88 @@ moe_status launch_logits(const moe_config& c, const void* x, const void* w_r, co
   }
 }
 
+// FP8 experts: gate/up (E4M3 codes of x rows and w13 rows) with the SwiGLU
+// epilogue into the bf16 intermediate, the intermediate re-quantised per row,
+// then the down projection into yp.  Weights as M only (experts expected to see
+// at most MOE_FFN_SWAP_MAX_ROWS rows).  ws: inter bf16 [R, I], codes [R, I],
+// scales [R].
+size_t ffn_fp8_ws_bytes(const moe_config& c) {
+  const size_t R = (size_t)rows_of(c);
+  return align_up(R * c.I * 2, 256) + align_up(R * c.I, 256) + align_up(R * 4, 256) + 256;
+}
+
+moe_status launch_ffn_fp8(const moe_config& c, const uint8_t* xq, const float* sx, const int32_t* offsets,
+                          const int32_t* kept, const int32_t* w_map, int n_w, const uint8_t* w13q,
+                          const float* s13, const uint8_t* w2q, const float* s2, void* yp, void* ws,
+                          cudaStream_t st) {
+  const int64_t R = rows_of(c);
+  if (R == 0) return MOE_OK;
+  if (expected_rows_per_expert(c) > MOE_FFN_SWAP_MAX_ROWS) return MOE_ERR_UNSUPPORTED;
+  if ((int64_t)n_w * 2 * c.I >= INT32_MAX || (int64_t)n_w * c.h >= INT32_MAX) return MOE_ERR_UNSUPPORTED;
+  char* w = static_cast<char*>(ws);
+  __nv_bfloat16* inter = reinterpret_cast<__nv_bfloat16*>(w);
+  uint8_t* interq = reinterpret_cast<uint8_t*>(w + align_up((size_t)R * c.I * 2, 256));
+  float* sinter = reinterpret_cast<float*>(w + align_up((size_t)R * c.I * 2, 256) + align_up((size_t)R * c.I, 256));
+  using S = FgShape<kFgTileRows, kFgStages>;
+  CUtensorMap w1m, w2m;
+  FgTokenMaps x1, x2;
+  MOE_TRY(make_tensor_map(&w1m, w13q, c.h, (uint64_t)n_w * 2 * c.I, 128, true));
+  MOE_TRY(make_tensor_map(&w2m, w2q, c.I, (uint64_t)n_w * c.h, 128, true));
+  for (int i = 0; i < 4; ++i) {
+    MOE_TRY(make_tensor_map(&x1.m[i], xq, c.h, R, 128u >> i, true));
+    MOE_TRY(make_tensor_map(&x2.m[i], interq, c.I, R, 128u >> i, true));
+  }
+  FgParams p1{};
+  p1.offsets = offsets;
+  p1.kept = kept;
+  p1.E = nphys(c);
+  p1.w_map = w_map;
+  p1.f_tiles = (c.I + 127) / 128;
+  p1.k_blocks = c.h / 128;
+  p1.a_rows = 2LL * c.I;
+  p1.up_rows = c.I;
+  p1.n_valid = c.I;
+  p1.out = inter;
+  p1.ldo = c.I;
+  p1.w_scale = s13;
+  p1.x_scale = sx;
+  FgParams p2 = p1;
+  p2.f_tiles = (c.h + 255) / 256;
+  p2.k_blocks = c.I / 128;
+  p2.a_rows = c.h;
+  p2.up_rows = 0;
+  p2.n_valid = c.h;
+  p2.out = static_cast<__nv_bfloat16*>(yp);
+  p2.ldo = c.h;
+  p2.w_scale = s2;
+  p2.x_scale = sinter;
+  const int grid = device_info().sms;
+  auto k1 = ffn_grouped_kernel<kTcSwiglu, kFgTileRows, kFgStages, true>;
+  auto k2 = ffn_grouped_kernel<kTcStore, kFgTileRows, kFgStages, true>;
+  CUDA_TRY(allow_smem(k1, S::kDynSmem));
+  CUDA_TRY(allow_smem(k2, S::kDynSmem));
+  k1<<<grid, kFgThreads, S::kDynSmem, st>>>(w1m, x1, p1);
+  CUDA_TRY(cudaGetLastError());
+  int64_t qb = (R + 7) / 8;
+  if (qb > (int64_t)grid * 16) qb = (int64_t)grid * 16;
+  quant_rows_kernel<__nv_bfloat16><<<(unsigned)qb, 256, 0, st>>>(inter, R, c.I, interq, sinter);
+  CUDA_TRY(cudaGetLastError());
+  k2<<<grid, kFgThreads, S::kDynSmem, st>>>(w2m, x2, p2);
+  CUDA_TRY(cudaGetLastError());
+  return MOE_OK;
+}
+
+moe_status launch_permute_fp8(const moe_config& c, const void* x, const int32_t* slot, uint8_t* xq, float* sx,
+                              cudaStream_t st) {
+  if (c.T == 0) return MOE_OK;
+  int64_t blocks = (c.T + 7) / 8;
+  if (blocks > (int64_t)device_info().sms * 16) blocks = (int64_t)device_info().sms * 16;
+  quant_permute_kernel<__nv_bfloat16><<<(unsigned)blocks, 256, 0, st>>>(static_cast<const __nv_bfloat16*>(x), slot,
+                                                                       c.T, c.K, c.h, xq, sx);
+  CUDA_TRY(cudaGetLastError());
+  return MOE_OK;
+}
+
 moe_status launch_ffn(const moe_config& c, const void* xp, const int32_t* offsets, const int32_t* kept,
                       const int32_t* w_map, int n_w, const void* w13, const void* w2, void* yp, void* inter,
                       cudaStream_t st) {
@@ -704,6 +794,14 @@ moe_status launch_shared_ffn(const moe_config& c, const void* x, const void* w13
 }
 
 // Device copy of an EPLB plan (moe_eplb_plan's outputs), or all null.
+// FP8 expert weights (moe_quantize_fp8 codes and row scales), or all null.
+struct Fp8Weights {
+  const uint8_t* w13q = nullptr;
+  const float* s13 = nullptr;
+  const uint8_t* w2q = nullptr;
+  const float* s2 = nullptr;
+};
+
 struct EplbDev {
   const int32_t* rep_offsets = nullptr;
   const int32_t* rep_phys = nullptr;
@@ -725,7 +823,7 @@ moe_status launch_eplb_map(const moe_config& c, const int32_t* ids, const EplbDe
 moe_status layer_core(const moe_config& c, const void* x, const void* w_r, const float* logit_offset,
                       const float* sel_bias, const void* w13, const void* w2, const void* w13s, const void* w2s,
                       void* y, const moe_layer_out* out, const LayerBuffers& b, cudaStream_t st,
-                      const EplbDev& plan = EplbDev()) {
+                      const EplbDev& plan = EplbDev(), const Fp8Weights& q = Fp8Weights()) {
   moe_layer_out o{};
   if (out != nullptr) o = *out;
   float* logits = o.logits ? o.logits : b.logits;
@@ -747,9 +845,15 @@ moe_status layer_core(const moe_config& c, const void* x, const void* w_r, const
     lids = b.phys_ids;
   }
   MOE_TRY(launch_layout(c, lids, counts, kept, offsets, slot, row_src, n_ij, rank_bytes, stats, b.layout_ws, st));
-  MOE_TRY(launch_permute(c, x, slot, row_src, b.xp, st));
-  MOE_TRY(launch_ffn(c, b.xp, offsets, kept, plan.phys_to_log, plan.phys_to_log ? c.E : nphys(c), w13, w2, b.yp,
-                     b.inter, st));
+  if (q.w13q != nullptr) {  // FP8 experts: quantise x per token while permuting
+    MOE_TRY(launch_permute_fp8(c, x, slot, static_cast<uint8_t*>(b.xp), b.xscale, st));
+    MOE_TRY(launch_ffn_fp8(c, static_cast<const uint8_t*>(b.xp), b.xscale, offsets, kept, plan.phys_to_log,
+                           plan.phys_to_log ? c.E : nphys(c), q.w13q, q.s13, q.w2q, q.s2, b.yp, b.inter, st));
+  } else {
+    MOE_TRY(launch_permute(c, x, slot, row_src, b.xp, st));
+    MOE_TRY(launch_ffn(c, b.xp, offsets, kept, plan.phys_to_log, plan.phys_to_log ? c.E : nphys(c), w13, w2, b.yp,
+                       b.inter, st));
+  }
   if (b.ys != nullptr)
     MOE_TRY(launch_shared_ffn(c, x, w13s, w2s, b.ys, static_cast<char*>(b.shared_ws) + 256, st));
   MOE_TRY(launch_combine(c, b.yp, slot, w, b.ys, y, st));
@@ -806,6 +910,8 @@ moe_status moe_workspace_size(const moe_config* cfg, int32_t op, size_t* bytes) 
     case MOE_OP_SHARED: *bytes = shared_ws_bytes(*cfg); return MOE_OK;
     case MOE_OP_BLOCK: *bytes = carve_layer(*cfg, nullptr, false, true).total; return MOE_OK;
     case MOE_OP_BLOCK_HOST: *bytes = carve_layer(*cfg, nullptr, true, true).total; return MOE_OK;
+    case MOE_OP_FFN_FP8: *bytes = ffn_fp8_ws_bytes(*cfg); return MOE_OK;
+    case MOE_OP_LAYER_FP8: *bytes = carve_layer(*cfg, nullptr, false, false, true).total; return MOE_OK;
   }
   return MOE_ERR_INVALID_ARG;
 }
@@ -1141,6 +1247,98 @@ moe_status moe_layer_forward_eplb(const moe_config* cfg, const void* x, const vo
   plan.phys_to_log = phys_to_log;
   return layer_core(*cfg, x, w_r, logit_offset, sel_bias, w13, w2, nullptr, nullptr, y, out, b, as_stream(stream),
                     plan);
+}
+
+moe_status fp8_config_ok(const moe_config* cfg) {
+  MOE_TRY(validate(cfg));
+  if (cfg->dtype != MOE_BF16 || cfg->h % 128 != 0 || cfg->I % 128 != 0) return MOE_ERR_UNSUPPORTED;
+  if (cfg->shared_I != 0) return MOE_ERR_UNSUPPORTED;
+  return MOE_OK;
+}
+
+moe_status moe_quantize_fp8(int64_t rows, int32_t cols, int32_t dtype, const void* src, uint8_t* codes,
+                            float* scales, void* stream) {
+  if (rows < 0 || cols <= 0 || cols % 16 != 0) return MOE_ERR_INVALID_ARG;
+  if (dtype != MOE_F32 && dtype != MOE_BF16) return MOE_ERR_INVALID_ARG;
+  if (rows == 0) return MOE_OK;
+  MOE_TRY(check_dtype_ptr(src));
+  MOE_TRY(check_dtype_ptr(codes));
+  MOE_TRY(check_ptr(scales, 4));
+  int64_t blocks = (rows + 7) / 8;
+  if (blocks > (int64_t)device_info().sms * 16) blocks = (int64_t)device_info().sms * 16;
+  if (dtype == MOE_BF16)
+    quant_rows_kernel<__nv_bfloat16><<<(unsigned)blocks, 256, 0, as_stream(stream)>>>(
+        static_cast<const __nv_bfloat16*>(src), rows, cols, codes, scales);
+  else
+    quant_rows_kernel<float><<<(unsigned)blocks, 256, 0, as_stream(stream)>>>(static_cast<const float*>(src), rows,
+                                                                              cols, codes, scales);
+  CUDA_TRY(cudaGetLastError());
+  return MOE_OK;
+}
+
+moe_status moe_permute_fp8(const moe_config* cfg, const void* x, const int32_t* slot, uint8_t* xq, float* sx,
+                           void* stream) {
+  MOE_TRY(fp8_config_ok(cfg));
+  if (cfg->T > 0) {
+    MOE_TRY(check_dtype_ptr(x));
+    MOE_TRY(check_ptr(slot, 4));
+  }
+  if (rows_of(*cfg) > 0) {
+    MOE_TRY(check_dtype_ptr(xq));
+    MOE_TRY(check_ptr(sx, 4));
+  }
+  return launch_permute_fp8(*cfg, x, slot, xq, sx, as_stream(stream));
+}
+
+moe_status moe_grouped_ffn_fp8(const moe_config* cfg, const uint8_t* xq, const float* sx, const int32_t* offsets,
+                               const int32_t* kept, const uint8_t* w13q, const float* s13, const uint8_t* w2q,
+                               const float* s2, void* yp, void* workspace, size_t workspace_bytes, void* stream) {
+  MOE_TRY(fp8_config_ok(cfg));
+  if (cfg->n_redundant != 0) return MOE_ERR_UNSUPPORTED;
+  if (rows_of(*cfg) > 0) {
+    MOE_TRY(check_dtype_ptr(xq));
+    MOE_TRY(check_ptr(sx, 4));
+    MOE_TRY(check_dtype_ptr(yp));
+  }
+  MOE_TRY(check_ptr(offsets, 4));
+  MOE_TRY(check_ptr(kept, 4));
+  MOE_TRY(check_dtype_ptr(w13q));
+  MOE_TRY(check_dtype_ptr(w2q));
+  MOE_TRY(check_ptr(s13, 4));
+  MOE_TRY(check_ptr(s2, 4));
+  MOE_TRY(check_ptr(workspace, 256));
+  if (workspace_bytes < ffn_fp8_ws_bytes(*cfg)) return MOE_ERR_WORKSPACE_TOO_SMALL;
+  return launch_ffn_fp8(*cfg, xq, sx, offsets, kept, nullptr, cfg->E, w13q, s13, w2q, s2, yp, workspace,
+                        as_stream(stream));
+}
+
+moe_status moe_layer_forward_fp8(const moe_config* cfg, const void* x, const void* w_r, const float* logit_offset,
+                                 const float* sel_bias, const uint8_t* w13q, const float* s13, const uint8_t* w2q,
+                                 const float* s2, void* y, const moe_layer_out* out, void* workspace,
+                                 size_t workspace_bytes, void* stream) {
+  MOE_TRY(fp8_config_ok(cfg));
+  if (cfg->n_redundant != 0) return MOE_ERR_UNSUPPORTED;
+  if (cfg->T > 0) {
+    MOE_TRY(check_dtype_ptr(x));
+    MOE_TRY(check_dtype_ptr(y));
+  }
+  MOE_TRY(check_dtype_ptr(w_r));
+  MOE_TRY(check_opt_ptr(logit_offset, 4));
+  MOE_TRY(check_opt_ptr(sel_bias, 4));
+  MOE_TRY(check_dtype_ptr(w13q));
+  MOE_TRY(check_dtype_ptr(w2q));
+  MOE_TRY(check_ptr(s13, 4));
+  MOE_TRY(check_ptr(s2, 4));
+  MOE_TRY(check_ptr(workspace, 256));
+  const LayerBuffers b = carve_layer(*cfg, workspace, false, false, true);
+  if (workspace_bytes < b.total) return MOE_ERR_WORKSPACE_TOO_SMALL;
+  Fp8Weights q;
+  q.w13q = w13q;
+  q.s13 = s13;
+  q.w2q = w2q;
+  q.s2 = s2;
+  return layer_core(*cfg, x, w_r, logit_offset, sel_bias, nullptr, nullptr, nullptr, nullptr, y, out, b,
+                    as_stream(stream), EplbDev(), q);
 }
 
 moe_status moe_check(void* stream) {

@@ -64,7 +64,9 @@ typedef enum {
   MOE_OP_LAYER_HOST = 3,  /* moe_layer_forward_host */
   MOE_OP_SHARED = 4,      /* moe_shared_ffn */
   MOE_OP_BLOCK = 5,       /* moe_block_forward */
-  MOE_OP_BLOCK_HOST = 6   /* moe_block_forward_host */
+  MOE_OP_BLOCK_HOST = 6,  /* moe_block_forward_host */
+  MOE_OP_FFN_FP8 = 7,     /* moe_grouped_ffn_fp8 */
+  MOE_OP_LAYER_FP8 = 8    /* moe_layer_forward_fp8 */
 } moe_op;
 
 /* Layer description.  Limits: T >= 0; h % 64 == 0; I % 64 == 0; 1 <= E <= 1024;
@@ -319,6 +321,44 @@ moe_status moe_layer_forward_eplb(const moe_config* cfg, const void* x, const vo
                                   const float* sel_bias, const void* w13, const void* w2, const int32_t* rep_offsets,
                                   const int32_t* rep_phys, const int32_t* phys_to_log, void* y,
                                   const moe_layer_out* out, void* workspace, size_t workspace_bytes, void* stream);
+
+/* FP8 experts.  The pages name FP8 MoE (expert weights and activations in 8
+ * bits) without a format; this library uses OCP E4M3 codes (round to nearest
+ * even, saturating at 448) with one float32 scale per row: scale = amax/448
+ * (1 for an all-zero row), code = E4M3(v / scale), both divisions in IEEE
+ * float32.  Weights are quantised per output row (w13 rows = gate/up units, w2
+ * rows = output features), expert inputs per token, and the bf16 SwiGLU
+ * intermediate per row before the down projection.  FP8 calls need a bf16
+ * layer with h % 128 == 0, I % 128 == 0, no shared expert and no replicas, and
+ * experts expected to see at most 160 rows (else MOE_ERR_UNSUPPORTED). */
+
+/* Row quantisation: codes[r, c] and scales[r] of src [rows, cols] (dtype
+ * MOE_BF16 or MOE_F32; cols % 16 == 0; src and codes 16-byte aligned), e.g.
+ * w13 viewed as [E*2I, h] and w2 as [E*h, I], once, before the layer runs. */
+moe_status moe_quantize_fp8(int64_t rows, int32_t cols, int32_t dtype, const void* src, uint8_t* codes,
+                            float* scales, void* stream);
+
+/* moe_permute with the expert inputs quantised: each token's row x[t] is
+ * quantised once and its codes and scale written to every kept permuted row
+ * slot[t,k]: xq [R,h] uint8, sx [R] float32 (pad rows are not written). */
+moe_status moe_permute_fp8(const moe_config* cfg, const void* x, const int32_t* slot, uint8_t* xq, float* sx,
+                           void* stream);
+
+/* moe_grouped_ffn on FP8 operands: g = (xq . w13q_gate) * sx[r] * s13[unit], u
+ * likewise, a = silu(g) * u stored in bf16 and re-quantised per row; yp[r] =
+ * (aq . w2q) * sa[r] * s2[feature], bf16; float32 accumulation.  xq [R,h],
+ * sx [R]; w13q [E,2I,h] uint8, s13 [E,2I] float32; w2q [E,h,I] uint8, s2 [E,h];
+ * yp [R,h] bf16; workspace >= moe_workspace_size(MOE_OP_FFN_FP8). */
+moe_status moe_grouped_ffn_fp8(const moe_config* cfg, const uint8_t* xq, const float* sx, const int32_t* offsets,
+                               const int32_t* kept, const uint8_t* w13q, const float* s13, const uint8_t* w2q,
+                               const float* s2, void* yp, void* workspace, size_t workspace_bytes, void* stream);
+
+/* moe_layer_forward with FP8 experts: bf16 router and routing, moe_permute_fp8,
+ * moe_grouped_ffn_fp8, combine.  workspace >= moe_workspace_size(MOE_OP_LAYER_FP8). */
+moe_status moe_layer_forward_fp8(const moe_config* cfg, const void* x, const void* w_r, const float* logit_offset,
+                                 const float* sel_bias, const uint8_t* w13q, const float* s13, const uint8_t* w2q,
+                                 const float* s2, void* y, const moe_layer_out* out, void* workspace,
+                                 size_t workspace_bytes, void* stream);
 
 /* Synchronises `stream`, then reports and clears the sticky device error word of
  * the current device: MOE_ERR_DEVICE_TIMEOUT, MOE_ERR_DEVICE_BAD_INDEX,

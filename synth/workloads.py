@@ -45,6 +45,7 @@ class Workload:
     zipf_s: Optional[float] = None                   # Zipf logit offsets
     shared_I: int = 0                                # shared expert intermediate (0: none)
     n_redundant: int = 0                             # EPLB: physical replicas beyond E (0: none)
+    fp8: bool = False                                # experts in FP8 (E4M3, row scales)
     seed: int = 0
 
     @property
@@ -95,7 +96,13 @@ ALL = {w.name: w for w in (TINY, MIXTRAL, DSV3, SWITCH) + DECODE}
 SWITCH_EPLB = SWITCH.replace(name="switch_base_eplb", n_redundant=16)
 DSV3_EPLB = DSV3.replace(name="deepseek_v3_eplb", n_redundant=64)
 
-EXTRA = {w.name: w for w in (PROFILE_DSV3, PROFILE_DSV3_E32, DSV3_BLOCK, SWITCH_EPLB, DSV3_EPLB)}
+# FP8 experts (E4M3 weights and expert inputs, float32 row scales) on the
+# weight-bound DeepSeek-V3 shapes.
+DSV3_FP8 = DSV3.replace(name="deepseek_v3_fp8", fp8=True)
+DECODE_FP8 = DECODE[1].replace(name="deepseek_v3_decode_T256_fp8", fp8=True)
+
+EXTRA = {w.name: w for w in (PROFILE_DSV3, PROFILE_DSV3_E32, DSV3_BLOCK, SWITCH_EPLB, DSV3_EPLB, DSV3_FP8,
+                             DECODE_FP8)}
 
 
 def sigma_in(w: Workload) -> float:
