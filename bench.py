@@ -183,8 +183,11 @@ def run_ours(args, rank, world, local_rank):
         xq = torch.empty(R, w.h, dtype=torch.uint8, device="cuda")
         sxp = torch.empty(R, dtype=torch.float32, device="cuda")
         ws_ffn = moe.alloc_workspace(cfg, moe.MOE_OP_FFN_FP8)
-    stages = (("logits", "route") + (("eplb_map",) if eplb else ()) + ("layout", "permute", "ffn")
-              + (("shared",) if shared else ()) + ("combine",))
+    # `--fused-permute`: the FFN gathers its rows from x (moe_grouped_ffn_gather)
+    # instead of the layer's explicit permute
+    gather = args.fused_permute and not fp8 and not eplb
+    stages = (("logits", "route") + (("eplb_map",) if eplb else ()) + ("layout",)
+              + (("ffn",) if gather else ("permute", "ffn")) + (("shared",) if shared else ()) + ("combine",))
     n_ev = len(stages) + 1
 
     def step(ev=None):
@@ -210,11 +213,15 @@ def run_ours(args, rank, world, local_rank):
         rec()
         if fp8:
             moe.moe_permute_fp8(cfg, inp["x"], lay.slot, xq, sxp)
-        else:
+            rec()
+        elif not gather:
             moe.moe_permute(cfg, inp["x"], lay.slot, lay.row_src, xp)
-        rec()
+            rec()
         if fp8:
             moe.moe_grouped_ffn_fp8(cfg, xq, sxp, lay.offsets, lay.kept, q13, s13, q2, s2, yp, ws_ffn)
+        elif gather:  # the permutation fused into the FFN: rows read from x through row_src
+            moe.moe_grouped_ffn_gather(cfg, inp["x"], lay.row_src, lay.offsets, lay.kept, inp["w13"], inp["w2"],
+                                       yp, ws_ffn)
         elif eplb:
             moe.moe_grouped_ffn_mapped(cfg, xp, lay.offsets, lay.kept, plan["phys_to_log"], inp["w13"], inp["w2"],
                                        yp, ws_ffn)
@@ -327,7 +334,7 @@ def run_ours(args, rank, world, local_rank):
         ffn_bytes = weight_bytes + rows_kept * (2 * w.h + 2 * w.I) * ds
     ffn_flops = 6.0 * w.h * w.I * rows_kept
     tokens_with_rows = int((lay.slot.view(T, K) >= 0).any(dim=1).sum().item())
-    permute_bytes = (tokens_with_rows + rows_kept) * w.h * ds
+    permute_bytes = (tokens_with_rows + rows_kept) * w.h * ds  # not moved when the FFN gathers from x
     combine_bytes = (rows_kept + T) * w.h * ds
     peaks, peak_kind = measured_peaks()
     hbm = float(peaks["hbm_gbs"])
@@ -335,7 +342,8 @@ def run_ours(args, rank, world, local_rank):
     tc_peak = float(peaks["bf16_tflops_sustained"]) * (2.0 if fp8 else 1.0)
     ffn_s = per_stage["ffn"] / 1e3
     ffn_gbs = ffn_bytes / ffn_s / 1e9
-    launches_per_step = 8 + (1 if (w.pad and w.capacity > 0) else 0) + (2 if shared else 0) + (1 if eplb else 0)
+    launches_per_step = (8 + (1 if (w.pad and w.capacity > 0) else 0) + (2 if shared else 0) + (1 if eplb else 0)
+                         - (1 if gather else 0) + (1 if fp8 else 0))
     ms = total_ms / args.steps
     out = {
         "metric": METRIC,
@@ -363,7 +371,8 @@ def run_ours(args, rank, world, local_rank):
                      "tensor_tflops": ffn_flops / ffn_s / 1e12,
                      "tensor_frac_of_sustained": ffn_flops / ffn_s / 1e12 / tc_peak},
         "stages_ms": per_stage,
-        "permute_gbs": permute_bytes / (per_stage["permute"] / 1e3) / 1e9,
+        "permute_gbs": permute_bytes / (per_stage["permute"] / 1e3) / 1e9 if "permute" in per_stage else None,
+        "permute_fused_into_ffn": gather,
         "combine_gbs": combine_bytes / (per_stage["combine"] / 1e3) / 1e9,
         "layout": {"dropped": stats["dropped"], "experts_touched": stats["experts_touched"],
                    "balancedness": stats["balancedness"], "offdiag_rows": stats["offdiag_rows"]},
@@ -463,6 +472,8 @@ def main():
     ap.add_argument("--ref-sample", type=int, default=1, help="tokens whose FFN the oracle evaluates per step")
     ap.add_argument("--cpu-sample", type=int, default=8, help="tokens in the cpu_baseline sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--fused-permute", action="store_true",
+                    help="gather the FFN's rows from x instead of permuting (bf16 weights-as-M layers)")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3) if args.impl == "ours" else args.warmup
 

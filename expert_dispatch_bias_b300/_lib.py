@@ -36,6 +36,7 @@ EXPORTS = (
     "moe_shared_ffn", "moe_combine_add", "moe_block_forward", "moe_block_forward_host",
     "moe_eplb_plan", "moe_eplb_map", "moe_grouped_ffn_mapped", "moe_layer_forward_eplb",
     "moe_quantize_fp8", "moe_permute_fp8", "moe_grouped_ffn_fp8", "moe_layer_forward_fp8",
+    "moe_grouped_ffn_gather",
 )
 
 
@@ -98,6 +99,7 @@ def _load() -> ctypes.CDLL:
         "moe_permute_fp8": (c_int32, [cfgp] + [c_void_p] * 5),
         "moe_grouped_ffn_fp8": (c_int32, [cfgp] + [c_void_p] * 10 + [c_size_t, c_void_p]),
         "moe_layer_forward_fp8": (c_int32, [cfgp] + [c_void_p] * 11 + [c_size_t, c_void_p]),
+        "moe_grouped_ffn_gather": (c_int32, [cfgp] + [c_void_p] * 8 + [c_size_t, c_void_p]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -204,6 +206,13 @@ def moe_grouped_ffn(cfg, xp, offsets, kept, w13, w2, yp, workspace, stream=None)
     _check(lib.moe_grouped_ffn(ctypes.byref(cfg), _ptr(xp), _ptr(offsets), _ptr(kept), _ptr(w13), _ptr(w2),
                                _ptr(yp), _ptr(workspace), workspace.numel() * workspace.element_size(),
                                _stream(stream)), "moe_grouped_ffn")
+
+
+def moe_grouped_ffn_gather(cfg, x, row_src, offsets, kept, w13, w2, yp, workspace, stream=None) -> None:
+    _check(lib.moe_grouped_ffn_gather(ctypes.byref(cfg), _ptr(x), _ptr(row_src), _ptr(offsets), _ptr(kept),
+                                      _ptr(w13), _ptr(w2), _ptr(yp), _ptr(workspace),
+                                      workspace.numel() * workspace.element_size(), _stream(stream)),
+           "moe_grouped_ffn_gather")
 
 
 def moe_combine(cfg, yp, slot, topk_w, y, stream=None) -> None:

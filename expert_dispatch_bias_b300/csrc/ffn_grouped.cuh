@@ -68,6 +68,7 @@ struct FgParams {
   const int32_t* w_map;     // expert -> its weight matrices (replicas share a logical expert's), or null
   const float* w_scale;     // FP8: scale of every weight row [experts * a_rows]
   const float* x_scale;     // FP8: scale of every token row [R]
+  const int32_t* row_src;   // gather: token of every permuted row [R] (rows are read from x)
 };
 
 // Tensor maps of the token rows with boxes of 128, 64, 32 and 16 rows.
@@ -104,6 +105,17 @@ __device__ __forceinline__ FgTile fg_decode(int t, const int32_t* mbp, const FgP
 }
 
 __device__ __forceinline__ uint32_t round16(int n) { return (uint32_t)((n + 15) & ~15); }
+
+// Four rows y0..y3 (one-row box of the map, 128 bytes each) of a 2-D tensor
+// at column x into consecutive 128-byte rows of shared memory.
+__device__ __forceinline__ void tma_gather4(void* smem_dst, const CUtensorMap* map, int x, int y0, int y1, int y2,
+                                            int y3, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes [%0], [%1, {%2, "
+      "%3, %4, %5, %6}], [%7];" ::"r"(smem_u32(smem_dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y0), "r"(y1), "r"(y2), "r"(y3), "r"(smem_u32(bar))
+      : "memory");
+}
 
 // Epilogue of one 32-token chunk: v (and u, SwiGLU) hold this warp's 32
 // features x 32 tokens; the bf16 results are transposed through the warp's
@@ -175,7 +187,9 @@ __device__ __forceinline__ void fg_drain(uint32_t t_lane, uint32_t col0, uint32_
 
 // FP8: E4M3 operands (tcgen05.mma kind::f8f6f4), 128-element k-blocks (the
 // same 128-byte rows), results scaled by weight-row and token scales.
-template <int EPI, int BT, int STAGES, bool FP8 = false>
+// GATHER: the token rows are read straight from x through row_src (tile::gather4
+// of a one-row box), so the permutation needs no buffer of its own.
+template <int EPI, int BT, int STAGES, bool FP8 = false, bool GATHER = false>
 __global__ void __launch_bounds__(kFgThreads, 1)
     ffn_grouped_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_constant__ FgTokenMaps maps,
                        FgParams p) {
@@ -188,6 +202,7 @@ __global__ void __launch_bounds__(kFgThreads, 1)
   __shared__ volatile uint32_t abort_flag;
   __shared__ int32_t mbp[1025];
   __shared__ int32_t scan_scratch[33];
+  __shared__ int32_t src_rows[GATHER ? BT : 1];  // gather: source token of each row of the current tile
 
   uint8_t* ring = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(dyn_smem) + 1023) & ~uintptr_t(1023));
   __nv_bfloat16* xs_all = reinterpret_cast<__nv_bfloat16*>(ring + (size_t)STAGES * S::kStageBytes);
@@ -226,59 +241,84 @@ __global__ void __launch_bounds__(kFgThreads, 1)
 
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer
-    if (lane == 0) {
-      int stage = 0;
-      uint32_t phase = 0;
-      uint32_t armed = 0, armed_parity = 0;
-      // weight rows of the two 128-row boxes of a tile
-      auto weight_rows = [&](const FgTile& tl, int64_t& a0, int64_t& a1) {
-        const int64_t we = p.w_map != nullptr ? p.w_map[tl.e] : tl.e;
-        if (EPI == kTcSwiglu) {
-          a0 = we * p.a_rows + 128 * tl.ft;
-          a1 = a0 + p.up_rows;
-        } else {
-          a0 = we * p.a_rows + 256 * tl.ft;
-          a1 = a0 + 128;
+    // Lane 0 issues every copy; with GATHER the whole warp first stages the
+    // tile's source rows in shared memory.  The loop's exit test is taken by
+    // lane 0 and broadcast, so the warp never diverges around __syncwarp.
+    int stage = 0;
+    uint32_t phase = 0;
+    uint32_t armed = 0, armed_parity = 0;
+    // weight rows of the two 128-row boxes of a tile
+    auto weight_rows = [&](const FgTile& tl, int64_t& a0, int64_t& a1) {
+      const int64_t we = p.w_map != nullptr ? p.w_map[tl.e] : tl.e;
+      if (EPI == kTcSwiglu) {
+        a0 = we * p.a_rows + 128 * tl.ft;
+        a1 = a0 + p.up_rows;
+      } else {
+        a0 = we * p.a_rows + 256 * tl.ft;
+        a1 = a0 + 128;
+      }
+    };
+    for (int t = blockIdx.x; t < total_tiles; t += gridDim.x) {
+      if (__shfl_sync(0xffffffffu, abort_flag != 0 ? 1 : 0, 0)) break;
+      const FgTile tl = fg_decode<BT>(t, mbp, p);
+      const int n16 = (int)round16(tl.n);
+      if (GATHER) {
+        __syncwarp();  // lane 0 has issued every gather of the previous tile
+        for (int i = lane; i < n16; i += 32) {
+          // rows past the tile's end repeat its first row (computed, masked on store)
+          const int32_t src = p.row_src[tl.r0 + (i < tl.n ? i : 0)];
+          src_rows[i] = src >= 0 ? src : 0;
         }
-      };
-      for (int t = blockIdx.x; t < total_tiles && !abort_flag; t += gridDim.x) {
-        const FgTile tl = fg_decode<BT>(t, mbp, p);
-        int64_t a0, a1;
-        weight_rows(tl, a0, a1);
-        const uint32_t x_bytes = round16(tl.n) * (uint32_t)(kTcBK * 2);
-        for (int kb = 0; kb < p.k_blocks; ++kb) {
+        __syncwarp();
+      }
+      int64_t a0, a1;
+      weight_rows(tl, a0, a1);
+      const uint32_t x_bytes = round16(tl.n) * (uint32_t)(kTcBK * 2);
+      for (int kb = 0; kb < p.k_blocks; ++kb) {
+        // lane 0 waits for the stage, arms it and loads the weights; with
+        // GATHER every lane then issues its share of the four-row gathers
+        int ok = 1;
+        if (lane == 0) {
           if (!mbar_wait(&empty_bar[stage], phase ^ 1u, &abort_flag)) {
             abort_flag = 1;
             raise_error(kErrTimeout);
-            break;
-          }
-          uint8_t* sw = ring + (size_t)stage * S::kStageBytes;
-          uint8_t* sx = sw + 2 * S::kWBytes;
-          mbar_expect_tx(&full_bar[stage], 2 * S::kWBytes + x_bytes);
-          const int kx = kb * (FP8 ? 128 : kTcBK);
-          tma_load_2d(sw, &map_w, kx, (int)a0, &full_bar[stage]);
-          tma_load_2d(sw + S::kWBytes, &map_w, kx, (int)a1, &full_bar[stage]);
-          {
-            // round16(n) rows as boxes of 128 rows, then at most one each of 64, 32 and 16
-            const int n16 = (int)round16(tl.n);
-            int b = 0;
-            for (; b + 128 <= n16; b += 128) tma_load_2d(sx + b * (kTcBK * 2), &map_x[0], kx, tl.r0 + b, &full_bar[stage]);
-            if ((n16 - b) & 64) { tma_load_2d(sx + b * (kTcBK * 2), &map_x[1], kx, tl.r0 + b, &full_bar[stage]); b += 64; }
-            if ((n16 - b) & 32) { tma_load_2d(sx + b * (kTcBK * 2), &map_x[2], kx, tl.r0 + b, &full_bar[stage]); b += 32; }
-            if ((n16 - b) & 16) tma_load_2d(sx + b * (kTcBK * 2), &map_x[3], kx, tl.r0 + b, &full_bar[stage]);
-          }
-          armed |= 1u << stage;
-          armed_parity = (armed_parity & ~(1u << stage)) | (phase << stage);
-          if (++stage == STAGES) {
-            stage = 0;
-            phase ^= 1u;
+            ok = 0;
           }
         }
+        if (GATHER) ok = __shfl_sync(0xffffffffu, ok, 0);
+        if (!ok) break;
+        uint8_t* sw = ring + (size_t)stage * S::kStageBytes;
+        uint8_t* sx = sw + 2 * S::kWBytes;
+        const int kx = kb * (FP8 ? 128 : kTcBK);
+        if (lane == 0) {
+          mbar_expect_tx(&full_bar[stage], 2 * S::kWBytes + x_bytes);
+          tma_load_2d(sw, &map_w, kx, (int)a0, &full_bar[stage]);
+          tma_load_2d(sw + S::kWBytes, &map_w, kx, (int)a1, &full_bar[stage]);
+        }
+        if (GATHER) {
+          __syncwarp();  // the stage is armed before any gather can complete on it
+          for (int i = 4 * lane; i < n16; i += 4 * 32)
+            tma_gather4(sx + i * (kTcBK * 2), &map_x[0], kx, src_rows[i], src_rows[i + 1], src_rows[i + 2],
+                        src_rows[i + 3], &full_bar[stage]);
+        } else if (lane == 0) {
+          // round16(n) rows as boxes of 128 rows, then at most one each of 64, 32 and 16
+          int b = 0;
+          for (; b + 128 <= n16; b += 128) tma_load_2d(sx + b * (kTcBK * 2), &map_x[0], kx, tl.r0 + b, &full_bar[stage]);
+          if ((n16 - b) & 64) { tma_load_2d(sx + b * (kTcBK * 2), &map_x[1], kx, tl.r0 + b, &full_bar[stage]); b += 64; }
+          if ((n16 - b) & 32) { tma_load_2d(sx + b * (kTcBK * 2), &map_x[2], kx, tl.r0 + b, &full_bar[stage]); b += 32; }
+          if ((n16 - b) & 16) tma_load_2d(sx + b * (kTcBK * 2), &map_x[3], kx, tl.r0 + b, &full_bar[stage]);
+        }
+        armed |= 1u << stage;
+        armed_parity = (armed_parity & ~(1u << stage)) | (phase << stage);
+        if (++stage == STAGES) {
+          stage = 0;
+          phase ^= 1u;
+        }
       }
-      if (abort_flag) {
-        for (int s = 0; s < STAGES; ++s)
-          if ((armed >> s) & 1u) mbar_wait(&full_bar[s], (armed_parity >> s) & 1u);
-      }
+    }
+    if (lane == 0 && abort_flag) {
+      for (int s = 0; s < STAGES; ++s)
+        if ((armed >> s) & 1u) mbar_wait(&full_bar[s], (armed_parity >> s) & 1u);
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer

@@ -504,10 +504,12 @@ moe_status launch_ffn_tokens_m(const moe_config& c, const void* xp, const int32_
 // the MMA's M operand and the expert's token rows as N (ffn_grouped.cuh).
 // Token tiles of up to 160 rows in a 4-stage ring of 52 KB stages.
 constexpr int kFgTileRows = 160, kFgStages = 4;
+// row_src non-null: the gate/up GEMM gathers its rows from x = xp through row_src
+// (no permuted copy of x); else xp holds the permuted rows.
 template <int BT, int STAGES>
 moe_status launch_ffn_grouped(const moe_config& c, const void* xp, const int32_t* offsets, const int32_t* kept,
                               const int32_t* w_map, int n_w, const void* w13, const void* w2, void* yp, void* inter,
-                              cudaStream_t st) {
+                              cudaStream_t st, const int32_t* row_src = nullptr) {
   using S = FgShape<BT, STAGES>;
   const int64_t R = rows_of(c);
   const int grid = device_info().sms;
@@ -516,7 +518,10 @@ moe_status launch_ffn_grouped(const moe_config& c, const void* xp, const int32_t
   MOE_TRY(make_tensor_map(&w1m, w13, c.h, (uint64_t)n_w * 2 * c.I, 128));
   MOE_TRY(make_tensor_map(&w2m, w2, c.I, (uint64_t)n_w * c.h, 128));
   for (int i = 0; i < 4; ++i) {
-    MOE_TRY(make_tensor_map(&x1.m[i], xp, c.h, R, 128u >> i));
+    if (row_src != nullptr)
+      MOE_TRY(make_tensor_map(&x1.m[i], xp, c.h, c.T, 1));  // rows of x, gathered four at a time
+    else
+      MOE_TRY(make_tensor_map(&x1.m[i], xp, c.h, R, 128u >> i));
     MOE_TRY(make_tensor_map(&x2.m[i], inter, c.I, R, 128u >> i));
   }
   FgParams p1{};
@@ -539,7 +544,10 @@ moe_status launch_ffn_grouped(const moe_config& c, const void* xp, const int32_t
   p2.n_valid = c.h;
   p2.out = static_cast<__nv_bfloat16*>(yp);
   p2.ldo = c.h;
-  auto k1 = ffn_grouped_kernel<kTcSwiglu, BT, STAGES>;
+  p1.row_src = row_src;
+  p2.row_src = nullptr;
+  auto k1 = row_src != nullptr ? ffn_grouped_kernel<kTcSwiglu, BT, STAGES, false, true>
+                               : ffn_grouped_kernel<kTcSwiglu, BT, STAGES>;
   auto k2 = ffn_grouped_kernel<kTcStore, BT, STAGES>;
   CUDA_TRY(allow_smem(k1, S::kDynSmem));
   CUDA_TRY(allow_smem(k2, S::kDynSmem));
@@ -703,6 +711,23 @@ moe_status launch_permute_fp8(const moe_config& c, const void* x, const int32_t*
                                                                        c.T, c.K, c.h, xq, sx);
   CUDA_TRY(cudaGetLastError());
   return MOE_OK;
+}
+
+// The grouped FFN reading its rows straight from x through row_src: bf16,
+// weights-as-M layers only (experts expected to see at most
+// MOE_FFN_SWAP_MAX_ROWS rows).  The layer calls do not use it: on B300 the
+// four-row TMA gathers cost about as much per instruction as a whole box, and
+// the gathered FFN measured no faster than permute + FFN at a few rows per
+// expert and up to 1.8x slower at DeepSeek-V3 prefill (144 rows per tile,
+// h = 7168).  It saves the permuted copy of x (R x h).
+moe_status launch_ffn_gather(const moe_config& c, const void* x, const int32_t* row_src, const int32_t* offsets,
+                             const int32_t* kept, const int32_t* w_map, int n_w, const void* w13, const void* w2,
+                             void* yp, void* inter, cudaStream_t st) {
+  if (rows_of(c) == 0 || c.T == 0) return MOE_OK;
+  if (c.dtype != MOE_BF16 || expected_rows_per_expert(c) > MOE_FFN_SWAP_MAX_ROWS) return MOE_ERR_UNSUPPORTED;
+  if ((int64_t)n_w * 2 * c.I >= INT32_MAX || (int64_t)n_w * c.h >= INT32_MAX) return MOE_ERR_UNSUPPORTED;
+  return launch_ffn_grouped<kFgTileRows, kFgStages>(c, x, offsets, kept, w_map, n_w, w13, w2, yp, inter, st,
+                                                    row_src);
 }
 
 moe_status launch_ffn(const moe_config& c, const void* xp, const int32_t* offsets, const int32_t* kept,
@@ -1247,6 +1272,25 @@ moe_status moe_layer_forward_eplb(const moe_config* cfg, const void* x, const vo
   plan.phys_to_log = phys_to_log;
   return layer_core(*cfg, x, w_r, logit_offset, sel_bias, w13, w2, nullptr, nullptr, y, out, b, as_stream(stream),
                     plan);
+}
+
+moe_status moe_grouped_ffn_gather(const moe_config* cfg, const void* x, const int32_t* row_src,
+                                  const int32_t* offsets, const int32_t* kept, const void* w13, const void* w2,
+                                  void* yp, void* workspace, size_t workspace_bytes, void* stream) {
+  MOE_TRY(validate(cfg));
+  if (cfg->T > 0) MOE_TRY(check_dtype_ptr(x));
+  if (rows_of(*cfg) > 0) {
+    MOE_TRY(check_ptr(row_src, 4));
+    MOE_TRY(check_dtype_ptr(yp));
+  }
+  MOE_TRY(check_ptr(offsets, 4));
+  MOE_TRY(check_ptr(kept, 4));
+  MOE_TRY(check_dtype_ptr(w13));
+  MOE_TRY(check_dtype_ptr(w2));
+  MOE_TRY(check_ptr(workspace, 256));
+  if (workspace_bytes < ffn_ws_bytes(*cfg)) return MOE_ERR_WORKSPACE_TOO_SMALL;
+  return launch_ffn_gather(*cfg, x, row_src, offsets, kept, nullptr, nphys(*cfg), w13, w2, yp,
+                           static_cast<char*>(workspace) + 256, as_stream(stream));
 }
 
 moe_status fp8_config_ok(const moe_config* cfg) {
