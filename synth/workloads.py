@@ -101,8 +101,14 @@ DSV3_EPLB = DSV3.replace(name="deepseek_v3_eplb", n_redundant=64)
 DSV3_FP8 = DSV3.replace(name="deepseek_v3_fp8", fp8=True)
 DECODE_FP8 = DECODE[1].replace(name="deepseek_v3_decode_T256_fp8", fp8=True)
 
+# Profiling cases: the DeepSeek-V3 token count and width with 16 experts (1.4 GB
+# of weights; permuted buffers of 470 MB, larger than L2; 2048 rows per expert,
+# so the tokens-as-M FFN) plus the shared expert; and the 32-expert case in FP8.
+PROFILE_DSV3_E16_BLOCK = DSV3.replace(name="deepseek_v3_e16_T4096_block", E=16, ep_size=16, shared_I=2048)
+PROFILE_DSV3_E32_FP8 = PROFILE_DSV3_E32.replace(name="deepseek_v3_e32_T512_fp8", fp8=True)
+
 EXTRA = {w.name: w for w in (PROFILE_DSV3, PROFILE_DSV3_E32, DSV3_BLOCK, SWITCH_EPLB, DSV3_EPLB, DSV3_FP8,
-                             DECODE_FP8)}
+                             DECODE_FP8, PROFILE_DSV3_E16_BLOCK, PROFILE_DSV3_E32_FP8)}
 
 
 def sigma_in(w: Workload) -> float:
