@@ -10,9 +10,11 @@
 // inclusive prefix is the histogram.  The look-back spin is bounded.
 //
 // Pass 2 (layout_finalize_kernel): every block scans kept[] into offsets,
-// turns ranks into slots (or -1 when over capacity), fills row_src and
-// accumulates n_ij; the last block to finish derives the per-chip bytes and
-// the scalar statistics and resets the look-back state for the next call.
+// turns ranks into slots (or -1 when over capacity), fills row_src and counts
+// its n_ij entries in shared memory (its tokens fall in a few source chips),
+// then adds them to n_ij and to the per-chip sent / received row counts; the
+// last block to finish turns those counts into bytes, derives the scalar
+// statistics and resets the look-back state for the next call.
 #pragma once
 
 #include "common.cuh"
@@ -26,6 +28,7 @@ constexpr int kLayoutItems = 4;                       // per thread
 constexpr int kLayoutTile = kLayoutThreads * kLayoutItems;
 constexpr int kFinalizeThreads = 256;
 constexpr int kFinalizeItems = 4;
+constexpr int kFinalizeBins = 4096;  // shared n_ij entries of one block
 
 enum : uint32_t { kTileEmpty = 0u, kTileAggregate = 1u, kTileInclusive = 2u };
 
@@ -53,7 +56,7 @@ inline LayoutScratch layout_scratch_at(void* base, int64_t A, int E) {
   const size_t nt = (size_t)layout_num_tiles(A);
   char* p = static_cast<char*>(base);
   LayoutScratch s;
-  s.header = reinterpret_cast<uint32_t*>(p);
+  s.header = reinterpret_cast<uint32_t*>(p);  // [0] tiles taken, [1] blocks done, [2..3] diagonal rows (u64)
   p += 256;
   s.flags = reinterpret_cast<uint32_t*>(p);
   p += align_up(nt * 4, 256);
@@ -98,6 +101,7 @@ __global__ void __launch_bounds__(kLayoutThreads) layout_rank_kernel(LayoutParam
     for (int64_t r = gtid; r < p.R; r += gstride) p.row_src[r] = -1;
     const int64_t nn = (int64_t)p.n_ep * p.n_ep;
     for (int64_t i = gtid; i < nn; i += gstride) p.n_ij[i] = 0;
+    for (int64_t i = gtid; i < 2 * p.n_ep; i += gstride) p.rank_bytes[i] = 0;  // row counts until pass 2 ends
   }
   __syncthreads();
   const int tile = (int)s_tile;
@@ -220,7 +224,17 @@ __global__ void __launch_bounds__(kFinalizeThreads) layout_finalize_kernel(Layou
     for (int e = tid; e <= p.E; e += kFinalizeThreads) p.offsets[e] = off[e];
 
   const int epr = p.E / p.n_ep;
+  const int N = p.n_ep;
   const int64_t a0 = (int64_t)blockIdx.x * (kFinalizeThreads * kFinalizeItems);
+  const int64_t a_end = min(p.A, a0 + kFinalizeThreads * kFinalizeItems);
+  // Source chips of this block's tokens: [i_lo, i_lo + span).
+  const int i_lo = a0 < a_end ? (int)((a0 / p.K) * N / p.T) : 0;
+  const int span = a0 < a_end ? (int)(((a_end - 1) / p.K) * N / p.T) - i_lo + 1 : 0;
+  const bool local = (int64_t)span * N <= kFinalizeBins;
+  __shared__ int32_t bins[kFinalizeBins];
+  if (local)
+    for (int b = tid; b < span * N; b += kFinalizeThreads) bins[b] = 0;
+  __syncthreads();
 #pragma unroll
   for (int r = 0; r < kFinalizeItems; ++r) {
     const int64_t a = a0 + r * kFinalizeThreads + tid;
@@ -241,8 +255,27 @@ __global__ void __launch_bounds__(kFinalizeThreads) layout_finalize_kernel(Layou
     if (keep) {
       const int64_t t = a / p.K;
       p.row_src[s] = (int32_t)t;
-      const int64_t i = (t * p.n_ep) / p.T;
-      atomicAdd(reinterpret_cast<unsigned long long*>(&p.n_ij[i * p.n_ep + e / epr]), 1ull);
+      const int i = (int)((t * N) / p.T), j = e / epr;
+      if (local) {
+        atomicAdd(&bins[(i - i_lo) * N + j], 1);
+      } else {
+        atomicAdd(reinterpret_cast<unsigned long long*>(&p.n_ij[(int64_t)i * N + j]), 1ull);
+        atomicAdd(reinterpret_cast<unsigned long long*>(&p.rank_bytes[i]), 1ull);
+        atomicAdd(reinterpret_cast<unsigned long long*>(&p.rank_bytes[N + j]), 1ull);
+        if (i == j) atomicAdd(reinterpret_cast<unsigned long long*>(p.ws.header + 2), 1ull);
+      }
+    }
+  }
+  __syncthreads();
+  if (local) {
+    for (int b = tid; b < span * N; b += kFinalizeThreads) {
+      const unsigned long long c = (unsigned long long)bins[b];
+      if (c == 0) continue;
+      const int i = i_lo + b / N, j = b % N;
+      atomicAdd(reinterpret_cast<unsigned long long*>(&p.n_ij[(int64_t)i * N + j]), c);
+      atomicAdd(reinterpret_cast<unsigned long long*>(&p.rank_bytes[i]), c);
+      atomicAdd(reinterpret_cast<unsigned long long*>(&p.rank_bytes[N + j]), c);
+      if (i == j) atomicAdd(reinterpret_cast<unsigned long long*>(p.ws.header + 2), c);
     }
   }
 
@@ -264,21 +297,14 @@ __global__ void __launch_bounds__(kFinalizeThreads) layout_finalize_kernel(Layou
     s_kept = 0;
   }
   __syncthreads();
-  const int N = p.n_ep;
   const long long rowbytes = (long long)p.h * p.ds;
-  for (int i = tid; i < N; i += kFinalizeThreads) {
-    long long sent = 0, recv = 0;
-    for (int j = 0; j < N; ++j) {
-      sent += (long long)__ldcg(reinterpret_cast<const unsigned long long*>(&p.n_ij[(size_t)i * N + j]));
-      recv += (long long)__ldcg(reinterpret_cast<const unsigned long long*>(&p.n_ij[(size_t)j * N + i]));
-    }
+  for (int i = tid; i < N; i += kFinalizeThreads) {  // row and column sums of n_ij
+    const long long sent = __ldcg(&p.rank_bytes[i]), recv = __ldcg(&p.rank_bytes[N + i]);
     p.rank_bytes[i] = sent * rowbytes;
     p.rank_bytes[N + i] = recv * rowbytes;
-    const long long diag =
-        (long long)__ldcg(reinterpret_cast<const unsigned long long*>(&p.n_ij[(size_t)i * N + i]));
     atomicMax(&s_max, (unsigned long long)recv);
     atomicAdd(&s_sum, (unsigned long long)recv);
-    atomicAdd(&s_off, (unsigned long long)(sent - diag));
+    atomicAdd(&s_off, (unsigned long long)sent);
   }
   for (int e = tid; e < p.E; e += kFinalizeThreads) {
     const int32_t k = __ldcg(&p.kept[e]);
@@ -290,13 +316,15 @@ __global__ void __launch_bounds__(kFinalizeThreads) layout_finalize_kernel(Layou
     moe_layout_stats st;
     st.kept_total = s_kept;
     st.dropped = p.A - s_kept;
-    st.offdiag_rows = (long long)s_off;
+    unsigned long long* diag = reinterpret_cast<unsigned long long*>(p.ws.header + 2);
+    st.offdiag_rows = (long long)(s_off - __ldcg(diag));  // all kept rows minus the diagonal
     st.experts_touched = s_touched;
     st.balancedness = s_max == 0 ? 1.0f : (float)((double)s_sum / ((double)N * (double)s_max));
     *p.stats = st;
     // reset the look-back state for the next call on this workspace
     p.ws.header[0] = 0;
     p.ws.header[1] = 0;
+    *diag = 0;
   }
   for (int t = tid; t < p.num_tiles; t += kFinalizeThreads) p.ws.flags[t] = kTileEmpty;
 }

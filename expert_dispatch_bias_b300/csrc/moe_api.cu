@@ -352,24 +352,21 @@ moe_status launch_combine(const moe_config& c, const void* yp, const int32_t* sl
   p.T = c.T;
   p.K = c.K;
   p.h = c.h;
-  const int warps_per_block = 8;
-  int64_t blocks = (c.T + warps_per_block - 1) / warps_per_block;
-  const int64_t cap = (int64_t)device_info().sms * 8;
-  if (blocks > cap) blocks = cap;
+  // Persistent grid: every SM holds as many blocks as fit, each warp strides
+  // over (token, chunk) units.
   const bool bf = c.dtype == MOE_BF16;
-  if (c.K <= 1) {
-    if (bf) combine_kernel<__nv_bfloat16, 1><<<(unsigned)blocks, 256, 0, st>>>(p);
-    else combine_kernel<float, 1><<<(unsigned)blocks, 256, 0, st>>>(p);
-  } else if (c.K <= 2) {
-    if (bf) combine_kernel<__nv_bfloat16, 2><<<(unsigned)blocks, 256, 0, st>>>(p);
-    else combine_kernel<float, 2><<<(unsigned)blocks, 256, 0, st>>>(p);
-  } else if (c.K <= 8) {
-    if (bf) combine_kernel<__nv_bfloat16, 8><<<(unsigned)blocks, 256, 0, st>>>(p);
-    else combine_kernel<float, 8><<<(unsigned)blocks, 256, 0, st>>>(p);
-  } else {
-    if (bf) combine_kernel<__nv_bfloat16, 16><<<(unsigned)blocks, 256, 0, st>>>(p);
-    else combine_kernel<float, 16><<<(unsigned)blocks, 256, 0, st>>>(p);
-  }
+  auto kern = c.K <= 1   ? (bf ? combine_kernel<__nv_bfloat16, 1> : combine_kernel<float, 1>)
+              : c.K <= 2 ? (bf ? combine_kernel<__nv_bfloat16, 2> : combine_kernel<float, 2>)
+              : c.K <= 8 ? (bf ? combine_kernel<__nv_bfloat16, 8> : combine_kernel<float, 8>)
+                         : (bf ? combine_kernel<__nv_bfloat16, 16> : combine_kernel<float, 16>);
+  const int vecs = c.h / (bf ? 8 : 4);
+  const int64_t units = c.T * ((vecs + kCombineChunk - 1) / kCombineChunk);
+  int per_sm = 0;
+  CUDA_TRY(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, 256, 0));
+  if (per_sm < 1) per_sm = 1;
+  int64_t blocks = (int64_t)device_info().sms * per_sm;
+  if (blocks > (units + 7) / 8) blocks = (units + 7) / 8;
+  kern<<<(unsigned)blocks, 256, 0, st>>>(p);
   CUDA_TRY(cudaGetLastError());
   return MOE_OK;
 }

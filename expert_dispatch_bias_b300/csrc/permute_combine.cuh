@@ -7,8 +7,10 @@
 // (cp.async.bulk shared->global).  HBM traffic is the algorithmic minimum: one
 // read of every token that has a kept slot, one write per kept assignment.
 //
-// Combine is a gather: one warp per token, 16-byte vector loads of the K
-// expert-output rows, float32 accumulation in k order, one vector store.
+// Combine is a gather: one warp per (token, column chunk of kCombineChunk
+// 16-byte vectors), 16-byte vector loads of the K expert-output rows, float32
+// accumulation in k order, one vector store.  Chunks rather than whole tokens
+// keep the work units small, so a persistent grid ends without a partial wave.
 #pragma once
 
 #include "common.cuh"
@@ -141,13 +143,20 @@ __device__ __forceinline__ uint4 pack(const float* f, __nv_bfloat16) {
                     pack_bf16x2(f[6], f[7]));
 }
 
+constexpr int kCombineChunk = 128;  // 16-byte vectors per work unit (4 per lane)
+
 template <typename T, int KMAX>
 __global__ void __launch_bounds__(256) combine_kernel(CombineParams p) {
   constexpr int V = Vec<T>::N;
   const int lane = threadIdx.x & 31;
   const int64_t warps = (int64_t)gridDim.x * (blockDim.x >> 5);
   const int vecs = p.h / V;
-  for (int64_t t = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); t < p.T; t += warps) {
+  const int chunks = (vecs + kCombineChunk - 1) / kCombineChunk;
+  const int64_t units = p.T * chunks;
+  for (int64_t u = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); u < units; u += warps) {
+    const int64_t t = u / chunks;
+    const int c0 = (int)(u - t * chunks) * kCombineChunk;
+    const int c1 = min(vecs, c0 + kCombineChunk);
     int32_t s_l = -1;
     float w_l = 0.0f;
     if (lane < p.K) {
@@ -163,7 +172,7 @@ __global__ void __launch_bounds__(256) combine_kernel(CombineParams p) {
     }
     const uint4* src = static_cast<const uint4*>(p.yp);
     uint4* dst = static_cast<uint4*>(p.y) + t * vecs;
-    for (int c = lane; c < vecs; c += 32) {
+    for (int c = c0 + lane; c < c1; c += 32) {
       uint4 v[KMAX];
 #pragma unroll
       for (int k = 0; k < KMAX; ++k)

@@ -1,9 +1,13 @@
-// Top-K routing: one warp per token.
+// Top-K routing: one warp per token selects, then the block's threads share
+// the float64 weights of its chosen experts.
 //
 // Scores, selection keys, group limit, top-K and combine weights as defined in
 // the header (moe_route).  Scores are evaluated in float64 so that the float32
 // keys are the correctly rounded values of the mathematical ones; the keys then
-// decide the selection through exact float32 comparisons and adds only.
+// decide the selection through exact float32 comparisons and adds only.  The
+// float64 pipe is narrow on this GPU, so the weights of a block's tokens are
+// evaluated one (token, k) pair per thread rather than by K lanes of each
+// token's warp: a quarter of the float64 instructions for K = 8.
 #pragma once
 
 #include <math.h>
@@ -14,6 +18,7 @@ namespace moe {
 
 constexpr int kRouteWarps = 8;      // tokens per block
 constexpr int kMaxGroupTopn = 8;
+constexpr int kRouteMaxK = 16;
 
 struct RouteParams {
   const float* logits;  // [T, E]
@@ -60,7 +65,42 @@ __device__ __forceinline__ RouteSel route_select(const float* key, const RoutePa
   // ---- group limit: bit g of gmask set iff group g is allowed
   uint32_t gmask = full;
   int gsize = p.E;
-  if (p.n_groups > 0) {
+  if (p.n_groups > 0 && p.group_topn <= 2 && (p.E / p.n_groups) % PER == 0 &&
+      ((p.E / p.n_groups / PER) & (p.E / p.n_groups / PER - 1)) == 0) {
+    // Each group is a power-of-two run of whole lanes: the two largest keys of
+    // every lane, merged across the group's lanes by butterfly shuffles.  The
+    // group score is the same float32 sum as the general path forms.
+    gsize = p.E / p.n_groups;
+    const int lanes_per_group = gsize / PER;
+    float t1 = -INFINITY, t2 = -INFINITY;  // t1 >= t2
+#pragma unroll
+    for (int i = 0; i < PER; ++i) {  // NaN keys compare false and are skipped
+      const float v = key[i];
+      if (v > t2) {
+        t2 = v > t1 ? t1 : v;
+        t1 = fmaxf(t1, v);
+      }
+    }
+    for (int o = 1; o < lanes_per_group; o <<= 1) {
+      const float b1 = __shfl_xor_sync(full, t1, o), b2 = __shfl_xor_sync(full, t2, o);
+      t2 = fmaxf(fminf(t1, b1), fmaxf(t2, b2));
+      t1 = fmaxf(t1, b1);
+    }
+    const float mine = p.group_topn == 1 ? t1 : __fadd_rn(t1, t2);
+    const float gscore = __shfl_sync(full, mine, (lane % p.n_groups) * lanes_per_group);
+    int rank = 0;
+    for (int g = 0; g < p.n_groups; ++g) {
+      const float v = __shfl_sync(full, gscore, g);
+      if (beats(v, g, gscore, lane)) ++rank;
+    }
+    const bool in = lane < p.n_groups;
+    gmask = __ballot_sync(full, in && rank < p.topk_groups);
+    if (p.topk_groups < p.n_groups) {
+      const int la = __ffs(__ballot_sync(full, in && rank == p.topk_groups - 1)) - 1;
+      const int lb = __ffs(__ballot_sync(full, in && rank == p.topk_groups)) - 1;
+      r.group_gap = __shfl_sync(full, gscore, la) - __shfl_sync(full, gscore, lb);
+    }
+  } else if (p.n_groups > 0) {
     __syncwarp();
 #pragma unroll
     for (int i = 0; i < PER; ++i) {
@@ -148,16 +188,15 @@ __device__ __forceinline__ RouteSel route_select(const float* key, const RoutePa
   return r;
 }
 
-// PER = experts held by each lane (contiguous: lane l holds l*PER .. l*PER+PER-1).
+// Selection for token t by the calling warp: writes ids[t, :], the chosen
+// logits to xs[0..K), and the softmax max and float64 denominator (when the
+// weights need the full one) to *zs, *ms.
 template <int PER>
-__global__ void __launch_bounds__(kRouteWarps * 32) route_kernel(RouteParams p) {
-  extern __shared__ float s_keys[];  // [kRouteWarps][E], used with a group limit
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int t = blockIdx.x * kRouteWarps + warp;
-  if (t >= p.T) return;  // uniform across the warp
+__device__ __forceinline__ void route_token(const RouteParams& p, int t, float* kk, float* xs, double* zs,
+                                            float* ms) {
+  const int lane = threadIdx.x & 31;
   const unsigned full = 0xffffffffu;
   const float* L = p.logits + (size_t)t * p.E;
-  float* kk = s_keys + warp * p.E;
 
   float lg[PER];
 #pragma unroll
@@ -221,8 +260,7 @@ __global__ void __launch_bounds__(kRouteWarps * 32) route_kernel(RouteParams p) 
     }
   }
 
-  // ---- weights from the unbiased float64 scores of the chosen experts
-  if (!p.sigmoid && !p.renorm && p.key_is_logit) {  // the full denominator is needed
+  if (!p.sigmoid && !p.renorm && p.key_is_logit) {  // the weights need the full denominator
 #pragma unroll
     for (int i = 0; i < PER; ++i) {
       const int e = lane * PER + i;
@@ -231,18 +269,45 @@ __global__ void __launch_bounds__(kRouteWarps * 32) route_kernel(RouteParams p) 
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) z += __shfl_xor_sync(full, z, o);
   }
-  double mys = 0.0;
   if (lane < p.K) {
-    const double x = (double)L[sel.my_id];
-    mys = p.sigmoid ? 1.0 / (1.0 + exp(-x)) : exp(x - (double)m);
-  }
-  double tot = mys;
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) tot += __shfl_xor_sync(full, tot, o);
-  if (lane < p.K) {
-    const double wk = p.renorm ? (mys / tot) : (p.sigmoid ? mys : mys / z);
     p.ids[(size_t)t * p.K + lane] = sel.my_id;
-    p.w[(size_t)t * p.K + lane] = (float)(wk * (double)p.scale);
+    xs[lane] = L[sel.my_id];
+  }
+  if (lane == 0) {
+    *zs = z;
+    *ms = m;
+  }
+}
+
+// PER = experts held by each lane (contiguous: lane l holds l*PER .. l*PER+PER-1).
+template <int PER>
+__global__ void __launch_bounds__(kRouteWarps * 32) route_kernel(RouteParams p) {
+  extern __shared__ float s_keys[];  // [kRouteWarps][E], used with a group limit
+  __shared__ float s_x[kRouteWarps * kRouteMaxK];    // logits of the chosen experts
+  __shared__ double s_s[kRouteWarps * kRouteMaxK];   // their float64 scores
+  __shared__ double s_z[kRouteWarps];                // softmax denominators
+  __shared__ float s_m[kRouteWarps];                 // largest logits
+  const int warp = threadIdx.x >> 5;
+  const int t0 = blockIdx.x * kRouteWarps;
+  const int nt = min(kRouteWarps, p.T - t0);  // tokens of this block
+  if (warp < nt) route_token<PER>(p, t0 + warp, s_keys + warp * p.E, s_x + warp * p.K, &s_z[warp], &s_m[warp]);
+  __syncthreads();
+
+  // ---- weights from the unbiased float64 scores of the chosen experts, one
+  // (token, k) pair per thread: pair j is token j / K, choice j % K.
+  const int pairs = nt * p.K;
+  for (int j = threadIdx.x; j < pairs; j += blockDim.x) {
+    const double x = (double)s_x[j];
+    s_s[j] = p.sigmoid ? 1.0 / (1.0 + exp(-x)) : exp(x - (double)s_m[j / p.K]);
+  }
+  __syncthreads();
+  for (int j = threadIdx.x; j < pairs; j += blockDim.x) {
+    const int tl = j / p.K;
+    const double* sc = s_s + tl * p.K;
+    double tot = 0.0;
+    for (int k = 0; k < p.K; ++k) tot += sc[k];
+    const double wk = p.renorm ? (s_s[j] / tot) : (p.sigmoid ? s_s[j] : s_s[j] / s_z[tl]);
+    p.w[(size_t)t0 * p.K + j] = (float)(wk * (double)p.scale);
   }
 }
 
