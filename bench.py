@@ -154,6 +154,7 @@ def run_ours(args, rank, world, local_rank):
     lay = moe.alloc_layout(cfg)
     ws_layout = moe.alloc_workspace(cfg, moe.MOE_OP_LAYOUT)
     ws_ffn = moe.alloc_workspace(cfg, moe.MOE_OP_FFN)
+    ws_logits = moe.alloc_workspace(cfg, moe.MOE_OP_LOGITS)
     xp = torch.empty(R, w.h, dtype=dt, device="cuda")
     yp = torch.empty(R, w.h, dtype=dt, device="cuda")
     y = torch.empty(T, w.h, dtype=dt, device="cuda")
@@ -164,7 +165,7 @@ def run_ours(args, rank, world, local_rank):
         ws_shared = moe.alloc_workspace(cfg, moe.MOE_OP_SHARED)
     eplb = w.n_redundant > 0  # replicas: plan once from this batch's logical expert loads (not timed)
     if eplb:
-        moe.moe_router_logits(cfg, inp["x"], inp["w_r"], inp["logit_offset"], logits)
+        moe.moe_router_logits(cfg, inp["x"], inp["w_r"], inp["logit_offset"], logits, ws_logits)
         moe.moe_route(cfg, logits, inp["sel_bias"], ids, wts)
         counts = torch.bincount(ids.view(-1).long(), minlength=E).cpu().numpy()
         plan_h = moe.moe_eplb_plan(E, N, w.n_redundant, counts)
@@ -199,7 +200,7 @@ def run_ours(args, rank, world, local_rank):
             n[0] += 1
 
         rec()
-        moe.moe_router_logits(cfg, inp["x"], inp["w_r"], inp["logit_offset"], logits)
+        moe.moe_router_logits(cfg, inp["x"], inp["w_r"], inp["logit_offset"], logits, ws_logits)
         rec()
         moe.moe_route(cfg, logits, inp["sel_bias"], ids, wts)
         rec()

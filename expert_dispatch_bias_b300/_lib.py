@@ -19,7 +19,7 @@ MOE_F32, MOE_BF16 = 0, 1
 MOE_SOFTMAX, MOE_SIGMOID = 0, 1
 MOE_OP_LAYOUT, MOE_OP_FFN, MOE_OP_LAYER, MOE_OP_LAYER_HOST = 0, 1, 2, 3
 MOE_OP_SHARED, MOE_OP_BLOCK, MOE_OP_BLOCK_HOST = 4, 5, 6
-MOE_OP_FFN_FP8, MOE_OP_LAYER_FP8 = 7, 8
+MOE_OP_FFN_FP8, MOE_OP_LAYER_FP8, MOE_OP_LOGITS = 7, 8, 9
 
 STATUS = {
     0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED", 3: "MOE_ERR_ALIGNMENT",
@@ -77,7 +77,7 @@ def _load() -> ctypes.CDLL:
         "moe_rows": (c_int32, [cfgp, POINTER(c_int64)]),
         "moe_workspace_size": (c_int32, [cfgp, c_int32, POINTER(c_size_t)]),
         "moe_workspace_init": (c_int32, [c_void_p, c_size_t, c_void_p]),
-        "moe_router_logits": (c_int32, [cfgp, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p]),
+        "moe_router_logits": (c_int32, [cfgp, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p]),
         "moe_route": (c_int32, [cfgp, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p]),
         "moe_dispatch_layout": (c_int32, [cfgp] + [c_void_p] * 10 + [c_size_t, c_void_p]),
         "moe_dispatch_layout_static": (c_int32, [cfgp] + [c_void_p] * 9 + [c_void_p]),
@@ -170,9 +170,10 @@ def moe_workspace_init(ws, stream=None) -> None:
     _check(lib.moe_workspace_init(_ptr(ws), ws.numel() * ws.element_size(), _stream(stream)), "moe_workspace_init")
 
 
-def moe_router_logits(cfg, x, w_r, logit_offset, logits, stream=None) -> None:
+def moe_router_logits(cfg, x, w_r, logit_offset, logits, workspace, stream=None) -> None:
+    """workspace: moe_workspace_size(cfg, MOE_OP_LOGITS) bytes (alloc_workspace)."""
     _check(lib.moe_router_logits(ctypes.byref(cfg), _ptr(x), _ptr(w_r), _ptr(logit_offset), _ptr(logits),
-                                 _stream(stream)), "moe_router_logits")
+                                 _ptr(workspace), _stream(stream)), "moe_router_logits")
 
 
 def moe_route(cfg, logits, sel_bias, topk_ids, topk_w, stream=None) -> None:

@@ -21,18 +21,23 @@
 // 0 and D1 in slot 1.  An expert with more than BT rows is split into equal
 // token tiles.
 //
-// Roles (192 threads), one persistent CTA per SM over a static round-robin of
+// Roles (224 threads), one persistent CTA per SM over a static round-robin of
 // tiles ordered (expert, feature tile, token tile), so the token tiles sharing
 // a weight tile run on neighbouring SMs and the second read hits L2:
-//   warp 0      one thread issues TMA loads: the two 128x64 weight boxes and the
-//               tile's token rows (boxes of 128, 64, 32 and 16 rows) into a
-//               STAGES-deep ring;
+//   warp 0      one thread issues the TMA loads of the two 128x64 weight boxes
+//               of every k-block into a WS-deep weight ring;
+//   warp 6      issues the loads of the tile's token rows (boxes of 128, 64, 32
+//               and 16 rows, or four-row gathers) into an XS-deep token ring;
 //   warp 1      allocates 512 TMEM columns; one thread issues tcgen05.mma
 //               (M=128, N = the tile's rows rounded up to 16, K=16), two per
-//               k-step, from descriptors computed once per stage;
+//               k-step, once both rings hold the k-block;
 //   warps 2..5  drain the accumulators with tcgen05.ld (warp w reads TMEM lanes
 //               32*(w%4).. = 32 features), transpose 32 features x 32 tokens
 //               through shared memory and store 64-byte row pieces.
+// The weights stream from DRAM while the token rows are mostly L2 hits; the two
+// rings are separate so that each is refilled as soon as its own slot frees and
+// their depths can be chosen apart (the launcher's choice and the measurements
+// behind it are beside kFgTileRows).
 // Rows past a tile's end are computed and masked on store.  Every wait is
 // bounded; a wait that runs out raises the sticky error, and the CTA drains its
 // copies and MMAs, frees TMEM and exits.
@@ -42,16 +47,18 @@
 
 namespace moe {
 
-constexpr int kFgThreads = 192;
+constexpr int kFgThreads = 224;
 constexpr int kFgXsStride = 40;  // bf16 per row of a warp's 32x32 transpose buffer (80 B: conflict-free 16-B reads)
 
-template <int BT, int STAGES>
+template <int BT, int WS, int XS>
 struct FgShape {
   static_assert(BT % 16 == 0 && BT >= 128 && BT <= 256, "token tiles of 128..256 rows");
   static constexpr uint32_t kWBytes = 128 * kTcBK * 2;            // one 128-row weight box: 16 KB
-  static constexpr uint32_t kStageBytes = 2 * kWBytes + BT * kTcBK * 2;
+  static constexpr uint32_t kWStage = 2 * kWBytes;                // both boxes of a k-block
+  static constexpr uint32_t kXStage = BT * kTcBK * 2;             // BT token rows of 128 bytes
+  static_assert(kXStage % 1024 == 0, "token stages start on 1024-byte swizzle atoms");
   static constexpr size_t kXsBytes = 4 * 32 * kFgXsStride * 2;    // transpose buffers of the 4 epilogue warps
-  static constexpr size_t kDynSmem = (size_t)STAGES * kStageBytes + kXsBytes + 1024;
+  static constexpr size_t kDynSmem = (size_t)WS * kWStage + (size_t)XS * kXStage + kXsBytes + 1024;
 };
 
 struct FgParams {
@@ -189,14 +196,14 @@ __device__ __forceinline__ void fg_drain(uint32_t t_lane, uint32_t col0, uint32_
 // same 128-byte rows), results scaled by weight-row and token scales.
 // GATHER: the token rows are read straight from x through row_src (tile::gather4
 // of a one-row box), so the permutation needs no buffer of its own.
-template <int EPI, int BT, int STAGES, bool FP8 = false, bool GATHER = false>
+template <int EPI, int BT, int WS, int XS, bool FP8 = false, bool GATHER = false>
 __global__ void __launch_bounds__(kFgThreads, 1)
     ffn_grouped_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_constant__ FgTokenMaps maps,
                        FgParams p) {
   const CUtensorMap* map_x = maps.m;
-  using S = FgShape<BT, STAGES>;
+  using S = FgShape<BT, WS, XS>;
   extern __shared__ uint8_t dyn_smem[];
-  __shared__ __align__(8) uint64_t full_bar[STAGES], empty_bar[STAGES];
+  __shared__ __align__(8) uint64_t wfull[WS], wempty[WS], xfull[XS], xempty[XS];
   __shared__ __align__(8) uint64_t tmem_full[2], tmem_empty[2], drain_bar;
   __shared__ uint32_t tmem_holder;
   __shared__ volatile uint32_t abort_flag;
@@ -204,8 +211,9 @@ __global__ void __launch_bounds__(kFgThreads, 1)
   __shared__ int32_t scan_scratch[33];
   __shared__ int32_t src_rows[GATHER ? BT : 1];  // gather: source token of each row of the current tile
 
-  uint8_t* ring = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(dyn_smem) + 1023) & ~uintptr_t(1023));
-  __nv_bfloat16* xs_all = reinterpret_cast<__nv_bfloat16*>(ring + (size_t)STAGES * S::kStageBytes);
+  uint8_t* ring_w = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(dyn_smem) + 1023) & ~uintptr_t(1023));
+  uint8_t* ring_x = ring_w + (size_t)WS * S::kWStage;
+  __nv_bfloat16* xs_all = reinterpret_cast<__nv_bfloat16*>(ring_x + (size_t)XS * S::kXStage);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
   // ---- per-expert token-tile prefix (every CTA computes it from kept)
@@ -216,9 +224,13 @@ __global__ void __launch_bounds__(kFgThreads, 1)
   const int total_tiles = total_tt * p.f_tiles;
 
   if (tid == 0) {
-    for (int s = 0; s < STAGES; ++s) {
-      mbar_init(&full_bar[s], 1);
-      mbar_init(&empty_bar[s], 1);
+    for (int s = 0; s < WS; ++s) {
+      mbar_init(&wfull[s], 1);
+      mbar_init(&wempty[s], 1);
+    }
+    for (int s = 0; s < XS; ++s) {
+      mbar_init(&xfull[s], 1);
+      mbar_init(&xempty[s], 1);
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(&tmem_full[a], 1);
@@ -240,30 +252,56 @@ __global__ void __launch_bounds__(kFgThreads, 1)
   const uint32_t tmem_base = tmem_holder;
 
   if (warp == 0) {
-    // ------------------------------------------------------------ TMA producer
-    // Lane 0 issues every copy; with GATHER the whole warp first stages the
-    // tile's source rows in shared memory.  The loop's exit test is taken by
-    // lane 0 and broadcast, so the warp never diverges around __syncwarp.
+    // ------------------------------------------------------------ weight producer
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      uint32_t armed = 0, armed_parity = 0;
+      for (int t = blockIdx.x; t < total_tiles && !abort_flag; t += gridDim.x) {
+        const FgTile tl = fg_decode<BT>(t, mbp, p);
+        // weight rows of the tile's two 128-row boxes
+        const int64_t we = p.w_map != nullptr ? p.w_map[tl.e] : tl.e;
+        const int64_t a0 = we * p.a_rows + (EPI == kTcSwiglu ? 128 * tl.ft : 256 * tl.ft);
+        const int64_t a1 = EPI == kTcSwiglu ? a0 + p.up_rows : a0 + 128;
+        for (int kb = 0; kb < p.k_blocks; ++kb) {
+          if (!mbar_wait(&wempty[stage], phase ^ 1u, &abort_flag)) {
+            abort_flag = 1;
+            raise_error(kErrTimeout);
+            break;
+          }
+          uint8_t* sw = ring_w + (size_t)stage * S::kWStage;
+          const int kx = kb * (FP8 ? 128 : kTcBK);
+          mbar_expect_tx(&wfull[stage], S::kWStage);
+          tma_load_2d(sw, &map_w, kx, (int)a0, &wfull[stage]);
+          tma_load_2d(sw + S::kWBytes, &map_w, kx, (int)a1, &wfull[stage]);
+          armed |= 1u << stage;
+          armed_parity = (armed_parity & ~(1u << stage)) | (phase << stage);
+          if (++stage == WS) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+      if (abort_flag) {  // let every armed copy land before shared memory is released
+        for (int s = 0; s < WS; ++s)
+          if ((armed >> s) & 1u) mbar_wait(&wfull[s], (armed_parity >> s) & 1u);
+      }
+    }
+  } else if (warp == 6) {
+    // ------------------------------------------------------------ token producer
+    // Lane 0 arms each stage; the copies are issued by lane 0 (boxes) or by
+    // every lane (GATHER, after the warp staged the tile's source rows).  Exit
+    // tests are taken by lane 0 and broadcast, so the warp never diverges
+    // around __syncwarp.
     int stage = 0;
     uint32_t phase = 0;
     uint32_t armed = 0, armed_parity = 0;
-    // weight rows of the two 128-row boxes of a tile
-    auto weight_rows = [&](const FgTile& tl, int64_t& a0, int64_t& a1) {
-      const int64_t we = p.w_map != nullptr ? p.w_map[tl.e] : tl.e;
-      if (EPI == kTcSwiglu) {
-        a0 = we * p.a_rows + 128 * tl.ft;
-        a1 = a0 + p.up_rows;
-      } else {
-        a0 = we * p.a_rows + 256 * tl.ft;
-        a1 = a0 + 128;
-      }
-    };
     for (int t = blockIdx.x; t < total_tiles; t += gridDim.x) {
       if (__shfl_sync(0xffffffffu, abort_flag != 0 ? 1 : 0, 0)) break;
       const FgTile tl = fg_decode<BT>(t, mbp, p);
       const int n16 = (int)round16(tl.n);
       if (GATHER) {
-        __syncwarp();  // lane 0 has issued every gather of the previous tile
+        __syncwarp();  // every gather of the previous tile has been issued
         for (int i = lane; i < n16; i += 32) {
           // rows past the tile's end repeat its first row (computed, masked on store)
           const int32_t src = p.row_src[tl.r0 + (i < tl.n ? i : 0)];
@@ -271,60 +309,53 @@ __global__ void __launch_bounds__(kFgThreads, 1)
         }
         __syncwarp();
       }
-      int64_t a0, a1;
-      weight_rows(tl, a0, a1);
-      const uint32_t x_bytes = round16(tl.n) * (uint32_t)(kTcBK * 2);
+      const uint32_t x_bytes = (uint32_t)n16 * (uint32_t)(kTcBK * 2);
+      bool ok = true;
       for (int kb = 0; kb < p.k_blocks; ++kb) {
-        // lane 0 waits for the stage, arms it and loads the weights; with
-        // GATHER every lane then issues its share of the four-row gathers
-        int ok = 1;
-        if (lane == 0) {
-          if (!mbar_wait(&empty_bar[stage], phase ^ 1u, &abort_flag)) {
-            abort_flag = 1;
-            raise_error(kErrTimeout);
-            ok = 0;
-          }
+        int w_ok = 1;
+        if (lane == 0 && !mbar_wait(&xempty[stage], phase ^ 1u, &abort_flag)) {
+          abort_flag = 1;
+          raise_error(kErrTimeout);
+          w_ok = 0;
         }
-        if (GATHER) ok = __shfl_sync(0xffffffffu, ok, 0);
-        if (!ok) break;
-        uint8_t* sw = ring + (size_t)stage * S::kStageBytes;
-        uint8_t* sx = sw + 2 * S::kWBytes;
+        if (!__shfl_sync(0xffffffffu, w_ok, 0)) {
+          ok = false;
+          break;
+        }
+        uint8_t* sx = ring_x + (size_t)stage * S::kXStage;
         const int kx = kb * (FP8 ? 128 : kTcBK);
-        if (lane == 0) {
-          mbar_expect_tx(&full_bar[stage], 2 * S::kWBytes + x_bytes);
-          tma_load_2d(sw, &map_w, kx, (int)a0, &full_bar[stage]);
-          tma_load_2d(sw + S::kWBytes, &map_w, kx, (int)a1, &full_bar[stage]);
-        }
+        if (lane == 0) mbar_expect_tx(&xfull[stage], x_bytes);
         if (GATHER) {
           __syncwarp();  // the stage is armed before any gather can complete on it
           for (int i = 4 * lane; i < n16; i += 4 * 32)
             tma_gather4(sx + i * (kTcBK * 2), &map_x[0], kx, src_rows[i], src_rows[i + 1], src_rows[i + 2],
-                        src_rows[i + 3], &full_bar[stage]);
+                        src_rows[i + 3], &xfull[stage]);
         } else if (lane == 0) {
           // round16(n) rows as boxes of 128 rows, then at most one each of 64, 32 and 16
           int b = 0;
-          for (; b + 128 <= n16; b += 128) tma_load_2d(sx + b * (kTcBK * 2), &map_x[0], kx, tl.r0 + b, &full_bar[stage]);
-          if ((n16 - b) & 64) { tma_load_2d(sx + b * (kTcBK * 2), &map_x[1], kx, tl.r0 + b, &full_bar[stage]); b += 64; }
-          if ((n16 - b) & 32) { tma_load_2d(sx + b * (kTcBK * 2), &map_x[2], kx, tl.r0 + b, &full_bar[stage]); b += 32; }
-          if ((n16 - b) & 16) tma_load_2d(sx + b * (kTcBK * 2), &map_x[3], kx, tl.r0 + b, &full_bar[stage]);
+          for (; b + 128 <= n16; b += 128) tma_load_2d(sx + b * (kTcBK * 2), &map_x[0], kx, tl.r0 + b, &xfull[stage]);
+          if ((n16 - b) & 64) { tma_load_2d(sx + b * (kTcBK * 2), &map_x[1], kx, tl.r0 + b, &xfull[stage]); b += 64; }
+          if ((n16 - b) & 32) { tma_load_2d(sx + b * (kTcBK * 2), &map_x[2], kx, tl.r0 + b, &xfull[stage]); b += 32; }
+          if ((n16 - b) & 16) tma_load_2d(sx + b * (kTcBK * 2), &map_x[3], kx, tl.r0 + b, &xfull[stage]);
         }
         armed |= 1u << stage;
         armed_parity = (armed_parity & ~(1u << stage)) | (phase << stage);
-        if (++stage == STAGES) {
+        if (++stage == XS) {
           stage = 0;
           phase ^= 1u;
         }
       }
+      if (!ok) break;
     }
     if (lane == 0 && abort_flag) {
-      for (int s = 0; s < STAGES; ++s)
-        if ((armed >> s) & 1u) mbar_wait(&full_bar[s], (armed_parity >> s) & 1u);
+      for (int s = 0; s < XS; ++s)
+        if ((armed >> s) & 1u) mbar_wait(&xfull[s], (armed_parity >> s) & 1u);
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
-      int stage = 0;
-      uint32_t phase = 0;
+      int ws = 0, xs_ = 0;
+      uint32_t wph = 0, xph = 0;
       int slot = 0;              // TMEM slot of the next tile of at most 128 rows
       uint32_t slot_phase = 0;   // bit s: uses of slot s so far, mod 2
       for (int t = blockIdx.x; t < total_tiles && !abort_flag; t += gridDim.x) {
@@ -343,7 +374,7 @@ __global__ void __launch_bounds__(kFgThreads, 1)
         }
         tc_fence_after();
         for (int kb = 0; kb < p.k_blocks; ++kb) {
-          if (!mbar_wait(&full_bar[stage], phase, &abort_flag)) {
+          if (!mbar_wait(&wfull[ws], wph, &abort_flag) || !mbar_wait(&xfull[xs_], xph, &abort_flag)) {
             abort_flag = 1;
             raise_error(kErrTimeout);
             ok = false;
@@ -351,8 +382,9 @@ __global__ void __launch_bounds__(kFgThreads, 1)
           }
           tc_fence_after();
           // descriptors of the stage's operands; a K=16 step advances 32 bytes (2 units)
-          const uint64_t dw0 = umma_desc_sw128(smem_u32(ring + (size_t)stage * S::kStageBytes));
-          const uint64_t dw1 = dw0 + (S::kWBytes >> 4), dx = dw0 + ((2 * S::kWBytes) >> 4);
+          const uint64_t dw0 = umma_desc_sw128(smem_u32(ring_w + (size_t)ws * S::kWStage));
+          const uint64_t dw1 = dw0 + (S::kWBytes >> 4);
+          const uint64_t dx = umma_desc_sw128(smem_u32(ring_x + (size_t)xs_ * S::kXStage));
 #pragma unroll
           for (int k = 0; k < kTcBK / 16; ++k) {
             const uint32_t acc = (kb | k) != 0 ? 1u : 0u;
@@ -364,10 +396,15 @@ __global__ void __launch_bounds__(kFgThreads, 1)
               umma_bf16(c1, dw1 + 2 * k, dx + 2 * k, idesc, acc);
             }
           }
-          umma_commit(&empty_bar[stage]);
-          if (++stage == STAGES) {
-            stage = 0;
-            phase ^= 1u;
+          umma_commit(&wempty[ws]);
+          umma_commit(&xempty[xs_]);
+          if (++ws == WS) {
+            ws = 0;
+            wph ^= 1u;
+          }
+          if (++xs_ == XS) {
+            xs_ = 0;
+            xph ^= 1u;
           }
         }
         if (!ok) break;
@@ -383,7 +420,7 @@ __global__ void __launch_bounds__(kFgThreads, 1)
       umma_commit(&drain_bar);
       mbar_wait(&drain_bar, 0u);
     }
-  } else {
+  } else if (warp >= 2 && warp <= 5) {
     // ------------------------------------------------------------ epilogue (warps 2..5)
     const int quarter = warp & 3;
     __nv_bfloat16* xs = xs_all + quarter * 32 * kFgXsStride;

@@ -130,6 +130,7 @@ struct LayerBuffers {
   void* layout_ws;
   size_t layout_ws_bytes;
   float* logits;
+  void* logits_ws;     // split sums of the router logits
   int32_t* ids;
   float* w;
   int32_t* counts;
@@ -154,6 +155,10 @@ struct LayerBuffers {
 
 size_t shared_ws_bytes(const moe_config& c) { return align_up((size_t)c.T * c.shared_I * ds_of(c), 256) + 256; }
 
+// Router logits: float32 partial sums of up to kLogitsMaxSplit slices of h.
+constexpr int kLogitsMaxSplit = 8;
+size_t logits_ws_bytes(const moe_config& c) { return align_up((size_t)kLogitsMaxSplit * c.T * c.E * 4, 256) + 256; }
+
 size_t ffn_fp8_ws_bytes(const moe_config& c);
 
 LayerBuffers carve_layer(const moe_config& c, void* ws, bool host_io, bool block = false, bool fp8 = false) {
@@ -164,6 +169,7 @@ LayerBuffers carve_layer(const moe_config& c, void* ws, bool host_io, bool block
   b.layout_ws_bytes = layout_scratch_bytes(A, nphys(c));
   b.layout_ws = cv.take<char>(b.layout_ws_bytes);
   b.logits = cv.take<float>((size_t)c.T * c.E);
+  b.logits_ws = cv.take<char>(logits_ws_bytes(c));
   b.ids = cv.take<int32_t>(A);
   b.w = cv.take<float>(A);
   b.counts = cv.take<int32_t>(nphys(c));
@@ -499,15 +505,19 @@ moe_status launch_ffn_tokens_m(const moe_config& c, const void* xp, const int32_
 // The grouped FFN: gate/up GEMM with the SwiGLU epilogue into the bf16
 // intermediate, then the down GEMM into yp, both with the expert weights as
 // the MMA's M operand and the expert's token rows as N (ffn_grouped.cuh).
-// Token tiles of up to 160 rows in a 4-stage ring of 52 KB stages.
-constexpr int kFgTileRows = 160, kFgStages = 4;
+// Token tiles of up to 160 rows; a ring of 4 weight k-blocks (32 KB each) and
+// one of 4 token k-blocks (20 KB each).  Measured at DeepSeek-V3 T=4096: 3.94
+// ms; rings of 5 + 2 (5.20 ms), 4 + 3 (4.13), 128-row tiles with 5 + 3 (4.30)
+// and 256-row tiles with 4 + 2 (5.13) starve the MMA of token k-blocks, whose
+// L2 latency under this load needs four in flight.
+constexpr int kFgTileRows = 160, kFgWStages = 4, kFgXStages = 4;
 // row_src non-null: the gate/up GEMM gathers its rows from x = xp through row_src
 // (no permuted copy of x); else xp holds the permuted rows.
-template <int BT, int STAGES>
+template <int BT, int WS, int XS>
 moe_status launch_ffn_grouped(const moe_config& c, const void* xp, const int32_t* offsets, const int32_t* kept,
                               const int32_t* w_map, int n_w, const void* w13, const void* w2, void* yp, void* inter,
                               cudaStream_t st, const int32_t* row_src = nullptr) {
-  using S = FgShape<BT, STAGES>;
+  using S = FgShape<BT, WS, XS>;
   const int64_t R = rows_of(c);
   const int grid = device_info().sms;
   CUtensorMap w1m, w2m;
@@ -543,9 +553,9 @@ moe_status launch_ffn_grouped(const moe_config& c, const void* xp, const int32_t
   p2.ldo = c.h;
   p1.row_src = row_src;
   p2.row_src = nullptr;
-  auto k1 = row_src != nullptr ? ffn_grouped_kernel<kTcSwiglu, BT, STAGES, false, true>
-                               : ffn_grouped_kernel<kTcSwiglu, BT, STAGES>;
-  auto k2 = ffn_grouped_kernel<kTcStore, BT, STAGES>;
+  auto k1 = row_src != nullptr ? ffn_grouped_kernel<kTcSwiglu, BT, WS, XS, false, true>
+                               : ffn_grouped_kernel<kTcSwiglu, BT, WS, XS>;
+  auto k2 = ffn_grouped_kernel<kTcStore, BT, WS, XS>;
   CUDA_TRY(allow_smem(k1, S::kDynSmem));
   CUDA_TRY(allow_smem(k2, S::kDynSmem));
   k1<<<grid, kFgThreads, S::kDynSmem, st>>>(w1m, x1, p1);
@@ -571,7 +581,7 @@ moe_status launch_ffn_tc(const moe_config& c, const void* xp, const int32_t* off
   if ((int64_t)n_w * 2 * c.I >= INT32_MAX || (int64_t)n_w * c.h >= INT32_MAX) return MOE_ERR_UNSUPPORTED;
   if (expected_rows_per_expert(c) > MOE_FFN_SWAP_MAX_ROWS)
     return launch_ffn_tokens_m(c, xp, offsets, kept, w_map, n_w, w13, w2, yp, inter, st);
-  return launch_ffn_grouped<kFgTileRows, kFgStages>(c, xp, offsets, kept, w_map, n_w, w13, w2, yp, inter, st);
+  return launch_ffn_grouped<kFgTileRows, kFgWStages, kFgXStages>(c, xp, offsets, kept, w_map, n_w, w13, w2, yp, inter, st);
 }
 
 // Router logits of a bf16 layer on the tensor cores: one segment of T rows
@@ -579,7 +589,7 @@ moe_status launch_ffn_tc(const moe_config& c, const void* xp, const int32_t* off
 // the tiles cover the SMs (BN halves while twice the tiles still fit one wave).
 template <int BN, int STAGES>
 moe_status launch_logits_tc_bn(const moe_config& c, const void* x, const void* w_r, const float* off,
-                               float* logits, cudaStream_t st) {
+                               float* logits, int k_split, void* ws, cudaStream_t st) {
   using S = TcShape<BN, STAGES>;
   CUtensorMap a, b;
   MOE_TRY(make_tensor_map(&a, x, c.h, c.T, kTcBM));
@@ -596,35 +606,69 @@ moe_status launch_logits_tc_bn(const moe_config& c, const void* x, const void* w
   p.out = logits;
   p.ldo = c.E;
   p.col_bias = off;
-  const int64_t tiles = (int64_t)((c.T + kTcBM - 1) / kTcBM) * p.n_tiles;
+  p.k_split = k_split;
+  p.partial = static_cast<float*>(ws);
+  const int64_t items = (int64_t)((c.T + kTcBM - 1) / kTcBM) * p.n_tiles * k_split;
   const int sms = device_info().sms;
-  const int grid = (int)(tiles < sms ? tiles : sms);
+  const int grid = (int)(items < sms ? items : sms);
   auto k = tc_gemm_kernel<kTcLogits, BN, STAGES>;
   CUDA_TRY(allow_smem(k, S::kDynSmem));
   k<<<grid, kTcThreads, S::kDynSmem, st>>>(a, b, p);
   CUDA_TRY(cudaGetLastError());
+  if (k_split > 1) {
+    const int64_t n = (int64_t)c.T * c.E;
+    const int64_t lanes = (c.E % 4 == 0) ? n / 4 : n;
+    int64_t blocks = (lanes + 255) / 256;
+    if (blocks > (int64_t)sms * 8) blocks = (int64_t)sms * 8;
+    logits_reduce_kernel<<<(unsigned)blocks, 256, 0, st>>>(p.partial, k_split, n, c.E, off, logits);
+    CUDA_TRY(cudaGetLastError());
+  }
   return MOE_OK;
 }
 
-int logits_tile_n(const moe_config& c, int sms) {
-  int bn = 16;
-  while (bn < c.E && bn < 256) bn *= 2;
-  const int64_t mblocks = (c.T + kTcBM - 1) / kTcBM;
-  while (bn > 16 && mblocks * ((c.E + bn / 2 - 1) / (bn / 2)) <= sms) bn /= 2;
-  return bn;
+// Column-tile width BN and number of slices of the sum over h.  Each work item
+// (row tile, column tile, slice) streams its k-blocks through one CTA's TMA
+// ring, whose rate is bound by latency, so the choice minimises the bytes the
+// busiest SM streams: waves x k-blocks per slice x (16 KB of x + BN rows of w_r),
+// with at least 8 k-blocks per slice and at most kLogitsMaxSplit slices; ties
+// go to fewer work items.
+struct LogitsPlan {
+  int bn, k_split;
+};
+LogitsPlan logits_plan(const moe_config& c, int sms) {
+  const int64_t mb = (c.T + kTcBM - 1) / kTcBM;
+  const int kb = c.h / kTcBK;
+  LogitsPlan best{256, 1};
+  int64_t best_cost = -1, best_items = 0;
+  for (int bn = 16; bn <= 256; bn *= 2) {
+    if (bn > 16 && bn / 2 >= c.E) break;  // a narrower tile already covers E
+    for (int ks = 1; ks <= kLogitsMaxSplit; ++ks) {
+      if (ks > 1 && kb / ks < 8) break;
+      const int64_t items = mb * ((c.E + bn - 1) / bn) * ks;
+      const int64_t waves = (items + sms - 1) / sms;
+      const int64_t cost = waves * ((kb + ks - 1) / ks) * (int64_t)(kTcBM * 128 + bn * 128);
+      if (best_cost < 0 || cost < best_cost || (cost == best_cost && items < best_items)) {
+        best = {bn, ks};
+        best_cost = cost;
+        best_items = items;
+      }
+    }
+  }
+  return best;
 }
 
 moe_status launch_logits(const moe_config& c, const void* x, const void* w_r, const float* off, float* logits,
-                         cudaStream_t st) {
+                         void* ws, cudaStream_t st) {
   if (c.T == 0) return MOE_OK;
   // float32 layers stay on CUDA cores: a TF32 product would miss their 1e-4 tolerance
   if (c.dtype == MOE_F32) return launch_logits_simt(c, x, w_r, off, logits, st);
-  switch (logits_tile_n(c, device_info().sms)) {
-    case 16: return launch_logits_tc_bn<16, 8>(c, x, w_r, off, logits, st);
-    case 32: return launch_logits_tc_bn<32, 8>(c, x, w_r, off, logits, st);
-    case 64: return launch_logits_tc_bn<64, 8>(c, x, w_r, off, logits, st);
-    case 128: return launch_logits_tc_bn<128, 6>(c, x, w_r, off, logits, st);
-    default: return launch_logits_tc_bn<256, 4>(c, x, w_r, off, logits, st);
+  const LogitsPlan lp = logits_plan(c, device_info().sms);
+  switch (lp.bn) {
+    case 16: return launch_logits_tc_bn<16, 8>(c, x, w_r, off, logits, lp.k_split, ws, st);
+    case 32: return launch_logits_tc_bn<32, 8>(c, x, w_r, off, logits, lp.k_split, ws, st);
+    case 64: return launch_logits_tc_bn<64, 8>(c, x, w_r, off, logits, lp.k_split, ws, st);
+    case 128: return launch_logits_tc_bn<128, 6>(c, x, w_r, off, logits, lp.k_split, ws, st);
+    default: return launch_logits_tc_bn<256, 4>(c, x, w_r, off, logits, lp.k_split, ws, st);
   }
 }
 
@@ -650,7 +694,7 @@ moe_status launch_ffn_fp8(const moe_config& c, const uint8_t* xq, const float* s
   __nv_bfloat16* inter = reinterpret_cast<__nv_bfloat16*>(w);
   uint8_t* interq = reinterpret_cast<uint8_t*>(w + align_up((size_t)R * c.I * 2, 256));
   float* sinter = reinterpret_cast<float*>(w + align_up((size_t)R * c.I * 2, 256) + align_up((size_t)R * c.I, 256));
-  using S = FgShape<kFgTileRows, kFgStages>;
+  using S = FgShape<kFgTileRows, kFgWStages, kFgXStages>;
   CUtensorMap w1m, w2m;
   FgTokenMaps x1, x2;
   MOE_TRY(make_tensor_map(&w1m, w13q, c.h, (uint64_t)n_w * 2 * c.I, 128, true));
@@ -684,8 +728,8 @@ moe_status launch_ffn_fp8(const moe_config& c, const uint8_t* xq, const float* s
   p2.w_scale = s2;
   p2.x_scale = sinter;
   const int grid = device_info().sms;
-  auto k1 = ffn_grouped_kernel<kTcSwiglu, kFgTileRows, kFgStages, true>;
-  auto k2 = ffn_grouped_kernel<kTcStore, kFgTileRows, kFgStages, true>;
+  auto k1 = ffn_grouped_kernel<kTcSwiglu, kFgTileRows, kFgWStages, kFgXStages, true>;
+  auto k2 = ffn_grouped_kernel<kTcStore, kFgTileRows, kFgWStages, kFgXStages, true>;
   CUDA_TRY(allow_smem(k1, S::kDynSmem));
   CUDA_TRY(allow_smem(k2, S::kDynSmem));
   k1<<<grid, kFgThreads, S::kDynSmem, st>>>(w1m, x1, p1);
@@ -723,7 +767,7 @@ moe_status launch_ffn_gather(const moe_config& c, const void* x, const int32_t* 
   if (rows_of(c) == 0 || c.T == 0) return MOE_OK;
   if (c.dtype != MOE_BF16 || expected_rows_per_expert(c) > MOE_FFN_SWAP_MAX_ROWS) return MOE_ERR_UNSUPPORTED;
   if ((int64_t)n_w * 2 * c.I >= INT32_MAX || (int64_t)n_w * c.h >= INT32_MAX) return MOE_ERR_UNSUPPORTED;
-  return launch_ffn_grouped<kFgTileRows, kFgStages>(c, x, offsets, kept, w_map, n_w, w13, w2, yp, inter, st,
+  return launch_ffn_grouped<kFgTileRows, kFgWStages, kFgXStages>(c, x, offsets, kept, w_map, n_w, w13, w2, yp, inter, st,
                                                     row_src);
 }
 
@@ -859,7 +903,7 @@ moe_status layer_core(const moe_config& c, const void* x, const void* w_r, const
   int64_t* n_ij = o.n_ij ? o.n_ij : b.n_ij;
   int64_t* rank_bytes = o.rank_bytes ? o.rank_bytes : b.rank_bytes;
   moe_layout_stats* stats = o.stats ? o.stats : b.stats;
-  MOE_TRY(launch_logits(c, x, w_r, logit_offset, logits, st));
+  MOE_TRY(launch_logits(c, x, w_r, logit_offset, logits, b.logits_ws, st));
   MOE_TRY(launch_route(c, logits, sel_bias, ids, w, st));
   const int32_t* lids = ids;  // expert ids the layout sees: physical replicas when the plan has any
   if (c.n_redundant > 0) {
@@ -934,6 +978,7 @@ moe_status moe_workspace_size(const moe_config* cfg, int32_t op, size_t* bytes) 
     case MOE_OP_BLOCK_HOST: *bytes = carve_layer(*cfg, nullptr, true, true).total; return MOE_OK;
     case MOE_OP_FFN_FP8: *bytes = ffn_fp8_ws_bytes(*cfg); return MOE_OK;
     case MOE_OP_LAYER_FP8: *bytes = carve_layer(*cfg, nullptr, false, false, true).total; return MOE_OK;
+    case MOE_OP_LOGITS: *bytes = logits_ws_bytes(*cfg); return MOE_OK;
   }
   return MOE_ERR_INVALID_ARG;
 }
@@ -945,15 +990,16 @@ moe_status moe_workspace_init(void* workspace, size_t workspace_bytes, void* str
 }
 
 moe_status moe_router_logits(const moe_config* cfg, const void* x, const void* w_r, const float* logit_offset,
-                             float* logits, void* stream) {
+                             float* logits, void* workspace, void* stream) {
   MOE_TRY(validate(cfg));
   if (cfg->T > 0) {
     MOE_TRY(check_dtype_ptr(x));
     MOE_TRY(check_ptr(logits, 4));
+    if (cfg->dtype == MOE_BF16) MOE_TRY(check_ptr(workspace, 256));
   }
   MOE_TRY(check_dtype_ptr(w_r));
   MOE_TRY(check_opt_ptr(logit_offset, 4));
-  return launch_logits(*cfg, x, w_r, logit_offset, logits, as_stream(stream));
+  return launch_logits(*cfg, x, w_r, logit_offset, logits, workspace, as_stream(stream));
 }
 
 moe_status moe_route(const moe_config* cfg, const float* logits, const float* sel_bias, int32_t* topk_ids,

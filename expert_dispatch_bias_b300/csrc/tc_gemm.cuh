@@ -17,6 +17,10 @@
 //           tile and stored in bf16 (the intermediate activation);
 //   store   bf16 store of the accumulator (the down projection);
 //   logits  float32 store plus an optional per-column offset (the router).
+//           With k_split > 1 the sum over K is cut into k_split slices, each
+//           its own work item that stores its raw float32 tile to
+//           partial[slice]; a separate kernel adds the slices in slice order
+//           plus the offset (logits_reduce_kernel).
 // Roles (192 threads):
 //   warp 0       one thread issues TMA loads (128 A rows and BN B rows of one
 //                64-element k-block, 128-byte swizzle) into a STAGES-deep ring;
@@ -69,7 +73,15 @@ struct TcParams {
   int64_t ldo;
   const float* col_bias;    // logits: per-column offset [n_valid] or null
   const int32_t* w_map;     // segment -> its B (weight) matrix, or null: segment e uses B_e
+  int k_split;              // logits: slices of the K sum (<= 1: none)
+  float* partial;           // logits, k_split > 1: [k_split][dense_rows][ldo] float32
 };
+
+// K-blocks [kb0, kb1) of slice s of S.
+__device__ __forceinline__ void tc_k_range(int s, int S, int k_blocks, int* kb0, int* kb1) {
+  *kb0 = (int)((int64_t)s * k_blocks / S);
+  *kb1 = (int)((int64_t)(s + 1) * k_blocks / S);
+}
 
 // ------------------------------------------------------------------ PTX wrappers
 __device__ __forceinline__ void tma_load_2d(void* smem_dst, const CUtensorMap* map, int x, int y, uint64_t* bar) {
@@ -189,6 +201,20 @@ __device__ __forceinline__ void store_bf16_row(__nv_bfloat16* dst, const float* 
     d[i] = make_uint4(packed[4 * i], packed[4 * i + 1], packed[4 * i + 2], packed[4 * i + 3]);
 }
 
+// Stores N float32 columns n0.. of a row, skipping columns >= n_valid.
+template <int N>
+__device__ __forceinline__ void store_f32_cols(float* row, int n0, int n_valid, bool vec, const float* a) {
+  if (vec && n0 + N <= n_valid) {
+    float4* d = reinterpret_cast<float4*>(row + n0);
+#pragma unroll
+    for (int i = 0; i < N / 4; ++i) d[i] = make_float4(a[4 * i], a[4 * i + 1], a[4 * i + 2], a[4 * i + 3]);
+  } else {
+#pragma unroll
+    for (int i = 0; i < N; ++i)
+      if (n0 + i < n_valid) row[n0 + i] = a[i];
+  }
+}
+
 // ------------------------------------------------------------------ tile schedule
 struct TcTile {
   int e;        // segment (expert)
@@ -239,7 +265,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   __syncthreads();
   const int32_t total_mb = block_exclusive_scan(mbp, p.E, scan_scratch);
   if (tid == 0) mbp[p.E] = total_mb;
-  const int total_tiles = total_mb * p.n_tiles;
+  const int KS = (EPI == kTcLogits && p.k_split > 1) ? p.k_split : 1;
+  const int total_tiles = total_mb * p.n_tiles * KS;  // work items: (tile, K slice)
 
   if (tid == 0) {
     for (int s = 0; s < STAGES; ++s) {
@@ -273,9 +300,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       uint32_t armed = 0;  // bit s: stage s was ever armed; its last arm had parity (phase bit at the time)
       uint32_t armed_parity = 0;
       for (int t = blockIdx.x; t < total_tiles && !abort_flag; t += gridDim.x) {
-        const TcTile tl = tc_decode(t, mbp, p);
+        const TcTile tl = tc_decode(t / KS, mbp, p);
+        int kb0, kb1;
+        tc_k_range(t % KS, KS, p.k_blocks, &kb0, &kb1);
         const int64_t brow = (int64_t)(p.w_map != nullptr ? p.w_map[tl.e] : tl.e) * p.b_rows;
-        for (int kb = 0; kb < p.k_blocks; ++kb) {
+        for (int kb = kb0; kb < kb1; ++kb) {
           if (!mbar_wait(&empty_bar[stage], phase ^ 1u, &abort_flag)) {
             abort_flag = 1;
             raise_error(kErrTimeout);
@@ -326,7 +355,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + (uint32_t)(acc * BN);
         bool ok = true;
-        for (int kb = 0; kb < p.k_blocks; ++kb) {
+        int kb0, kb1;
+        tc_k_range(t % KS, KS, p.k_blocks, &kb0, &kb1);
+        for (int kb = kb0; kb < kb1; ++kb) {
           if (!mbar_wait(&full_bar[stage], phase, &abort_flag)) {
             abort_flag = 1;
             raise_error(kErrTimeout);
@@ -339,7 +370,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 #pragma unroll
           for (int k = 0; k < kTcBK / 16; ++k) {
             umma_bf16(d_tmem, umma_desc_sw128(sa + k * 32), umma_desc_sw128(sb + k * 32), idesc,
-                      (kb | k) != 0 ? 1u : 0u);
+                      (kb != kb0 || k != 0) ? 1u : 0u);
           }
           umma_commit(&empty_bar[stage]);
           if (++stage == STAGES) {
@@ -361,6 +392,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   } else {
     // ------------------------------------------------------------ epilogue (warps 2..5)
     const int quarter = warp & 3;
+    // float32 rows as float4 when every row start is 16-byte aligned (the
+    // partial buffers share the output's row pitch and are 256-byte aligned)
+    const bool vec_out = (p.ldo % 4) == 0 && (reinterpret_cast<uintptr_t>(p.out) & 15u) == 0;
     int acc = 0;
     uint32_t acc_phase = 0;
     for (int t = blockIdx.x; t < total_tiles; t += gridDim.x) {
@@ -370,7 +404,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         break;
       }
       tc_fence_after();
-      const TcTile tl = tc_decode(t, mbp, p);
+      const int slice = t % KS;
+      const TcTile tl = tc_decode(t / KS, mbp, p);
       const int row = tl.m0 + quarter * 32 + lane;
       const bool valid = row < tl.m_end;
       const uint32_t taddr = tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(acc * BN);
@@ -410,8 +445,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         }
       } else {
         const int n0 = tl.nt * BN;
-        float* orow = static_cast<float*>(p.out) + (int64_t)row * p.ldo;
-        const bool vec = (p.ldo % 4) == 0 && (reinterpret_cast<uintptr_t>(p.out) & 15u) == 0;
+        // a slice stores its raw sum to its partial buffer; the offset is added
+        // once, to the sum of the slices
+        float* orow = KS > 1 ? p.partial + ((int64_t)slice * p.dense_rows + row) * p.ldo
+                             : static_cast<float*>(p.out) + (int64_t)row * p.ldo;
+        const bool bias = KS == 1 && p.col_bias != nullptr;
 #pragma unroll 1
         for (int c = 0; c < BN; c += CH) {
           uint32_t v[CH];
@@ -422,17 +460,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 #pragma unroll
             for (int i = 0; i < CH; ++i) {
               const int n = n0 + c + i;
-              a[i] = __uint_as_float(v[i]) + ((p.col_bias != nullptr && n < p.n_valid) ? p.col_bias[n] : 0.0f);
+              a[i] = __uint_as_float(v[i]) + ((bias && n < p.n_valid) ? p.col_bias[n] : 0.0f);
             }
-            if (vec && n0 + c + CH <= p.n_valid) {
-              float4* d = reinterpret_cast<float4*>(orow + n0 + c);
-#pragma unroll
-              for (int i = 0; i < CH / 4; ++i) d[i] = make_float4(a[4 * i], a[4 * i + 1], a[4 * i + 2], a[4 * i + 3]);
-            } else {
-#pragma unroll
-              for (int i = 0; i < CH; ++i)
-                if (n0 + c + i < p.n_valid) orow[n0 + c + i] = a[i];
-            }
+            store_f32_cols<CH>(orow, n0 + c, p.n_valid, vec_out, a);
           }
         }
       }
@@ -451,6 +481,42 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     tc_fence_after();
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base), "r"(S::kTmemCols)
                  : "memory");
+  }
+}
+
+// Router logits from k_split partial sums: out[i] = ((P_0[i] + P_1[i]) + ...)
+// + offset[i % E], slices added in slice order.  P is [k_split][n] with n = T*E;
+// float4 lanes when E % 4 == 0 (every partial starts 256-byte aligned).
+__global__ void __launch_bounds__(256) logits_reduce_kernel(const float* P, int k_split, int64_t n, int E,
+                                                            const float* off, float* out) {
+  const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+  if ((E & 3) == 0) {
+    const int64_t n4 = n >> 2;
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n4; i += stride) {
+      float4 a = __ldcg(reinterpret_cast<const float4*>(P) + i);
+      for (int s = 1; s < k_split; ++s) {
+        const float4 b = __ldcg(reinterpret_cast<const float4*>(P + (int64_t)s * n) + i);
+        a.x += b.x;
+        a.y += b.y;
+        a.z += b.z;
+        a.w += b.w;
+      }
+      if (off != nullptr) {
+        const int e = (int)((i << 2) % E);
+        a.x += off[e];
+        a.y += off[e + 1];
+        a.z += off[e + 2];
+        a.w += off[e + 3];
+      }
+      reinterpret_cast<float4*>(out)[i] = a;
+    }
+  } else {
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += stride) {
+      float a = __ldcg(P + i);
+      for (int s = 1; s < k_split; ++s) a += __ldcg(P + (int64_t)s * n + i);
+      if (off != nullptr) a += off[i % E];
+      out[i] = a;
+    }
   }
 }
 

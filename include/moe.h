@@ -68,7 +68,8 @@ typedef enum {
   MOE_OP_BLOCK = 5,       /* moe_block_forward */
   MOE_OP_BLOCK_HOST = 6,  /* moe_block_forward_host */
   MOE_OP_FFN_FP8 = 7,     /* moe_grouped_ffn_fp8 */
-  MOE_OP_LAYER_FP8 = 8    /* moe_layer_forward_fp8 */
+  MOE_OP_LAYER_FP8 = 8,   /* moe_layer_forward_fp8 */
+  MOE_OP_LOGITS = 9       /* moe_router_logits */
 } moe_op;
 
 /* Layer description.  Limits: T >= 0; h % 64 == 0; I % 64 == 0; 1 <= E <= 1024;
@@ -142,9 +143,14 @@ moe_status moe_workspace_init(void* workspace, size_t workspace_bytes, void* str
 
 /* Router logits ([overview] glossary "Router"): logits[t,e] = sum_j x[t,j] w_r[e,j]
  * (+ logit_offset[e]), float32 accumulation.  x [T,h] dtype; w_r [E,h] dtype;
- * logit_offset [E] float32 or NULL; logits [T,E] float32. */
+ * logit_offset [E] float32 or NULL; logits [T,E] float32.  bf16 layers cut the
+ * sum over j into up to 8 slices (chosen from T, E, h and the SM count) whose
+ * float32 partial sums are added in slice order, so a result never depends on
+ * timing.  workspace: moe_workspace_size(MOE_OP_LOGITS) bytes, 256-byte aligned,
+ * zero-filled once by moe_workspace_init (a successful call leaves it so);
+ * float32 layers ignore it (NULL allowed).  One call at a time per workspace. */
 moe_status moe_router_logits(const moe_config* cfg, const void* x, const void* w_r,
-                             const float* logit_offset, float* logits, void* stream);
+                             const float* logit_offset, float* logits, void* workspace, void* stream);
 
 /* Top-K routing ([overview] glossary "top-K"; [notes] "负载均衡": the aux-loss-free
  * per-expert bias steers selection only; [overview] glossary "Expert group").

@@ -54,6 +54,10 @@ def test_rows_and_workspace_sizes():
     host = moe.moe_workspace_size(_cfg(), moe.MOE_OP_LAYER_HOST)
     assert host >= layer + 2 * 4096 * 7168 * 2
     assert moe.moe_workspace_size(_cfg(T=0), moe.MOE_OP_LAYOUT) > 0
+    # router logits: float32 partial sums of up to 8 slices of h, inside the layer's too
+    logits = moe.moe_workspace_size(_cfg(), moe.MOE_OP_LOGITS)
+    assert logits >= 8 * 4096 * 256 * 4
+    assert layer >= logits + ffn + 2 * 4096 * 8 * 7168 * 2
 
 
 @pytest.mark.parametrize("bad", [

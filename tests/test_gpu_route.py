@@ -22,27 +22,40 @@ def test_router_logits(name):
     cfg = moe.config_from(w)
     L = torch.empty(w.T, w.E, dtype=torch.float32, device="cuda")
     off = dev_of(h["logit_offset"]) if h["logit_offset"] is not None else None
-    moe.moe_router_logits(cfg, dev_of(h["x"]), dev_of(h["w_r"]), off, L)
+    moe.moe_router_logits(cfg, dev_of(h["x"]), dev_of(h["w_r"]), off, L, moe.alloc_workspace(cfg, moe.MOE_OP_LOGITS))
     assert moe.moe_check() == 0
     # float32 accumulation of exact bf16/f32 products vs float64 sums
     assert rel_err(np_of(L), ref, "f32") < 1e-4
 
 
+# (T, h, E): partial row blocks, expert counts that do not fill a column tile,
+# every column-tile width; h of 1024 and more also slices the sum over h
+# (1 row tile of 8 experts at h=4096: 8 slices; 2 row tiles x 8 column tiles of
+# 128 at h=7168: 8; 33 tiles of 256 at h=7168: 4).
 @pytest.mark.parametrize("T,h,E", [(1, 64, 8), (130, 128, 5), (300, 192, 33), (129, 64, 1000), (1200, 128, 256),
-                                   (2500, 64, 1000), (40, 768, 128)])
+                                   (2500, 64, 1000), (40, 768, 128), (130, 1024, 5), (1, 4096, 8),
+                                   (300, 2048, 33), (129, 7168, 1000), (4100, 7168, 256)])
 @pytest.mark.parametrize("offset", [False, True])
 def test_router_logits_ragged(T, h, E, offset):
-    """bf16 logits on the tensor cores: partial row blocks, expert counts that do
-    not fill a column tile, every column-tile width, with and without offsets."""
+    """bf16 logits on the tensor cores, with and without offsets.  A second call
+    on the same workspace gives the same bits (the slice counters are reset and
+    the slices are added in a fixed order)."""
     w = workloads.Workload("logits_case", T=T, h=h, E=E, K=1, I=64, dtype="bf16", score="softmax")
     x = synth.normal(3, synth.TID_TEST + 20, (T, h), 1.0, "bf16")
     wr = synth.normal(3, synth.TID_TEST + 21, (E, h), 1.0 / np.sqrt(h), "bf16")
     off = synth.uniform(3, synth.TID_TEST + 22, E, -2.0, 2.0) if offset else None
     ref = oracle.router_logits(x, wr, "bf16", off)
+    cfg = moe.config_from(w)
+    ws = moe.alloc_workspace(cfg, moe.MOE_OP_LOGITS)
     L = torch.full((T, E), float("nan"), dtype=torch.float32, device="cuda")
-    moe.moe_router_logits(moe.config_from(w), dev_of(x), dev_of(wr), dev_of(off) if offset else None, L)
+    args = (cfg, dev_of(x), dev_of(wr), dev_of(off) if offset else None)
+    moe.moe_router_logits(*args, L, ws)
     assert moe.moe_check() == 0
     assert rel_err(np_of(L), ref, "f32") < 1e-4
+    L2 = torch.full((T, E), float("nan"), dtype=torch.float32, device="cuda")
+    moe.moe_router_logits(*args, L2, ws)
+    assert moe.moe_check() == 0
+    assert torch.equal(L, L2)
 
 
 @pytest.mark.parametrize("name", NAMES)
