@@ -39,10 +39,11 @@ if ROOT not in sys.path:
 METRIC = "MoE-layer tokens/s at DeepSeek-V3 shape; permute GB/s & GEMM % of peak"
 # DRAM bytes (read + write) of the grouped FFN's two launches over its
 # algorithmic bytes, from one ncu capture of the 32-expert DeepSeek-V3-shaped
-# layer (deepseek_v3_e32_T512: 2.974 GB measured / 2.970 GB algorithmic).  Both
-# scale with the touched experts and kept rows, so a full launch's traffic is
-# this ratio times its algorithmic bytes.  Re-measure whenever the kernel changes.
-FFN_TRAFFIC_RATIO = 1.001
+# layer (deepseek_v3_e32_T512: 2.9703 GB measured / 2.9696 GB algorithmic, the
+# kernel with separate weight and token rings).  Both scale with the touched
+# experts and kept rows, so a full launch's traffic is this ratio times its
+# algorithmic bytes.  Re-measure whenever the kernel changes.
+FFN_TRAFFIC_RATIO = 1.0002
 FALLBACK_PEAKS = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0}
 
 
