@@ -66,6 +66,33 @@ inline LayoutScratch layout_scratch_at(void* base, int64_t A, int E) {
   return s;
 }
 
+// Block-wide sum (or max) of one int64 per thread; every thread gets the
+// result.  Shuffles within warps, then one warp over the warp results:
+// no contended atomics.  All threads of the block must call it.
+template <bool MAX>
+__device__ __forceinline__ long long block_reduce_ll(long long v, long long* scratch /* >= 33 */) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = (blockDim.x + 31) >> 5;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    const long long u = __shfl_xor_sync(0xffffffffu, v, o);
+    v = MAX ? (u > v ? u : v) : v + u;
+  }
+  __syncthreads();  // scratch may still be read by a previous call
+  if (lane == 0) scratch[warp] = v;
+  __syncthreads();
+  if (warp == 0) {
+    long long w = lane < nw ? scratch[lane] : 0;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      const long long u = __shfl_xor_sync(0xffffffffu, w, o);
+      w = MAX ? (u > w ? u : w) : w + u;
+    }
+    if (lane == 0) scratch[32] = w;
+  }
+  __syncthreads();
+  return scratch[32];
+}
+
 struct LayoutParams {
   const int32_t* ids;   // [A] = [T, K]
   int64_t A;
@@ -286,40 +313,35 @@ __global__ void __launch_bounds__(kFinalizeThreads) layout_finalize_kernel(Layou
   __syncthreads();
   if (!s_last) return;
   __threadfence();
-  __shared__ unsigned long long s_max, s_sum, s_off;
-  __shared__ int s_touched;
-  __shared__ long long s_kept;
-  if (tid == 0) {
-    s_max = 0;
-    s_sum = 0;
-    s_off = 0;
-    s_touched = 0;
-    s_kept = 0;
-  }
-  __syncthreads();
+  __shared__ long long red[33];
   const long long rowbytes = (long long)p.h * p.ds;
+  long long rmax = 0, rsum = 0, ssum = 0, kept_sum = 0, touched = 0;
   for (int i = tid; i < N; i += kFinalizeThreads) {  // row and column sums of n_ij
     const long long sent = __ldcg(&p.rank_bytes[i]), recv = __ldcg(&p.rank_bytes[N + i]);
     p.rank_bytes[i] = sent * rowbytes;
     p.rank_bytes[N + i] = recv * rowbytes;
-    atomicMax(&s_max, (unsigned long long)recv);
-    atomicAdd(&s_sum, (unsigned long long)recv);
-    atomicAdd(&s_off, (unsigned long long)sent);
+    rmax = recv > rmax ? recv : rmax;
+    rsum += recv;
+    ssum += sent;
   }
   for (int e = tid; e < p.E; e += kFinalizeThreads) {
     const int32_t k = __ldcg(&p.kept[e]);
-    if (k > 0) atomicAdd(&s_touched, 1);
-    atomicAdd(reinterpret_cast<unsigned long long*>(&s_kept), (unsigned long long)k);
+    touched += k > 0;
+    kept_sum += k;
   }
-  __syncthreads();
+  rmax = block_reduce_ll<true>(rmax, red);
+  rsum = block_reduce_ll<false>(rsum, red);
+  ssum = block_reduce_ll<false>(ssum, red);
+  kept_sum = block_reduce_ll<false>(kept_sum, red);
+  touched = block_reduce_ll<false>(touched, red);
   if (tid == 0) {
     moe_layout_stats st;
-    st.kept_total = s_kept;
-    st.dropped = p.A - s_kept;
+    st.kept_total = kept_sum;
+    st.dropped = p.A - kept_sum;
     unsigned long long* diag = reinterpret_cast<unsigned long long*>(p.ws.header + 2);
-    st.offdiag_rows = (long long)(s_off - __ldcg(diag));  // all kept rows minus the diagonal
-    st.experts_touched = s_touched;
-    st.balancedness = s_max == 0 ? 1.0f : (float)((double)s_sum / ((double)N * (double)s_max));
+    st.offdiag_rows = ssum - (long long)__ldcg(diag);  // all kept rows minus the diagonal
+    st.experts_touched = (int32_t)touched;
+    st.balancedness = rmax == 0 ? 1.0f : (float)((double)rsum / ((double)N * (double)rmax));
     *p.stats = st;
     // reset the look-back state for the next call on this workspace
     p.ws.header[0] = 0;
@@ -327,6 +349,173 @@ __global__ void __launch_bounds__(kFinalizeThreads) layout_finalize_kernel(Layou
     *diag = 0;
   }
   for (int t = tid; t < p.num_tiles; t += kFinalizeThreads) p.ws.flags[t] = kTileEmpty;
+}
+
+// Small layouts (T*K <= kLayoutSmallMax) in one block of 1024 threads and one
+// launch: the same stable per-expert ranks (warp w owns assignments
+// [w*256, w*256 + 256) in token order, 8 rounds of 32), the prefix over warps,
+// the offsets, slots, row_src, n_ij (in shared memory when N_EP^2 <=
+// kFinalizeBins, else global atomics), the per-chip bytes and the statistics;
+// no look-back and no cross-block hand-off, so a decode-sized batch costs a few
+// global round trips.  The look-back state in the workspace is not touched.
+constexpr int kLayoutSmallThreads = 1024;
+constexpr int kLayoutSmallItems = 8;
+constexpr int kLayoutSmallMax = kLayoutSmallThreads * kLayoutSmallItems;
+
+__host__ __device__ inline size_t layout_small_smem(int E, int n_ep) {
+  const size_t bins = (size_t)n_ep * n_ep <= (size_t)kFinalizeBins ? (size_t)n_ep * n_ep : 0;
+  return (32 * (size_t)E + (size_t)E + 1 + bins) * sizeof(int32_t);
+}
+
+__global__ void __launch_bounds__(kLayoutSmallThreads) layout_small_kernel(LayoutParams p) {
+  extern __shared__ int32_t sm[];
+  const int E = p.E, N = p.n_ep;
+  int32_t* cnt = sm;                 // [32][E]: per-warp counts, then prefixes over warps
+  int32_t* off = cnt + 32 * E;       // [E + 1]
+  int32_t* bins = off + E + 1;       // [N][N] when local
+  const bool local = (int64_t)N * N <= kFinalizeBins;
+  __shared__ int32_t scratch[33];
+  __shared__ long long red[33];
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+
+  for (int i = tid; i < 32 * E; i += kLayoutSmallThreads) cnt[i] = 0;
+  if (local)
+    for (int i = tid; i < N * N; i += kLayoutSmallThreads) bins[i] = 0;
+  for (int64_t r = tid; r < p.R; r += kLayoutSmallThreads) p.row_src[r] = -1;
+  if (!local) {
+    for (int64_t i = tid; i < (int64_t)N * N; i += kLayoutSmallThreads) p.n_ij[i] = 0;
+    for (int i = tid; i < 2 * N; i += kLayoutSmallThreads) p.rank_bytes[i] = 0;
+  }
+  __syncthreads();
+
+  // ---- stable rank of every assignment among its expert's, per warp
+  const int64_t base = (int64_t)warp * (32 * kLayoutSmallItems);
+  int e_of[kLayoutSmallItems];
+  int32_t local_rank[kLayoutSmallItems];
+#pragma unroll
+  for (int r = 0; r < kLayoutSmallItems; ++r) {
+    const int64_t a = base + r * 32 + lane;
+    int e = a < p.A ? p.ids[a] : -1;
+    if (a < p.A && (e < 0 || e >= E)) {
+      raise_error(kErrBadIndex);
+      e = -1;
+    }
+    const unsigned grp = __match_any_sync(0xffffffffu, e);
+    const unsigned lower = grp & ((1u << lane) - 1u);
+    const int32_t before = e >= 0 ? cnt[warp * E + e] : 0;
+    __syncwarp();
+    if (e >= 0 && lower == 0) cnt[warp * E + e] = before + __popc(grp);
+    __syncwarp();
+    e_of[r] = e;
+    local_rank[r] = before + __popc(lower);
+  }
+  __syncthreads();
+  const bool pad = p.pad && p.cap > 0;
+  long long kept_sum = 0, touched = 0;
+  for (int e = tid; e < E; e += kLayoutSmallThreads) {  // prefix over warps, histogram, kept
+    int32_t run = 0;
+    for (int w = 0; w < 32; ++w) {
+      const int32_t c = cnt[w * E + e];
+      cnt[w * E + e] = run;
+      run += c;
+    }
+    const int32_t k = p.cap > 0 ? min(run, p.cap) : run;
+    p.counts[e] = run;
+    p.kept[e] = k;
+    off[e] = pad ? p.cap : k;
+    touched += k > 0;
+    kept_sum += k;
+  }
+  kept_sum = block_reduce_ll<false>(kept_sum, red);
+  touched = block_reduce_ll<false>(touched, red);
+  const int32_t total = block_exclusive_scan(off, E, scratch);
+  if (tid == 0) off[E] = total;
+  __syncthreads();
+  for (int e = tid; e <= E; e += kLayoutSmallThreads) p.offsets[e] = off[e];
+
+  // ---- slots, row sources and the dispatch matrix
+  const int epr = E / N;
+  long long diag_rows = 0;  // kept rows with i == j, counted here when n_ij is not in shared memory
+#pragma unroll
+  for (int r = 0; r < kLayoutSmallItems; ++r) {
+    const int64_t a = base + r * 32 + lane;
+    const int e = e_of[r];
+    if (e < 0) continue;
+    const int32_t rank = cnt[warp * E + e] + local_rank[r];
+    bool keep = p.cap <= 0 || rank < p.cap;
+    int32_t s = keep ? off[e] + rank : -1;
+    if (s >= p.R) {  // cannot happen for a consistent layout; never used as an address
+      raise_error(kErrBadIndex);
+      keep = false;
+      s = -1;
+    }
+    p.slot[a] = s;
+    if (keep) {
+      const int64_t t = a / p.K;
+      p.row_src[s] = (int32_t)t;
+      const int i = (int)((t * N) / p.T), j = e / epr;
+      if (local) {
+        atomicAdd(&bins[i * N + j], 1);
+      } else {
+        atomicAdd(reinterpret_cast<unsigned long long*>(&p.n_ij[(int64_t)i * N + j]), 1ull);
+        atomicAdd(reinterpret_cast<unsigned long long*>(&p.rank_bytes[i]), 1ull);
+        atomicAdd(reinterpret_cast<unsigned long long*>(&p.rank_bytes[N + j]), 1ull);
+        diag_rows += i == j;
+      }
+    }
+  }
+  __syncthreads();
+
+  // ---- per-chip bytes and statistics: chip i's sent rows (row i of n_ij) and
+  // received rows (column i); one warp per chip, lanes over the other index
+  const long long rowbytes = (long long)p.h * p.ds;
+  long long rmax = 0, rsum = 0, ssum = 0, dsum = 0;
+  if (local) {
+    for (int i = tid; i < N * N; i += kLayoutSmallThreads) p.n_ij[i] = bins[i];
+    for (int i = warp; i < N; i += 32) {
+      long long sent = 0, recv = 0;
+      for (int j = lane; j < N; j += 32) {
+        sent += bins[i * N + j];
+        recv += bins[j * N + i];
+      }
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) {
+        sent += __shfl_xor_sync(0xffffffffu, sent, o);
+        recv += __shfl_xor_sync(0xffffffffu, recv, o);
+      }
+      if (lane == 0) {
+        p.rank_bytes[i] = sent * rowbytes;
+        p.rank_bytes[N + i] = recv * rowbytes;
+        rmax = recv > rmax ? recv : rmax;
+        rsum += recv;
+        ssum += sent;
+        dsum += bins[i * N + i];
+      }
+    }
+  } else {
+    for (int i = tid; i < N; i += kLayoutSmallThreads) {
+      const long long sent = p.rank_bytes[i], recv = p.rank_bytes[N + i];
+      p.rank_bytes[i] = sent * rowbytes;
+      p.rank_bytes[N + i] = recv * rowbytes;
+      rmax = recv > rmax ? recv : rmax;
+      rsum += recv;
+      ssum += sent;
+    }
+    dsum = diag_rows;
+  }
+  rmax = block_reduce_ll<true>(rmax, red);
+  rsum = block_reduce_ll<false>(rsum, red);
+  ssum = block_reduce_ll<false>(ssum, red);
+  dsum = block_reduce_ll<false>(dsum, red);
+  if (tid == 0) {
+    moe_layout_stats st;
+    st.kept_total = kept_sum;
+    st.dropped = p.A - kept_sum;
+    st.offdiag_rows = ssum - dsum;
+    st.experts_touched = (int32_t)touched;
+    st.balancedness = rmax == 0 ? 1.0f : (float)((double)rsum / ((double)N * (double)rmax));
+    *p.stats = st;
+  }
 }
 
 // Replica map of expert-parallel load balancing: the physical expert of every

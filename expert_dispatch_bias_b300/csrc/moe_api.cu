@@ -300,6 +300,13 @@ moe_status launch_layout(const moe_config& c, const int32_t* ids, int32_t* count
   p.rank_bytes = rank_bytes;
   p.stats = stats;
   p.ws = layout_scratch_at(ws, p.A, nphys(c));
+  if (p.A <= kLayoutSmallMax) {  // one block, one launch
+    const size_t smem = layout_small_smem(p.E, p.n_ep);
+    CUDA_TRY(allow_smem(layout_small_kernel, smem));
+    layout_small_kernel<<<1, kLayoutSmallThreads, smem, st>>>(p);
+    CUDA_TRY(cudaGetLastError());
+    return MOE_OK;
+  }
   const size_t smem1 = (size_t)(kLayoutWarps + 2) * nphys(c) * sizeof(int32_t);
   CUDA_TRY(allow_smem(layout_rank_kernel, smem1));
   layout_rank_kernel<<<p.num_tiles, kLayoutThreads, smem1, st>>>(p);

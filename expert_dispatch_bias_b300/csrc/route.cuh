@@ -19,6 +19,7 @@ namespace moe {
 constexpr int kRouteWarps = 8;      // tokens per block
 constexpr int kMaxGroupTopn = 8;
 constexpr int kRouteMaxK = 16;
+constexpr int kRefineMax = 64;      // experts whose keys one refinement step evaluates exactly
 
 struct RouteParams {
   const float* logits;  // [T, E]
@@ -49,7 +50,19 @@ struct RouteSel {
   int my_id;        // lane k < K: the k-th chosen expert
   float min_gap;    // smallest gap between adjacent keys of the K+1 best allowed
   float group_gap;  // gap between the last kept and the first dropped group score
+  float kth1;       // key of the (K+1)-th best allowed expert (-inf: fewer allowed)
+  uint32_t gmask;   // bit g: group g allowed (all ones without groups)
+  int gsize;        // experts per group (E without groups)
 };
+
+// Groups that are power-of-two runs of whole lanes (lane l holds experts
+// l*PER..) with a top-1 or top-2 group score: the shuffle form of the limit.
+template <int PER>
+__device__ __forceinline__ bool lane_groups(const RouteParams& p) {
+  if (p.n_groups <= 0 || p.group_topn > 2) return false;
+  const int gs = p.E / p.n_groups;
+  return gs % PER == 0 && ((gs / PER) & (gs / PER - 1)) == 0;
+}
 
 // Group limit and top-K on the keys held by this warp (lane l: experts
 // l*PER..), with the gaps that decide whether an approximation of the keys
@@ -65,8 +78,7 @@ __device__ __forceinline__ RouteSel route_select(const float* key, const RoutePa
   // ---- group limit: bit g of gmask set iff group g is allowed
   uint32_t gmask = full;
   int gsize = p.E;
-  if (p.n_groups > 0 && p.group_topn <= 2 && (p.E / p.n_groups) % PER == 0 &&
-      ((p.E / p.n_groups / PER) & (p.E / p.n_groups / PER - 1)) == 0) {
+  if (lane_groups<PER>(p)) {
     // Each group is a power-of-two run of whole lanes: the two largest keys of
     // every lane, merged across the group's lanes by butterfly shuffles.  The
     // group score is the same float32 sum as the general path forms.
@@ -155,6 +167,9 @@ __device__ __forceinline__ RouteSel route_select(const float* key, const RoutePa
   }
   r.my_id = 0;
   r.min_gap = INFINITY;
+  r.kth1 = -INFINITY;
+  r.gmask = gmask;
+  r.gsize = gsize;
   float prev = 0.0f;
   for (int k = 0; k <= p.K; ++k) {
     float bk = -INFINITY;
@@ -179,7 +194,10 @@ __device__ __forceinline__ RouteSel route_select(const float* key, const RoutePa
     if (bi == NONE) break;  // fewer than K+1 experts allowed
     if (k > 0) r.min_gap = fminf(r.min_gap, prev - bk);
     prev = bk;
-    if (k == p.K) break;
+    if (k == p.K) {
+      r.kth1 = bk;
+      break;
+    }
 #pragma unroll
     for (int i = 0; i < PER; ++i)
       if (lane * PER + i == bi) avail[i] = false;
@@ -188,12 +206,56 @@ __device__ __forceinline__ RouteSel route_select(const float* key, const RoutePa
   return r;
 }
 
+// Replaces key[i] by the exact sigmoid key fl32(sigmoid(x) + b), x and the
+// sigmoid in float64, for every expert i of this lane with need[i] and not yet
+// done[i]: the warp compacts those experts into `eids` and evaluates one per
+// lane.  Returns false, changing nothing, when more than kRefineMax would be.
+template <int PER>
+__device__ __forceinline__ bool refine_keys(float* key, bool* done, const bool* need, const float* L,
+                                            const RouteParams& p, int32_t* eids, float* vals) {
+  const unsigned full = 0xffffffffu;
+  const int lane = threadIdx.x & 31;
+  const unsigned below = (1u << lane) - 1u;
+  int n = 0;
+#pragma unroll
+  for (int i = 0; i < PER; ++i) n += __popc(__ballot_sync(full, need[i] && !done[i]));
+  if (n > kRefineMax) return false;
+  int base = 0;
+#pragma unroll
+  for (int i = 0; i < PER; ++i) {
+    const bool f = need[i] && !done[i];
+    const unsigned m = __ballot_sync(full, f);
+    if (f) eids[base + __popc(m & below)] = lane * PER + i;
+    base += __popc(m);
+  }
+  __syncwarp();
+  for (int j = lane; j < n; j += 32) {
+    const int e = eids[j];
+    const double b = p.bias != nullptr ? (double)p.bias[e] : 0.0;
+    vals[j] = (float)(1.0 / (1.0 + exp(-(double)L[e])) + b);
+  }
+  __syncwarp();
+  base = 0;
+#pragma unroll
+  for (int i = 0; i < PER; ++i) {
+    const bool f = need[i] && !done[i];
+    const unsigned m = __ballot_sync(full, f);
+    if (f) {
+      key[i] = vals[base + __popc(m & below)];
+      done[i] = true;
+    }
+    base += __popc(m);
+  }
+  __syncwarp();
+  return true;
+}
+
 // Selection for token t by the calling warp: writes ids[t, :], the chosen
 // logits to xs[0..K), and the softmax max and float64 denominator (when the
 // weights need the full one) to *zs, *ms.
 template <int PER>
 __device__ __forceinline__ void route_token(const RouteParams& p, int t, float* kk, float* xs, double* zs,
-                                            float* ms) {
+                                            float* ms, int32_t* eids, float* vals) {
   const int lane = threadIdx.x & 31;
   const unsigned full = 0xffffffffu;
   const float* L = p.logits + (size_t)t * p.E;
@@ -249,14 +311,62 @@ __device__ __forceinline__ void route_token(const RouteParams& p, int t, float* 
   RouteSel sel = route_select<PER>(key, p, kk);
   if (!exact) {
     const float group_tol = 4.0f * (float)p.group_topn * kKeyErr;  // twice 2n * 2^-20
-    if (!(sel.min_gap > 2.0f * kKeyErr && (p.n_groups == 0 || sel.group_gap > group_tol))) {
+    const bool group_open = p.n_groups > 0 && !(sel.group_gap > group_tol);
+    if (!(sel.min_gap > 2.0f * kKeyErr) || group_open) {
+      // Refinement: keys within 3 kKeyErr of a threshold are made exact.  An
+      // approximate key a (|a - exact| <= kKeyErr) below the n-th largest key
+      // tau of its group by more than 2 kKeyErr has an exact key below the n
+      // keys at or above tau, so the group score (sum of the n largest) is
+      // exact once the keys at or above tau - 2 kKeyErr are; likewise the top
+      // K+1 of the allowed experts lie at or above the (K+1)-th key minus
+      // 2 kKeyErr.  Comparisons between an exact key and an approximate one
+      // more than 2 kKeyErr apart are decided as between the exact keys, so
+      // the selection on the refined keys is the selection on the exact keys.
+      bool done[PER], need[PER];
 #pragma unroll
-      for (int i = 0; i < PER; ++i) {
-        const int e = lane * PER + i;
-        const double b = (p.bias != nullptr && e < p.E) ? (double)p.bias[e] : 0.0;
-        key[i] = e < p.E ? (float)(1.0 / (1.0 + exp(-(double)lg[i])) + b) : -INFINITY;
+      for (int i = 0; i < PER; ++i) done[i] = false;
+      bool ok = p.n_groups == 0 || lane_groups<PER>(p);
+      if (ok && group_open) {
+        const int lanes_per_group = p.E / p.n_groups / PER;
+        float t1 = -INFINITY, t2 = -INFINITY;  // this group's two largest keys
+#pragma unroll
+        for (int i = 0; i < PER; ++i) {
+          const float v = key[i];
+          if (v > t2) {
+            t2 = v > t1 ? t1 : v;
+            t1 = fmaxf(t1, v);
+          }
+        }
+        for (int o = 1; o < lanes_per_group; o <<= 1) {
+          const float b1 = __shfl_xor_sync(full, t1, o), b2 = __shfl_xor_sync(full, t2, o);
+          t2 = fmaxf(fminf(t1, b1), fmaxf(t2, b2));
+          t1 = fmaxf(t1, b1);
+        }
+        const float thr = (p.group_topn == 1 ? t1 : t2) - 3.0f * kKeyErr;
+#pragma unroll
+        for (int i = 0; i < PER; ++i) need[i] = lane * PER + i < p.E && key[i] >= thr;
+        ok = refine_keys<PER>(key, done, need, L, p, eids, vals);
+        if (ok) sel = route_select<PER>(key, p, kk);  // exact group limit
       }
-      sel = route_select<PER>(key, p, kk);
+      if (ok) {
+        const float thr = sel.kth1 - 3.0f * kKeyErr;
+#pragma unroll
+        for (int i = 0; i < PER; ++i) {
+          const int e = lane * PER + i;
+          need[i] = e < p.E && ((sel.gmask >> (e / sel.gsize)) & 1u) && key[i] >= thr;
+        }
+        ok = refine_keys<PER>(key, done, need, L, p, eids, vals);
+        if (ok) sel = route_select<PER>(key, p, kk);
+      }
+      if (!ok) {  // too many keys near a threshold: every key exactly
+#pragma unroll
+        for (int i = 0; i < PER; ++i) {
+          const int e = lane * PER + i;
+          const double b = (p.bias != nullptr && e < p.E) ? (double)p.bias[e] : 0.0;
+          key[i] = e < p.E ? (float)(1.0 / (1.0 + exp(-(double)lg[i])) + b) : -INFINITY;
+        }
+        sel = route_select<PER>(key, p, kk);
+      }
     }
   }
 
@@ -281,8 +391,10 @@ __device__ __forceinline__ void route_token(const RouteParams& p, int t, float* 
 
 // PER = experts held by each lane (contiguous: lane l holds l*PER .. l*PER+PER-1).
 template <int PER>
-__global__ void __launch_bounds__(kRouteWarps * 32) route_kernel(RouteParams p) {
+__global__ void __launch_bounds__(kRouteWarps * 32, PER <= 8 ? 4 : 1) route_kernel(RouteParams p) {
   extern __shared__ float s_keys[];  // [kRouteWarps][E], used with a group limit
+  __shared__ int32_t s_eid[kRouteWarps][kRefineMax];  // experts being refined
+  __shared__ float s_eval[kRouteWarps][kRefineMax];   // their exact keys
   __shared__ float s_x[kRouteWarps * kRouteMaxK];    // logits of the chosen experts
   __shared__ double s_s[kRouteWarps * kRouteMaxK];   // their float64 scores
   __shared__ double s_z[kRouteWarps];                // softmax denominators
@@ -290,7 +402,9 @@ __global__ void __launch_bounds__(kRouteWarps * 32) route_kernel(RouteParams p) 
   const int warp = threadIdx.x >> 5;
   const int t0 = blockIdx.x * kRouteWarps;
   const int nt = min(kRouteWarps, p.T - t0);  // tokens of this block
-  if (warp < nt) route_token<PER>(p, t0 + warp, s_keys + warp * p.E, s_x + warp * p.K, &s_z[warp], &s_m[warp]);
+  if (warp < nt)
+    route_token<PER>(p, t0 + warp, s_keys + warp * p.E, s_x + warp * p.K, &s_z[warp], &s_m[warp], s_eid[warp],
+                     s_eval[warp]);
   __syncthreads();
 
   // ---- weights from the unbiased float64 scores of the chosen experts, one

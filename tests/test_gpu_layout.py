@@ -75,6 +75,16 @@ EDGE = {
     "single_expert": (_wl(333, 1, 1, ep=1), "zeros"),
     "T_below_ep": (_wl(32, 256, 8, ep=64), "uniform"),
     "capacity_one_pad": (_wl(200, 8, 2, cap=1, pad=1, ep=4), "uniform"),
+    # up to 8192 assignments take the one-block layout, more the two-pass one:
+    # both sides of the boundary, and the drop/pad/skew cases above on the
+    # two-pass layout
+    "small_limit": (_wl(1024, 256, 8, ep=64), "uniform"),
+    "small_limit_plus_one": (_wl(8193, 64, 1, cap=200, ep=8), "uniform"),
+    "ragged_capacity_two_pass": (_wl(10000, 60, 3, cap=450, ep=6), "uniform"),
+    "all_to_expert0_two_pass": (_wl(20000, 16, 1, cap=1000, ep=4), "zeros"),
+    "pad_two_pass": (_wl(2777, 32, 4, cap=300, pad=1, ep=8), "uniform"),
+    "T_below_ep_wide": (_wl(40, 1024, 16, ep=64), "uniform"),
+    "small_ep128": (_wl(500, 256, 8, ep=128), "uniform"),  # N_EP^2 above the shared n_ij bins
 }
 
 
@@ -113,7 +123,7 @@ def test_lookback_wait_times_out_with_status():
     """A tile whose predecessor never publishes: the bounded look-back gives up
     after about a second, sets the sticky error and the kernel returns; the
     context stays usable and the next call is correct."""
-    w = _wl(768, 32, 8, ep=4)      # 6144 assignments: three tiles
+    w = _wl(1280, 32, 8, ep=4)     # 10240 assignments: the two-pass layout, five tiles
     ids = synth.uniform_topk_ids(2, synth.TID_TEST, w.T, w.E, w.K)
     cfg = moe.config_from(w)
     ws = moe.alloc_workspace(cfg, moe.MOE_OP_LAYOUT)
