@@ -318,6 +318,10 @@ moe_status launch_layout(const moe_config& c, const int32_t* ids, int32_t* count
   return MOE_OK;
 }
 
+// Rows up to this size are permuted by warps (permute_warp_kernel), wider ones
+// through shared memory by the bulk-copy engine (permute_bulk_kernel).
+constexpr uint32_t kPermWarpMaxRowBytes = 4096;
+
 moe_status launch_permute(const moe_config& c, const void* x, const int32_t* slot, const int32_t* row_src,
                           void* xp, cudaStream_t st) {
   const uint32_t row_bytes = (uint32_t)c.h * ds_of(c);
@@ -332,6 +336,21 @@ moe_status launch_permute(const moe_config& c, const void* x, const int32_t* slo
     }
   }
   if (c.T == 0) return MOE_OK;
+  if (row_bytes <= kPermWarpMaxRowBytes) {
+    auto kern = c.K <= 1 ? permute_warp_kernel<1> : c.K <= 2 ? permute_warp_kernel<2>
+              : c.K <= 8 ? permute_warp_kernel<8> : permute_warp_kernel<16>;
+    const int row_vecs = (int)(row_bytes / 16);
+    const int64_t units = c.T * ((row_vecs + kPermChunk - 1) / kPermChunk);
+    int per_sm = 0;
+    CUDA_TRY(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, 256, 0));
+    if (per_sm < 1) per_sm = 1;
+    int64_t blocks = (int64_t)device_info().sms * per_sm;
+    if (blocks > (units + 7) / 8) blocks = (units + 7) / 8;
+    kern<<<(unsigned)blocks, 256, 0, st>>>(static_cast<const uint4*>(x), slot, c.T, c.K, row_vecs,
+                                           static_cast<uint4*>(xp));
+    CUDA_TRY(cudaGetLastError());
+    return MOE_OK;
+  }
   PermuteParams p{};
   p.x = static_cast<const uint8_t*>(x);
   p.slot = slot;

@@ -7,6 +7,11 @@
 // (cp.async.bulk shared->global).  HBM traffic is the algorithmic minimum: one
 // read of every token that has a kept slot, one write per kept assignment.
 //
+// Narrow rows (a few KB) pay the bulk-copy engine's per-copy cost more than
+// its bandwidth, so they are permuted by warps instead (permute_warp_kernel):
+// one warp per (token, chunk of kCombineChunk 16-byte vectors), each vector
+// read once and written to every kept slot.
+//
 // Combine is a gather: one warp per (token, column chunk of kCombineChunk
 // 16-byte vectors), 16-byte vector loads of the K expert-output rows, float32
 // accumulation in k order, one vector store.  Chunks rather than whole tokens
@@ -84,6 +89,41 @@ __global__ void __launch_bounds__(32) permute_bulk_kernel(PermuteParams p) {
       if (tok[b] >= 0) mbar_wait(&bar[b], (phase >> b) & 1u);
   }
   bulk_wait_all<0>();
+}
+
+// Permutation by warps over (token, column chunk) units on a persistent grid:
+// row_vecs 16-byte vectors per row; a unit's vectors are read once and stored
+// to each of the token's kept slots.
+constexpr int kPermChunk = 128;  // 16-byte vectors per work unit (4 per lane)
+
+template <int KMAX>
+__global__ void __launch_bounds__(256) permute_warp_kernel(const uint4* x, const int32_t* slot, int64_t T, int K,
+                                                           int row_vecs, uint4* xp) {
+  const int lane = threadIdx.x & 31;
+  const int64_t warps = (int64_t)gridDim.x * (blockDim.x >> 5);
+  const int chunks = (row_vecs + kPermChunk - 1) / kPermChunk;
+  const int64_t units = T * chunks;
+  for (int64_t u = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); u < units; u += warps) {
+    const int64_t t = u / chunks;
+    const int c0 = (int)(u - t * chunks) * kPermChunk;
+    const int c1 = min(row_vecs, c0 + kPermChunk);
+    const int32_t s_l = lane < K ? slot[t * K + lane] : -1;
+    int32_t s[KMAX];
+    bool any = false;
+#pragma unroll
+    for (int k = 0; k < KMAX; ++k) {
+      s[k] = __shfl_sync(0xffffffffu, s_l, k);
+      any |= k < K && s[k] >= 0;
+    }
+    if (!any) continue;  // uniform: every assignment of the token was dropped
+    const uint4* src = x + t * row_vecs;
+    for (int c = c0 + lane; c < c1; c += 32) {
+      const uint4 v = __ldg(src + c);
+#pragma unroll
+      for (int k = 0; k < KMAX; ++k)
+        if (k < K && s[k] >= 0) xp[(int64_t)s[k] * row_vecs + c] = v;
+    }
+  }
 }
 
 // Zero the pad rows (row_src == -1) of a padded permuted buffer.
