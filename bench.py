@@ -247,10 +247,12 @@ def run_ours(args, rank, world, local_rank):
     if world > 1:
         dist.barrier()
     torch.cuda.synchronize()
+    launches0 = moe.moe_launch_count()  # the library counts every kernel it launches
     with ClockSampler(local_rank) as clk:
         for i in range(args.steps):
             step(events[i])
         torch.cuda.synchronize()
+    timed_launches = moe.moe_launch_count() - launches0
     if world > 1:
         dist.barrier()
     st = moe.moe_check()
@@ -344,8 +346,14 @@ def run_ours(args, rank, world, local_rank):
     tc_peak = float(peaks["bf16_tflops_sustained"]) * (2.0 if fp8 else 1.0)
     ffn_s = per_stage["ffn"] / 1e3
     ffn_gbs = ffn_bytes / ffn_s / 1e9
-    launches_per_step = (8 + (1 if (w.pad and w.capacity > 0) else 0) + (2 if shared else 0) + (1 if eplb else 0)
-                         - (1 if gather else 0) + (1 if fp8 else 0))
+    # the FFN is compute-bound when its arithmetic intensity is above the ridge of
+    # the measured peaks (Mixtral: ~1000 rows per expert), else bound by HBM
+    tensor_bound = ffn_flops / ffn_bytes > tc_peak * 1e12 / (hbm * 1e9)
+    # FFN_TRAFFIC_RATIO was captured on the bf16 weights-as-M kernel (experts
+    # expected to see at most 160 rows); other variants report no traffic
+    expected_rows = (min(w.capacity, T) if w.capacity > 0 else -(-T * K // (E + w.n_redundant)))
+    traffic_known = not fp8 and w.dtype == "bf16" and expected_rows <= 160
+    ffn_tflops = ffn_flops / ffn_s / 1e12
     ms = total_ms / args.steps
     out = {
         "metric": METRIC,
@@ -363,15 +371,22 @@ def run_ours(args, rank, world, local_rank):
         "config": workload_config(w),
         "e2e": {"value": job_throughput(T, world, args.steps, e2e_ms), "unit": "tokens/s",
                 "h2d_bytes_per_step": T * w.h * ds, "d2h_bytes_per_step": T * w.h * ds},
-        "gpu_launches": launches_per_step * args.steps,
-        "roofline": {"kernel": "grouped SwiGLU FFN (gate/up + down tcgen05 GEMMs)", "bound": "hbm",
-                     "achieved": ffn_gbs, "peak": hbm, "unit": "GB/s", "frac": ffn_gbs / hbm,
-                     "peak_source": peak_kind, "algorithmic_bytes": ffn_bytes,
-                     "traffic": FFN_TRAFFIC_RATIO * ffn_bytes,
-                     "traffic_source": "ncu DRAM bytes / algorithmic bytes on deepseek_v3_e32_T512, scaled to this "
-                                       "launch's algorithmic bytes",
-                     "tensor_tflops": ffn_flops / ffn_s / 1e12,
-                     "tensor_frac_of_sustained": ffn_flops / ffn_s / 1e12 / tc_peak},
+        "gpu_launches": timed_launches,
+        "roofline": {"kernel": "grouped SwiGLU FFN (gate/up + down tcgen05 GEMMs)",
+                     "bound": "tensor" if tensor_bound else "hbm",
+                     "achieved": ffn_tflops if tensor_bound else ffn_gbs,
+                     "peak": tc_peak if tensor_bound else hbm,
+                     "unit": "TFLOP/s" if tensor_bound else "GB/s",
+                     "frac": ffn_tflops / tc_peak if tensor_bound else ffn_gbs / hbm,
+                     "peak_source": peak_kind + (" (bf16 sustained" + (" x 2 for FP8" if fp8 else "") + ")"
+                                                 if tensor_bound else " (HBM copy)"),
+                     "achieved_gbs": ffn_gbs, "algorithmic_bytes": ffn_bytes, "algorithmic_flops": ffn_flops,
+                     "traffic": FFN_TRAFFIC_RATIO * ffn_bytes if traffic_known else None,
+                     "traffic_source": ("ncu DRAM bytes / algorithmic bytes on deepseek_v3_e32_T512, scaled to this "
+                                        "launch's algorithmic bytes") if traffic_known else
+                                       "not captured for this FFN variant since its last change",
+                     "tensor_tflops": ffn_tflops,
+                     "tensor_frac_of_sustained": ffn_tflops / tc_peak},
         "stages_ms": per_stage,
         "permute_gbs": permute_bytes / (per_stage["permute"] / 1e3) / 1e9 if "permute" in per_stage else None,
         "permute_fused_into_ffn": gather,

@@ -36,7 +36,7 @@ EXPORTS = (
     "moe_shared_ffn", "moe_combine_add", "moe_block_forward", "moe_block_forward_host",
     "moe_eplb_plan", "moe_eplb_map", "moe_grouped_ffn_mapped", "moe_layer_forward_eplb",
     "moe_quantize_fp8", "moe_permute_fp8", "moe_grouped_ffn_fp8", "moe_layer_forward_fp8",
-    "moe_grouped_ffn_gather",
+    "moe_grouped_ffn_gather", "moe_launch_count",
 )
 
 
@@ -87,6 +87,7 @@ def _load() -> ctypes.CDLL:
         "moe_layer_forward": (c_int32, [cfgp] + [c_void_p] * 9 + [c_size_t, c_void_p]),
         "moe_layer_forward_host": (c_int32, [cfgp] + [c_void_p] * 8 + [c_size_t, c_void_p]),
         "moe_check": (c_int32, [c_void_p]),
+        "moe_launch_count": (ctypes.c_uint64, []),
         "moe_shared_ffn": (c_int32, [cfgp] + [c_void_p] * 5 + [c_size_t, c_void_p]),
         "moe_combine_add": (c_int32, [cfgp] + [c_void_p] * 6),
         "moe_block_forward": (c_int32, [cfgp] + [c_void_p] * 11 + [c_size_t, c_void_p]),
@@ -332,6 +333,11 @@ def moe_layer_forward_fp8(cfg, x, w_r, logit_offset, sel_bias, w13q, s13, w2q, s
 def moe_check(stream=None) -> int:
     """Synchronises the stream; returns the status (does not raise)."""
     return lib.moe_check(_stream(stream))
+
+
+def moe_launch_count() -> int:
+    """Kernels the library has launched in this process so far."""
+    return int(lib.moe_launch_count())
 
 
 def layer_out(**tensors) -> MoeLayerOut:

@@ -10,6 +10,7 @@
 #include <string.h>
 
 #include <algorithm>
+#include <atomic>
 #include <vector>
 
 #include <cudaTypedefs.h>
@@ -37,6 +38,15 @@ namespace {
     const moe_status st_ = (expr);       \
     if (st_ != MOE_OK) return st_;       \
   } while (0)
+
+// Kernels this library has launched in the process (moe_launch_count).
+std::atomic<uint64_t> g_launches{0};
+
+// Called right after every kernel launch: counts it and returns the launch error.
+inline cudaError_t launched() {
+  g_launches.fetch_add(1, std::memory_order_relaxed);
+  return cudaGetLastError();
+}
 
 #define CUDA_TRY(expr)                               \
   do {                                               \
@@ -233,7 +243,7 @@ moe_status launch_logits_simt(const moe_config& c, const void* x, const void* w_
     simt_gemm_kernel<float, kSimtLogits><<<grid, kSimtThreads, 0, st>>>(p);
   else
     simt_gemm_kernel<__nv_bfloat16, kSimtLogits><<<grid, kSimtThreads, 0, st>>>(p);
-  CUDA_TRY(cudaGetLastError());
+  CUDA_TRY(launched());
   return MOE_OK;
 }
 
@@ -242,7 +252,7 @@ cudaError_t launch_route_per(const RouteParams& p, cudaStream_t st) {
   const int blocks = (p.T + kRouteWarps - 1) / kRouteWarps;
   const size_t smem = p.n_groups > 0 ? (size_t)kRouteWarps * p.E * sizeof(float) : 0;
   route_kernel<PER><<<blocks, kRouteWarps * 32, smem, st>>>(p);
-  return cudaGetLastError();
+  return launched();
 }
 
 moe_status launch_route(const moe_config& c, const float* logits, const float* bias, int32_t* ids, float* w,
@@ -304,17 +314,17 @@ moe_status launch_layout(const moe_config& c, const int32_t* ids, int32_t* count
     const size_t smem = layout_small_smem(p.E, p.n_ep);
     CUDA_TRY(allow_smem(layout_small_kernel, smem));
     layout_small_kernel<<<1, kLayoutSmallThreads, smem, st>>>(p);
-    CUDA_TRY(cudaGetLastError());
+    CUDA_TRY(launched());
     return MOE_OK;
   }
   const size_t smem1 = (size_t)(kLayoutWarps + 2) * nphys(c) * sizeof(int32_t);
   CUDA_TRY(allow_smem(layout_rank_kernel, smem1));
   layout_rank_kernel<<<p.num_tiles, kLayoutThreads, smem1, st>>>(p);
-  CUDA_TRY(cudaGetLastError());
+  CUDA_TRY(launched());
   const int64_t per_block = kFinalizeThreads * kFinalizeItems;
   const int blocks2 = (int)((p.A + per_block - 1) / per_block) > 0 ? (int)((p.A + per_block - 1) / per_block) : 1;
   layout_finalize_kernel<<<blocks2, kFinalizeThreads, (nphys(c) + 1) * sizeof(int32_t), st>>>(p);
-  CUDA_TRY(cudaGetLastError());
+  CUDA_TRY(launched());
   return MOE_OK;
 }
 
@@ -332,7 +342,7 @@ moe_status launch_permute(const moe_config& c, const void* x, const int32_t* slo
     const int blocks = (int)((n + 255) / 256 < 148 * 8 ? (n + 255) / 256 : 148 * 8);
     if (n > 0) {
       zero_pad_rows_kernel<<<blocks, 256, 0, st>>>(row_src, R, vecs, static_cast<uint4*>(xp));
-      CUDA_TRY(cudaGetLastError());
+      CUDA_TRY(launched());
     }
   }
   if (c.T == 0) return MOE_OK;
@@ -348,7 +358,7 @@ moe_status launch_permute(const moe_config& c, const void* x, const int32_t* slo
     if (blocks > (units + 7) / 8) blocks = (units + 7) / 8;
     kern<<<(unsigned)blocks, 256, 0, st>>>(static_cast<const uint4*>(x), slot, c.T, c.K, row_vecs,
                                            static_cast<uint4*>(xp));
-    CUDA_TRY(cudaGetLastError());
+    CUDA_TRY(launched());
     return MOE_OK;
   }
   PermuteParams p{};
@@ -368,7 +378,7 @@ moe_status launch_permute(const moe_config& c, const void* x, const int32_t* slo
   int64_t blocks = (int64_t)device_info().sms * per_sm;
   if (blocks > c.T) blocks = c.T;
   permute_bulk_kernel<<<(unsigned)blocks, 32, smem, st>>>(p);
-  CUDA_TRY(cudaGetLastError());
+  CUDA_TRY(launched());
   return MOE_OK;
 }
 
@@ -399,7 +409,7 @@ moe_status launch_combine(const moe_config& c, const void* yp, const int32_t* sl
   int64_t blocks = (int64_t)device_info().sms * per_sm;
   if (blocks > (units + 7) / 8) blocks = (units + 7) / 8;
   kern<<<(unsigned)blocks, 256, 0, st>>>(p);
-  CUDA_TRY(cudaGetLastError());
+  CUDA_TRY(launched());
   return MOE_OK;
 }
 
@@ -426,7 +436,7 @@ cudaError_t launch_ffn_simt(const moe_config& c, const void* xp, const int32_t* 
   p.N = c.I;
   p.K = c.h;
   simt_gemm_kernel<T, kSimtSwiglu><<<dim3((c.I + kSimtBN - 1) / kSimtBN, mblocks), kSimtThreads, 0, st>>>(p);
-  cudaError_t e = cudaGetLastError();
+  cudaError_t e = launched();
   if (e != cudaSuccess) return e;
   SimtParams q = p;
   q.A = inter;
@@ -440,7 +450,7 @@ cudaError_t launch_ffn_simt(const moe_config& c, const void* xp, const int32_t* 
   q.N = c.h;
   q.K = c.I;
   simt_gemm_kernel<T, kSimtPlain><<<dim3((c.h + kSimtBN - 1) / kSimtBN, mblocks), kSimtThreads, 0, st>>>(q);
-  return cudaGetLastError();
+  return launched();
 }
 
 // cuTensorMapEncodeTiled through the runtime's driver entry point (no -lcuda).
@@ -522,9 +532,9 @@ moe_status launch_ffn_tokens_m(const moe_config& c, const void* xp, const int32_
   CUDA_TRY(allow_smem(k1, S::kDynSmem));
   CUDA_TRY(allow_smem(k2, S::kDynSmem));
   k1<<<grid, kTcThreads, S::kDynSmem, st>>>(a1, b1, p1);
-  CUDA_TRY(cudaGetLastError());
+  CUDA_TRY(launched());
   k2<<<grid, kTcThreads, S::kDynSmem, st>>>(a2, b2, p2);
-  CUDA_TRY(cudaGetLastError());
+  CUDA_TRY(launched());
   return MOE_OK;
 }
 
@@ -585,9 +595,9 @@ moe_status launch_ffn_grouped(const moe_config& c, const void* xp, const int32_t
   CUDA_TRY(allow_smem(k1, S::kDynSmem));
   CUDA_TRY(allow_smem(k2, S::kDynSmem));
   k1<<<grid, kFgThreads, S::kDynSmem, st>>>(w1m, x1, p1);
-  CUDA_TRY(cudaGetLastError());
+  CUDA_TRY(launched());
   k2<<<grid, kFgThreads, S::kDynSmem, st>>>(w2m, x2, p2);
-  CUDA_TRY(cudaGetLastError());
+  CUDA_TRY(launched());
   return MOE_OK;
 }
 
@@ -640,14 +650,14 @@ moe_status launch_logits_tc_bn(const moe_config& c, const void* x, const void* w
   auto k = tc_gemm_kernel<kTcLogits, BN, STAGES>;
   CUDA_TRY(allow_smem(k, S::kDynSmem));
   k<<<grid, kTcThreads, S::kDynSmem, st>>>(a, b, p);
-  CUDA_TRY(cudaGetLastError());
+  CUDA_TRY(launched());
   if (k_split > 1) {
     const int64_t n = (int64_t)c.T * c.E;
     const int64_t lanes = (c.E % 4 == 0) ? n / 4 : n;
     int64_t blocks = (lanes + 255) / 256;
     if (blocks > (int64_t)sms * 8) blocks = (int64_t)sms * 8;
     logits_reduce_kernel<<<(unsigned)blocks, 256, 0, st>>>(p.partial, k_split, n, c.E, off, logits);
-    CUDA_TRY(cudaGetLastError());
+    CUDA_TRY(launched());
   }
   return MOE_OK;
 }
@@ -759,13 +769,13 @@ moe_status launch_ffn_fp8(const moe_config& c, const uint8_t* xq, const float* s
   CUDA_TRY(allow_smem(k1, S::kDynSmem));
   CUDA_TRY(allow_smem(k2, S::kDynSmem));
   k1<<<grid, kFgThreads, S::kDynSmem, st>>>(w1m, x1, p1);
-  CUDA_TRY(cudaGetLastError());
+  CUDA_TRY(launched());
   int64_t qb = (R + 7) / 8;
   if (qb > (int64_t)grid * 16) qb = (int64_t)grid * 16;
   quant_rows_kernel<__nv_bfloat16><<<(unsigned)qb, 256, 0, st>>>(inter, R, c.I, interq, sinter);
-  CUDA_TRY(cudaGetLastError());
+  CUDA_TRY(launched());
   k2<<<grid, kFgThreads, S::kDynSmem, st>>>(w2m, x2, p2);
-  CUDA_TRY(cudaGetLastError());
+  CUDA_TRY(launched());
   return MOE_OK;
 }
 
@@ -776,7 +786,7 @@ moe_status launch_permute_fp8(const moe_config& c, const void* x, const int32_t*
   if (blocks > (int64_t)device_info().sms * 16) blocks = (int64_t)device_info().sms * 16;
   quant_permute_kernel<__nv_bfloat16><<<(unsigned)blocks, 256, 0, st>>>(static_cast<const __nv_bfloat16*>(x), slot,
                                                                        c.T, c.K, c.h, xq, sx);
-  CUDA_TRY(cudaGetLastError());
+  CUDA_TRY(launched());
   return MOE_OK;
 }
 
@@ -829,7 +839,7 @@ moe_status launch_shared_ffn(const moe_config& c, const void* x, const void* w13
     p.K = c.h;
     const unsigned mblocks = (unsigned)((c.T + kSimtBM - 1) / kSimtBM);
     simt_gemm_kernel<float, kSimtSwiglu><<<dim3((Is + kSimtBN - 1) / kSimtBN, mblocks), kSimtThreads, 0, st>>>(p);
-    CUDA_TRY(cudaGetLastError());
+    CUDA_TRY(launched());
     SimtParams q = p;
     q.A = inter;
     q.lda = Is;
@@ -842,7 +852,7 @@ moe_status launch_shared_ffn(const moe_config& c, const void* x, const void* w13
     q.N = c.h;
     q.K = Is;
     simt_gemm_kernel<float, kSimtPlain><<<dim3((c.h + kSimtBN - 1) / kSimtBN, mblocks), kSimtThreads, 0, st>>>(q);
-    CUDA_TRY(cudaGetLastError());
+    CUDA_TRY(launched());
     return MOE_OK;
   }
   using S = TcShape<kFfnBN, kFfnStages>;
@@ -879,9 +889,9 @@ moe_status launch_shared_ffn(const moe_config& c, const void* x, const void* w13
   CUDA_TRY(allow_smem(k1, S::kDynSmem));
   CUDA_TRY(allow_smem(k2, S::kDynSmem));
   k1<<<g1, kTcThreads, S::kDynSmem, st>>>(a1, b1, p1);
-  CUDA_TRY(cudaGetLastError());
+  CUDA_TRY(launched());
   k2<<<g2, kTcThreads, S::kDynSmem, st>>>(a2, b2, p2);
-  CUDA_TRY(cudaGetLastError());
+  CUDA_TRY(launched());
   return MOE_OK;
 }
 
@@ -908,7 +918,7 @@ moe_status launch_eplb_map(const moe_config& c, const int32_t* ids, const EplbDe
   if (blocks > (int64_t)device_info().sms * 8) blocks = (int64_t)device_info().sms * 8;
   eplb_map_kernel<<<(unsigned)blocks, 256, 0, st>>>(ids, A, c.K, c.E, nphys(c), plan.rep_offsets, plan.rep_phys,
                                                       phys);
-  CUDA_TRY(cudaGetLastError());
+  CUDA_TRY(launched());
   return MOE_OK;
 }
 
@@ -967,6 +977,8 @@ moe_status check_layer_ptrs(const moe_config& c, const void* x, const void* w_r,
 }  // namespace
 
 extern "C" {
+
+uint64_t moe_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
 
 const char* moe_status_string(moe_status s) {
   switch (s) {
@@ -1385,7 +1397,7 @@ moe_status moe_quantize_fp8(int64_t rows, int32_t cols, int32_t dtype, const voi
   else
     quant_rows_kernel<float><<<(unsigned)blocks, 256, 0, as_stream(stream)>>>(static_cast<const float*>(src), rows,
                                                                               cols, codes, scales);
-  CUDA_TRY(cudaGetLastError());
+  CUDA_TRY(launched());
   return MOE_OK;
 }
 

@@ -137,6 +137,11 @@ moe_status moe_rows(const moe_config* cfg, int64_t* rows);
  * host only). */
 moe_status moe_workspace_size(const moe_config* cfg, int32_t op, size_t* bytes);
 
+/* Kernels this library has launched in the process so far (every successful
+ * launch, any stream or device).  Reading it before and after a region counts
+ * the region's launches; it is never reset.  Host only, thread-safe. */
+uint64_t moe_launch_count(void);
+
 /* Zero-fills a workspace.  Must run once after allocation, and again after a call
  * on it returned MOE_ERR_DEVICE_TIMEOUT; calls that succeed leave it reusable. */
 moe_status moe_workspace_init(void* workspace, size_t workspace_bytes, void* stream);
