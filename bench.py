@@ -88,13 +88,18 @@ class ClockSampler:
               "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
               "clocks_event_reasons.sw_power_cap")
 
-    def __init__(self, index: int):
+    def __init__(self, index: int, path: str = None):
+        """Samples GPU `index` every 100 ms into `path` (a temporary file if None)."""
         self.index = index
         self.proc = None
-        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_{index}.csv")
+        if path is None:
+            import tempfile
+            fd, path = tempfile.mkstemp(prefix=f"moe_clocks_{index}_", suffix=".csv")
+            os.close(fd)
+        self.path = path
 
     def __enter__(self):
-        os.makedirs(os.path.dirname(self.path), exist_ok=True)
+        os.makedirs(os.path.dirname(os.path.abspath(self.path)), exist_ok=True)
         try:
             self.fh = open(self.path, "w")
             self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
@@ -248,7 +253,7 @@ def run_ours(args, rank, world, local_rank):
         dist.barrier()
     torch.cuda.synchronize()
     launches0 = moe.moe_launch_count()  # the library counts every kernel it launches
-    with ClockSampler(local_rank) as clk:
+    with ClockSampler(local_rank, args.clocks_csv) as clk:
         for i in range(args.steps):
             step(events[i])
         torch.cuda.synchronize()
@@ -489,6 +494,7 @@ def main():
     ap.add_argument("--ref-sample", type=int, default=1, help="tokens whose FFN the oracle evaluates per step")
     ap.add_argument("--cpu-sample", type=int, default=8, help="tokens in the cpu_baseline sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--clocks-csv", default=None, help="where to keep the nvidia-smi samples of the timed region")
     ap.add_argument("--fused-permute", action="store_true",
                     help="gather the FFN's rows from x instead of permuting (bf16 weights-as-M layers)")
     args = ap.parse_args()
