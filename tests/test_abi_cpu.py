@@ -99,3 +99,19 @@ def test_argument_errors_before_any_launch():
     st = lib.moe_grouped_ffn(ctypes.byref(cfg), 4096, 4096, 4096, 4096, 4096, 4096, 4096, 1024, None)
     assert st == 4
     assert lib.moe_status_string(6) == b"MOE_ERR_DEVICE_TIMEOUT"
+    # bf16 router logits need their workspace (the partial sums of the h slices)
+    st = lib.moe_router_logits(ctypes.byref(cfg), 4096, 4096, None, 4096, None, None)
+    assert st == 1
+    st = lib.moe_router_logits(ctypes.byref(cfg), 4096, 4096, None, 4096, 4096 + 128, None)
+    assert st == 3
+
+
+def test_launch_count_host_only():
+    """The launch counter is host state: readable without a GPU, and no call
+    refused on the host (no launch) moves it."""
+    import expert_dispatch_bias_b300 as moe
+    n0 = moe.moe_launch_count()
+    assert n0 >= 0
+    cfg = _cfg()
+    assert moe.lib.moe_route(ctypes.byref(cfg), None, None, 4096, 4096, None) == 1
+    assert moe.moe_launch_count() == n0
