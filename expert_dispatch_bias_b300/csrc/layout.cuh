@@ -15,6 +15,9 @@
 // then adds them to n_ij and to the per-chip sent / received row counts; the
 // last block to finish turns those counts into bytes, derives the scalar
 // statistics and resets the look-back state for the next call.
+//
+// Up to kLayoutSmallMax assignments (decode batches) one block does all of it
+// in one launch (layout_small_kernel), without the look-back.
 #pragma once
 
 #include "common.cuh"

@@ -9,8 +9,8 @@
 //
 // Narrow rows (a few KB) pay the bulk-copy engine's per-copy cost more than
 // its bandwidth, so they are permuted by warps instead (permute_warp_kernel):
-// one warp per (token, chunk of kCombineChunk 16-byte vectors), each vector
-// read once and written to every kept slot.
+// one warp per (token, chunk of kPermChunk 16-byte vectors), each vector read
+// once and written to every kept slot.
 //
 // Combine is a gather: one warp per (token, column chunk of kCombineChunk
 // 16-byte vectors), 16-byte vector loads of the K expert-output rows, float32
