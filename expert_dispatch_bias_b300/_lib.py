@@ -77,7 +77,8 @@ def _load() -> ctypes.CDLL:
         "moe_rows": (c_int32, [cfgp, POINTER(c_int64)]),
         "moe_workspace_size": (c_int32, [cfgp, c_int32, POINTER(c_size_t)]),
         "moe_workspace_init": (c_int32, [c_void_p, c_size_t, c_void_p]),
-        "moe_router_logits": (c_int32, [cfgp, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p]),
+        "moe_router_logits": (c_int32, [cfgp, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_size_t,
+                                        c_void_p]),
         "moe_route": (c_int32, [cfgp, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p]),
         "moe_dispatch_layout": (c_int32, [cfgp] + [c_void_p] * 10 + [c_size_t, c_void_p]),
         "moe_dispatch_layout_static": (c_int32, [cfgp] + [c_void_p] * 9 + [c_void_p]),
@@ -173,8 +174,9 @@ def moe_workspace_init(ws, stream=None) -> None:
 
 def moe_router_logits(cfg, x, w_r, logit_offset, logits, workspace, stream=None) -> None:
     """workspace: moe_workspace_size(cfg, MOE_OP_LOGITS) bytes (alloc_workspace)."""
+    nbytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
     _check(lib.moe_router_logits(ctypes.byref(cfg), _ptr(x), _ptr(w_r), _ptr(logit_offset), _ptr(logits),
-                                 _ptr(workspace), _stream(stream)), "moe_router_logits")
+                                 _ptr(workspace), nbytes, _stream(stream)), "moe_router_logits")
 
 
 def moe_route(cfg, logits, sel_bias, topk_ids, topk_w, stream=None) -> None:

@@ -1028,12 +1028,15 @@ moe_status moe_workspace_init(void* workspace, size_t workspace_bytes, void* str
 }
 
 moe_status moe_router_logits(const moe_config* cfg, const void* x, const void* w_r, const float* logit_offset,
-                             float* logits, void* workspace, void* stream) {
+                             float* logits, void* workspace, size_t workspace_bytes, void* stream) {
   MOE_TRY(validate(cfg));
   if (cfg->T > 0) {
     MOE_TRY(check_dtype_ptr(x));
     MOE_TRY(check_ptr(logits, 4));
-    if (cfg->dtype == MOE_BF16) MOE_TRY(check_ptr(workspace, 256));
+    if (cfg->dtype == MOE_BF16) {
+      MOE_TRY(check_ptr(workspace, 256));
+      if (workspace_bytes < logits_ws_bytes(*cfg)) return MOE_ERR_WORKSPACE_TOO_SMALL;
+    }
   }
   MOE_TRY(check_dtype_ptr(w_r));
   MOE_TRY(check_opt_ptr(logit_offset, 4));

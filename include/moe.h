@@ -151,11 +151,13 @@ moe_status moe_workspace_init(void* workspace, size_t workspace_bytes, void* str
  * logit_offset [E] float32 or NULL; logits [T,E] float32.  bf16 layers cut the
  * sum over j into up to 8 slices (chosen from T, E, h and the SM count) whose
  * float32 partial sums are added in slice order, so a result never depends on
- * timing.  workspace: moe_workspace_size(MOE_OP_LOGITS) bytes, 256-byte aligned,
- * zero-filled once by moe_workspace_init (a successful call leaves it so);
- * float32 layers ignore it (NULL allowed).  One call at a time per workspace. */
+ * timing.  workspace: workspace_bytes >= moe_workspace_size(MOE_OP_LOGITS),
+ * 256-byte aligned (else MOE_ERR_WORKSPACE_TOO_SMALL / MOE_ERR_ALIGNMENT before
+ * any launch); float32 layers ignore it (NULL allowed).  One call at a time per
+ * workspace. */
 moe_status moe_router_logits(const moe_config* cfg, const void* x, const void* w_r,
-                             const float* logit_offset, float* logits, void* workspace, void* stream);
+                             const float* logit_offset, float* logits, void* workspace,
+                             size_t workspace_bytes, void* stream);
 
 /* Top-K routing ([overview] glossary "top-K"; [notes] "负载均衡": the aux-loss-free
  * per-expert bias steers selection only; [overview] glossary "Expert group").

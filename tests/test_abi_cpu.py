@@ -100,10 +100,13 @@ def test_argument_errors_before_any_launch():
     assert st == 4
     assert lib.moe_status_string(6) == b"MOE_ERR_DEVICE_TIMEOUT"
     # bf16 router logits need their workspace (the partial sums of the h slices)
-    st = lib.moe_router_logits(ctypes.byref(cfg), 4096, 4096, None, 4096, None, None)
+    need = moe.moe_workspace_size(cfg, moe.MOE_OP_LOGITS)
+    st = lib.moe_router_logits(ctypes.byref(cfg), 4096, 4096, None, 4096, None, need, None)
     assert st == 1
-    st = lib.moe_router_logits(ctypes.byref(cfg), 4096, 4096, None, 4096, 4096 + 128, None)
+    st = lib.moe_router_logits(ctypes.byref(cfg), 4096, 4096, None, 4096, 4096 + 128, need, None)
     assert st == 3
+    st = lib.moe_router_logits(ctypes.byref(cfg), 4096, 4096, None, 4096, 4096, need - 1, None)
+    assert st == 4
 
 
 def test_launch_count_host_only():
