@@ -410,6 +410,12 @@ __global__ void __launch_bounds__(kRouteWarps * 32, PER <= 8 ? 4 : 1) route_kern
   // ---- weights from the unbiased float64 scores of the chosen experts, one
   // (token, k) pair per thread: pair j is token j / K, choice j % K.
   const int pairs = nt * p.K;
+  if (p.K == 1 && p.renorm && p.key_is_logit) {
+    // renormalised top-1 on the logits: the chosen expert holds the largest
+    // logit, so its score is exp(0) = 1 and its weight exactly 1 * scale
+    for (int j = threadIdx.x; j < pairs; j += blockDim.x) p.w[(size_t)t0 + j] = p.scale;
+    return;
+  }
   for (int j = threadIdx.x; j < pairs; j += blockDim.x) {
     const double x = (double)s_x[j];
     s_s[j] = p.sigmoid ? 1.0 / (1.0 + exp(-x)) : exp(x - (double)s_m[j / p.K]);
