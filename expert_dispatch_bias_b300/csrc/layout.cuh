@@ -69,6 +69,13 @@ inline LayoutScratch layout_scratch_at(void* base, int64_t A, int E) {
   return s;
 }
 
+// Bytes at the start of the scratch that must be zero before a layout call: the
+// header (counters) and the tile flags, which layout_scratch_at places first.
+// The per-tile sums after them are written before they are read.
+inline size_t layout_scratch_zero_bytes(int64_t A) {
+  return 256 + align_up((size_t)layout_num_tiles(A) * 4, 256);
+}
+
 // Block-wide sum (or max) of one int64 per thread; every thread gets the
 // result.  Shuffles within warps, then one warp over the warp results:
 // no contended atomics.  All threads of the block must call it.

@@ -108,13 +108,20 @@ moe_status check_opt_ptr(const void* p, size_t a) { return (p == nullptr || alig
 struct DeviceInfo {
   int sms = 0;
 };
+// SM count per device, looked up once; several host threads may fill an entry
+// at the same time (they store the same value), hence the atomics.
 DeviceInfo device_info() {
-  static DeviceInfo cache[64];
+  static std::atomic<int> cache[64];
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev < 0 || dev >= 64) dev = 0;
-  if (cache[dev].sms == 0) cudaDeviceGetAttribute(&cache[dev].sms, cudaDevAttrMultiProcessorCount, dev);
-  return cache[dev];
+  DeviceInfo d;
+  d.sms = cache[dev].load(std::memory_order_relaxed);
+  if (d.sms == 0) {
+    cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev);
+    cache[dev].store(d.sms, std::memory_order_relaxed);
+  }
+  return d;
 }
 
 template <typename K>
@@ -204,19 +211,24 @@ LayerBuffers carve_layer(const moe_config& c, void* ws, bool host_io, bool block
 }
 
 // Device address of g_layout_static_scratch on the current device, looked up
-// once per device (host code cannot use the symbol itself as an address).
+// once per device, on the first call there (host code cannot use the symbol
+// itself as an address).  Concurrent first calls from several host threads
+// store the same value; the atomics make that race well defined.  The address
+// belongs to the device's current context: after cudaDeviceReset it is stale,
+// so a process that resets a device must not call moe_dispatch_layout_static
+// on it again.
 moe_status static_layout_scratch(void** out) {
-  static void* addr[64] = {};
+  static std::atomic<void*> addr[64];
   int dev = 0;
   CUDA_TRY(cudaGetDevice(&dev));
   if (dev < 0 || dev >= 64) return MOE_ERR_UNSUPPORTED;
-  if (addr[dev] == nullptr) {
-    void* p = nullptr;
+  void* p = addr[dev].load(std::memory_order_acquire);
+  if (p == nullptr) {
     CUDA_TRY(cudaGetSymbolAddress(&p, g_layout_static_scratch));
     if (p == nullptr) return MOE_ERR_CUDA;
-    addr[dev] = p;
+    addr[dev].store(p, std::memory_order_release);
   }
-  *out = addr[dev];
+  *out = p;
   return MOE_OK;
 }
 
@@ -1096,10 +1108,9 @@ moe_status moe_dispatch_layout_static(const moe_config* cfg, const int32_t* topk
   if (layout_scratch_bytes(A, nphys(*cfg)) > MOE_LAYOUT_STATIC_SCRATCH_BYTES) return MOE_ERR_WORKSPACE_TOO_SMALL;
   void* scratch = nullptr;
   MOE_TRY(static_layout_scratch(&scratch));
-  // the counters and tile flags must start at zero; the per-tile sums are
-  // written before they are read
-  const size_t zero_bytes = 256 + align_up((size_t)layout_num_tiles(A) * 4, 256);
-  CUDA_TRY(cudaMemsetAsync(scratch, 0, zero_bytes, as_stream(stream)));
+  // the counters and tile flags must start at zero (the array keeps the
+  // previous call's contents); the per-tile sums are written before they are read
+  CUDA_TRY(cudaMemsetAsync(scratch, 0, layout_scratch_zero_bytes(A), as_stream(stream)));
   return launch_layout(*cfg, topk_ids, counts, kept, offsets, slot, row_src, n_ij, rank_bytes, stats, scratch,
                        as_stream(stream));
 }

@@ -412,8 +412,11 @@ __global__ void __launch_bounds__(kRouteWarps * 32, PER <= 8 ? 4 : 1) route_kern
   const int pairs = nt * p.K;
   if (p.K == 1 && p.renorm && p.key_is_logit) {
     // renormalised top-1 on the logits: the chosen expert holds the largest
-    // logit, so its score is exp(0) = 1 and its weight exactly 1 * scale
-    for (int j = threadIdx.x; j < pairs; j += blockDim.x) p.w[(size_t)t0 + j] = p.scale;
+    // logit, so its score is exp(0) = 1 and its weight exactly 1 * scale.  A
+    // row whose chosen logit is not finite (NaN, or every logit -inf) gets NaN,
+    // as s / s with s = exp(x - max) gives in the general path.
+    for (int j = threadIdx.x; j < pairs; j += blockDim.x)
+      p.w[(size_t)t0 + j] = isfinite(s_x[j]) ? p.scale : __int_as_float(0x7fffffff);
     return;
   }
   for (int j = threadIdx.x; j < pairs; j += blockDim.x) {

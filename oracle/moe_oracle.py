@@ -189,9 +189,20 @@ def route(L: np.ndarray, cfg, bias: Optional[np.ndarray] = None):
     return ids, w, keys, allowed
 
 
+# Near-ties.  Two implementations whose logits differ in the last bits (float32
+# against float64 sums) may route a token differently only where the decision
+# rests on keys that nearly tie.  The margins below measure, per token, how far
+# the decision is from a tie: the relative gap between the two scores the
+# decision compares.  READING (the benchmark spec tolerance rule; [overview] glossary
+# "top-K"): a top-K difference is excused only where such a gap is < 1e-4.
+
+
 def group_margin(keys: np.ndarray, cfg) -> np.ndarray:
     """Relative gap between the last kept and the first dropped group score of every
-    token (inf without a group limit).  See topk_margin."""
+    token: (g_M - g_{M+1}) / |g_M| with the group scores sorted descending and M
+    = topk_groups (inf without a group limit or when every group is kept).  A
+    group's score is the sum of its ``group_topn`` largest keys, as in
+    allowed_experts."""
     T, E = keys.shape
     out = np.full(T, np.inf)
     if cfg.n_groups <= 0 or cfg.topk_groups >= cfg.n_groups:
@@ -209,9 +220,9 @@ def group_margin(keys: np.ndarray, cfg) -> np.ndarray:
 
 
 def topk_margin(keys: np.ndarray, allowed: np.ndarray, K: int) -> np.ndarray:
-    """Relative gap between the K-th and (K+1)-th allowed key of every token
-    (inf when fewer than K+1 experts are allowed).  Used to tell genuine routing
-    differences from near-ties when floating-point logits differ slightly."""
+    """Relative gap between the K-th and (K+1)-th allowed key of every token,
+    (k_K - k_{K+1}) / |k_K| (inf when fewer than K+1 experts are allowed): how
+    far the choice of the K-expert SET is from a tie."""
     T, E = keys.shape
     out = np.full(T, np.inf)
     for t in range(T):
@@ -219,6 +230,28 @@ def topk_margin(keys: np.ndarray, allowed: np.ndarray, K: int) -> np.ndarray:
         if len(v) > K:
             out[t] = abs(v[K - 1] - v[K]) / max(abs(v[K - 1]), 1e-30)
     return out
+
+
+def order_margin(keys: np.ndarray, allowed: np.ndarray, K: int) -> np.ndarray:
+    """Smallest relative gap (k_i - k_{i+1}) / |k_i| between adjacent keys among a
+    token's K+1 largest allowed keys (inf when at most one key is allowed).
+
+    The ids are listed in descending key order, so two chosen experts whose keys
+    nearly tie may swap places, just as the K-th and (K+1)-th may swap in and
+    out of the set; this margin covers both (it is <= topk_margin)."""
+    T, E = keys.shape
+    out = np.full(T, np.inf)
+    for t in range(T):
+        v = sorted(keys[t][allowed[t]].astype(np.float64).tolist(), reverse=True)[:K + 1]
+        for a, b in zip(v, v[1:]):
+            out[t] = min(out[t], abs(a - b) / max(abs(a), 1e-30))
+    return out
+
+
+def near_tie_margin(keys: np.ndarray, allowed: np.ndarray, cfg) -> np.ndarray:
+    """Per token, the smaller of order_margin and group_margin: the relative gap of
+    the closest comparison the routing decision (groups, set and order) rests on."""
+    return np.minimum(order_margin(keys, allowed, cfg.K), group_margin(keys, cfg))
 
 
 # ----------------------------------------------------------------- step 3: dispatch layout

@@ -19,3 +19,16 @@ GOLDEN = os.path.join(ROOT, "tests", "golden")
 @pytest.fixture(scope="session")
 def golden_dir():
     return GOLDEN
+
+
+def pytest_terminal_summary(terminalreporter):
+    """Counts of near-tie routing differences of the end-to-end layer tests: a
+    token may route differently from the oracle only where the oracle's keys
+    nearly tie (relative gap < 1e-4); every such token is counted here."""
+    helpers = sys.modules.get("gpu_helpers")
+    log = getattr(helpers, "NEAR_TIE_LOG", None)
+    if not log:
+        return
+    terminalreporter.section("near-tie routing (tokens / oracle near-ties / routed differently / compared)")
+    for name, tokens, near, diff, compared in log:
+        terminalreporter.write_line(f"{name}: {tokens} / {near} / {diff} / {compared}")

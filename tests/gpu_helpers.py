@@ -80,3 +80,13 @@ def oracle_routing(name: str):
 
 def expert_weights(w: workloads.Workload, e: int):
     return workloads.host_w13(w, e), workloads.host_w2(w, e)
+
+
+# Routing differences seen by the end-to-end tests, printed in pytest's terminal
+# summary (tests/conftest.py): (test, tokens, near-tie tokens of the oracle,
+# tokens the GPU routed differently, tokens compared in float).
+NEAR_TIE_LOG = []
+
+
+def log_near_ties(name: str, tokens: int, near_tie: int, routed_differently: int, compared: int) -> None:
+    NEAR_TIE_LOG.append((name, tokens, near_tie, routed_differently, compared))

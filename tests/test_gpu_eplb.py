@@ -11,8 +11,8 @@ import oracle
 import synth
 from synth import device, workloads
 
-from gpu_helpers import TOL, dev_of, host_inputs, np_of, rel_err
-from test_gpu_layer import NEAR_TIE, order_margin
+from gpu_helpers import log_near_ties, TOL, dev_of, host_inputs, np_of, rel_err
+from test_gpu_layer import NEAR_TIE
 
 pytestmark = pytest.mark.gpu
 
@@ -89,7 +89,7 @@ def check_layer_eplb(w, sample=None, seed=0):
     assert moe.moe_check() == 0
     gids = np_of(o["topk_ids"])
     bad = np.nonzero((gids != ids).any(axis=1))[0]
-    margin = np.minimum(order_margin(keys, allowed, K), oracle.group_margin(keys, w))
+    margin = oracle.near_tie_margin(keys, allowed, w)
     assert np.all(margin[bad] < NEAR_TIE), f"routing differs away from a near-tie at tokens {bad[:8]}"
     # the layout over physical experts, bit-exact against the oracle's from the GPU's logical ids
     pcfg = w.replace(E=P, n_groups=0, topk_groups=0, group_topn=0)
@@ -118,8 +118,10 @@ def check_layer_eplb(w, sample=None, seed=0):
     yp = np.zeros(xp.shape, dtype=xp.dtype)
     for e, (idx, val) in parts.items():
         yp[idx] = val
-    ref = oracle.combine(yp, lay["slot"], np_of(o["topk_w"]), pcfg, tokens=list(tokens), rounded=False)
+    # the oracle's own weights (the GPU's routed like the oracle at these tokens)
+    ref = oracle.combine(yp, lay["slot"], wts, pcfg, tokens=list(tokens), rounded=False)
     err = rel_err(np_of(y)[tokens], ref, w.dtype)
+    log_near_ties(w.name, T, int((margin < NEAR_TIE).sum()), len(bad), len(tokens))
     assert err <= TOL[w.dtype], err
     return stats
 

@@ -1,6 +1,8 @@
 """The permutation fused into the grouped FFN (rows gathered from x through
-row_src) against the two-step path (explicit permute, then the FFN on the
-permuted copy): bit-identical expert outputs, since only the load path differs."""
+row_src) against the oracle: the oracle permutes x by row_src and runs every
+expert's FFN (a sample of experts, every row of each, at full size).  The
+two-step path (explicit permute, then the FFN on the permuted copy) must also
+give bit-identical expert outputs, since only the load path differs."""
 import numpy as np
 import pytest
 import torch
@@ -10,7 +12,7 @@ import oracle
 import synth
 from synth import device, workloads
 
-from gpu_helpers import dev_of
+from gpu_helpers import TOL, dev_of, expert_weights, np_of, rel_err
 
 pytestmark = pytest.mark.gpu
 
@@ -46,6 +48,20 @@ def test_gather_equals_permute_then_ffn(w):
     assert moe.moe_check() == 0
     rows = torch.from_numpy(lay["row_src"] >= 0).cuda()
     assert torch.equal(ya[rows], yb[rows])
+    # against the oracle on the oracle's own permutation of x
+    xp_ref = oracle.permute(np_of(inp["x"]), lay["row_src"])
+    nz = np.nonzero(lay["kept"])[0]
+    full_size = w.h * w.I > 4 << 20
+    if full_size:
+        experts = sorted({int(nz[0]), int(nz[len(nz) // 2]), int(nz[-1])})
+        get13, get2 = (lambda e: expert_weights(w, e)[0]), (lambda e: expert_weights(w, e)[1])
+    else:
+        experts = [int(e) for e in nz]
+        get13, get2 = (lambda e: np_of(inp["w13"][e])), (lambda e: np_of(inp["w2"][e]))
+    ref = oracle.grouped_ffn(xp_ref, lay["offsets"], lay["kept"], get13, get2, w, experts=experts, rounded=False)
+    got = np_of(yb)
+    worst = max(rel_err(got[idx], val, w.dtype) for idx, val in ref.values() if len(idx))
+    assert worst <= TOL[w.dtype], worst
 
 
 def test_gather_refuses_tokens_as_m_layers():

@@ -137,3 +137,24 @@ def test_route_sigmoid_near_ties(E, K, G, topn):
     if G:
         kw.update(n_groups=G, topk_groups=G // 2, group_topn=topn)
     _route_case(kw, L, bias)
+
+
+def test_top1_weight_of_non_finite_logits_is_nan():
+    """Renormalised top-1 on the logits writes the scale as the weight without
+    evaluating s / s; rows whose logits are NaN or all -inf still get NaN, as
+    the oracle's float64 evaluation gives, so bad router input is not hidden."""
+    w = workloads.SWITCH.replace(name="switch_nan", T=64)
+    cfg = moe.config_from(w)
+    L = synth.normal(4, synth.TID_TEST + 23, (w.T, w.E), 1.0, "f32").astype(np.float32)
+    L[3, :] = np.nan
+    L[9, :] = -np.inf
+    ids = torch.empty(w.T, 1, dtype=torch.int32, device="cuda")
+    wts = torch.empty(w.T, 1, dtype=torch.float32, device="cuda")
+    moe.moe_route(cfg, dev_of(L), None, ids, wts)
+    assert moe.moe_check() == 0
+    got = np_of(wts)[:, 0]
+    _, ref, _, _ = oracle.route(L, w)
+    bad = [3, 9]
+    assert np.isnan(ref[bad, 0]).all() and np.isnan(got[bad]).all()
+    good = np.setdiff1d(np.arange(w.T), bad)
+    assert np.array_equal(got[good], ref[good, 0]) and (got[good] == w.scale).all()

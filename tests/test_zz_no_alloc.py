@@ -66,6 +66,35 @@ def test_static_layout_matches_workspace_layout(w):
             assert torch.equal(a, b)
 
 
+SEQUENCE = [
+    workloads.DSV3,                                                                   # two passes, 16 tiles
+    workloads.DSV3.replace(name="dsv3_decode_T256", T=256),                           # one block (2048 assignments)
+    workloads.Workload("mid", T=3000, h=64, E=60, K=4, I=64, dtype="bf16", score="softmax", capacity=220,
+                       ep_size=6),                                                    # two passes, 3 tiles, drops
+    workloads.DSV3,
+    workloads.Workload("mid", T=3000, h=64, E=60, K=4, I=64, dtype="bf16", score="softmax", capacity=220,
+                       ep_size=6),
+]
+
+
+def test_static_layout_sequence_of_mixed_configurations():
+    """Each call starts clean whatever the previous call left in the shared array:
+    a multi-tile layout, then the one-block path, then a smaller multi-tile one
+    with drops, and back, each equal to the workspace call."""
+    for i, w in enumerate(SEQUENCE):
+        cfg = moe.config_from(w)
+        ids = torch.from_numpy(synth.uniform_topk_ids(30 + i, synth.TID_TEST + 21, w.T, w.E, w.K)).cuda()
+        ref_buf = moe.alloc_layout(cfg)
+        moe.moe_dispatch_layout(cfg, ids, ref_buf.counts, ref_buf.kept, ref_buf.offsets, ref_buf.slot,
+                                ref_buf.row_src, ref_buf.n_ij, ref_buf.rank_bytes, ref_buf.stats,
+                                moe.alloc_workspace(cfg, moe.MOE_OP_LAYOUT))
+        buf = moe.alloc_layout(cfg)
+        _call_static(cfg, ids, buf)
+        assert moe.moe_check() == 0
+        for a, b in zip(_outputs(buf), _outputs(ref_buf)):
+            assert torch.equal(a, b), (i, w.name)
+
+
 def test_static_layout_refuses_layouts_above_its_fixed_scratch():
     w = workloads.Workload("big", T=400000, h=64, E=1024, K=8, I=64, dtype="bf16", score="softmax", ep_size=8)
     cfg = moe.config_from(w)
