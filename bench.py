@@ -3,16 +3,23 @@
   python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
 
 A step is one pass of the whole hot path over one batch: router logits ->
-routing -> dispatch layout -> permute -> grouped SwiGLU FFN -> combine, each a
-call of the C library on the current stream, with CUDA events between the
-calls so every stage is timed live inside the timed region.  Inputs are
-resident in HBM before timing starts; the per-step working set (22.5 GB of
-expert weights at the DeepSeek-V3 shape) is far larger than the 126 MB L2.
+routing -> dispatch layout -> permute -> grouped SwiGLU FFN -> combine, issued
+as ONE call of the C library (moe_layer_forward, or the block / replica / FP8
+layer call of the workload) on the current stream.  The library records the
+caller's CUDA events between its stages (moe_layer_out.stage_events), so each
+stage is timed live inside the timed region without extra host calls.  Inputs
+are resident in HBM before timing starts; the per-step working set (22.5 GB
+of expert weights at the DeepSeek-V3 shape) is far larger than the 126 MB L2.
 
-``e2e`` repeats the measurement through moe_layer_forward_host: the host->device
-copy of x from pinned memory, the layer and the device->host copy of y are all
-inside its timed region, every step; two streams take alternate steps so one
-step's copies overlap the other's compute.
+``e2e`` repeats the measurement through moe_layer_forward_host: the
+host->device copy of x from pinned memory, the layer and the device->host
+copy of y are all inside its timed region, every step; two streams take
+alternate steps so one step's copies overlap the other's compute.
+
+After the headline workload the same run measures every other workload of
+the pages (Mixtral, Switch-Base, the DeepSeek-V3 decode sweep) into
+``workloads``, and times permute and combine alone with L2 flushed before
+every repetition (``cold``) beside their in-step (``warm``) rates.
 
 Under torchrun (N > 1) every rank runs an independent replica of the layer
 (the path has no data exchange on one node: the expert-parallel traffic is
@@ -26,10 +33,13 @@ from __future__ import annotations
 
 import argparse
 import json
+import math
 import os
+import platform
 import statistics
 import subprocess
 import sys
+import threading
 import time
 
 ROOT = os.path.dirname(os.path.abspath(__file__))
@@ -45,6 +55,10 @@ METRIC = "MoE-layer tokens/s at DeepSeek-V3 shape; permute GB/s & GEMM % of peak
 # algorithmic bytes.  Re-measure whenever the kernel changes.
 FFN_TRAFFIC_RATIO = 1.0002
 FALLBACK_PEAKS = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0}
+# The other workloads of the pages, measured after the headline one.
+SWEEP = ("mixtral_8x7b", "switch_base", "deepseek_v3_decode_T32", "deepseek_v3_decode_T256",
+         "deepseek_v3_decode_T1024")
+L2_FLUSH_BYTES = 256 << 20   # written between cold repetitions (L2 is 126 MB)
 
 
 def measured_peaks():
@@ -65,6 +79,11 @@ def workload_config(w):
             "parallelism": "replicas"}
 
 
+def find_workload(name):
+    from synth import workloads
+    return workloads.ALL.get(name) or workloads.EXTRA[name]
+
+
 # ---------------------------------------------------------------------------- ranks
 def max_over_ranks(value: float, world: int, device) -> float:
     """The largest `value` over all ranks (one scalar all-reduce; timing only)."""
@@ -83,286 +102,412 @@ def job_throughput(tokens_per_rank: int, world: int, steps: int, max_ms: float) 
 
 
 # ---------------------------------------------------------------------------- clocks
-class ClockSampler:
-    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
-              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
-              "clocks_event_reasons.sw_power_cap")
+REASON_BITS = {"hw_slowdown": 0x8, "hw_thermal_slowdown": 0x40, "sw_thermal_slowdown": 0x20,
+               "sw_power_cap": 0x4}
 
-    def __init__(self, index: int, path: str = None):
-        """Samples GPU `index` every 100 ms into `path` (a temporary file if None)."""
-        self.index = index
-        self.proc = None
-        if path is None:
-            import tempfile
-            fd, path = tempfile.mkstemp(prefix=f"moe_clocks_{index}_", suffix=".csv")
-            os.close(fd)
-        self.path = path
+
+class ClockSampler:
+    """Samples the SM clock, power and clock-event reasons of one GPU while the
+    timed region runs: through NVML every `period_s` (read-only queries), or
+    through `nvidia-smi -lms 100` where NVML is unavailable."""
+
+    def __init__(self, cuda_index: int, period_s: float = 0.005, csv_path: str = None):
+        self.index = cuda_index
+        self.period = period_s
+        self.csv_path = csv_path
+        self.rows = []          # (sm_mhz, max_mhz, power_w, reasons bitmask)
+        self.kind = None
+        self._stop = threading.Event()
+
+    def _nvml_handle(self):
+        import pynvml
+        import torch
+        pynvml.nvmlInit()
+        try:
+            uuid = str(torch.cuda.get_device_properties(self.index).uuid)
+            return pynvml.nvmlDeviceGetHandleByUUID("GPU-" + uuid)
+        except Exception:  # noqa: BLE001
+            return pynvml.nvmlDeviceGetHandleByIndex(self.index)
+
+    def _loop(self, h):
+        import pynvml
+        mx = pynvml.nvmlDeviceGetMaxClockInfo(h, pynvml.NVML_CLOCK_SM)
+        while not self._stop.is_set():
+            try:
+                self.rows.append((float(pynvml.nvmlDeviceGetClockInfo(h, pynvml.NVML_CLOCK_SM)), float(mx),
+                                  pynvml.nvmlDeviceGetPowerUsage(h) / 1e3,
+                                  int(pynvml.nvmlDeviceGetCurrentClocksEventReasons(h))))
+            except Exception:  # noqa: BLE001
+                pass
+            time.sleep(self.period)
 
     def __enter__(self):
-        os.makedirs(os.path.dirname(os.path.abspath(self.path)), exist_ok=True)
         try:
-            self.fh = open(self.path, "w")
-            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
-                                          "--format=csv,noheader,nounits", "-lms", "100"],
-                                         stdout=self.fh, stderr=subprocess.DEVNULL)
-        except OSError:
-            self.proc = None
-        time.sleep(0.3)
+            h = self._nvml_handle()
+            self.kind = f"nvml every {self.period * 1e3:.0f} ms"
+            self.thread = threading.Thread(target=self._loop, args=(h,), daemon=True)
+            self.thread.start()
+        except Exception as e:  # noqa: BLE001
+            self.kind = f"nvidia-smi every 100 ms (NVML unavailable: {type(e).__name__}: {e})"
+            self.thread = None
+            import tempfile
+            fd, path = tempfile.mkstemp(prefix=f"moe_clocks_{self.index}_", suffix=".csv")
+            os.close(fd)
+            self.smi_path = path
+            fields = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active")
+            try:
+                self.fh = open(path, "w")
+                self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.index), f"--query-gpu={fields}",
+                                              "--format=csv,noheader,nounits", "-lms", "100"],
+                                             stdout=self.fh, stderr=subprocess.DEVNULL)
+            except OSError:
+                self.proc = None
+            time.sleep(0.3)
         return self
 
     def __exit__(self, *exc):
-        if self.proc is not None:
+        if self.thread is not None:
+            self._stop.set()
+            self.thread.join(timeout=5)
+        elif getattr(self, "proc", None) is not None:
             self.proc.terminate()
             self.proc.wait(timeout=10)
             self.fh.close()
+            for line in open(self.smi_path):
+                p = [x.strip() for x in line.split(",")]
+                try:
+                    self.rows.append((float(p[0]), float(p[1]), float(p[2]), int(p[3], 16)))
+                except (ValueError, IndexError):
+                    continue
+        if self.csv_path:
+            os.makedirs(os.path.dirname(os.path.abspath(self.csv_path)), exist_ok=True)
+            with open(self.csv_path, "w") as f:
+                f.write("sm_mhz,max_sm_mhz,power_w,reasons\n")
+                for r in self.rows:
+                    f.write(f"{r[0]:.0f},{r[1]:.0f},{r[2]:.1f},0x{r[3]:x}\n")
 
     def summary(self):
-        if self.proc is None:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
-        rows = []
-        for line in open(self.path):
-            parts = [p.strip() for p in line.split(",")]
-            if len(parts) < 8:
-                continue
-            try:
-                rows.append((float(parts[0]), float(parts[1]), float(parts[2]), parts[4:8]))
-            except ValueError:
-                continue
-        if not rows:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
-        loaded = [r for r in rows if r[2] > 300.0] or rows
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        reasons = sorted({names[i] for r in loaded for i, v in enumerate(r[3]) if v.lower() == "active"})
-        return {"sm_mhz": statistics.median(r[0] for r in loaded), "sm_max_mhz": max(r[1] for r in rows),
-                "samples": len(loaded), "power_w_max": max(r[2] for r in rows), "reasons": reasons}
+        if not self.rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "source": self.kind}
+        loaded = [r for r in self.rows if r[2] > 300.0] or self.rows
+        reasons = sorted({n for r in loaded for n, bit in REASON_BITS.items() if r[3] & bit})
+        return {"sm_mhz": statistics.median(r[0] for r in loaded), "sm_max_mhz": max(r[1] for r in self.rows),
+                "samples": len(self.rows), "samples_under_load": len([r for r in self.rows if r[2] > 300.0]),
+                "power_w_max": max(r[2] for r in self.rows), "reasons": reasons, "source": self.kind}
 
 
 # ---------------------------------------------------------------------------- our arm
-def run_ours(args, rank, world, local_rank):
-    import numpy as np
-    import torch
-    import torch.distributed as dist
+class Layer:
+    """One workload's layer on the device: inputs, buffers and the one library
+    call a step makes, with its per-step outputs and stage events."""
 
-    import expert_dispatch_bias_b300 as moe
-    from synth import device, workloads
+    def __init__(self, w, weights_from=None):
+        import torch
+
+        import expert_dispatch_bias_b300 as moe
+        from synth import device
+
+        self.moe, self.w = moe, w
+        self.cfg = cfg = moe.config_from(w)
+        reuse = weights_from is not None
+        self.inp = inp = device.layer_inputs(w, weights=not reuse)
+        if reuse:   # same expert shapes and seed: the same weights
+            for k in ("w13", "w2", "w13s", "w2s"):
+                if k in weights_from:
+                    inp[k] = weights_from[k]
+        dt = inp["x"].dtype
+        self.R = R = moe.moe_rows(cfg)
+        T, K, E, N = w.T, w.K, w.E, w.ep_size
+        P = E + w.n_redundant
+        i32 = dict(dtype=torch.int32, device="cuda")
+        self.out = dict(topk_ids=torch.empty(T, K, **i32), topk_w=torch.empty(T, K, device="cuda"),
+                        counts=torch.empty(P, **i32), kept=torch.empty(P, **i32), offsets=torch.empty(P + 1, **i32),
+                        slot=torch.empty(T, K, **i32), row_src=torch.empty(max(R, 1), **i32),
+                        n_ij=torch.empty(N * N, dtype=torch.int64, device="cuda"),
+                        rank_bytes=torch.empty(2 * N, dtype=torch.int64, device="cuda"),
+                        stats=torch.empty(4, dtype=torch.int64, device="cuda"))
+        self.y = torch.empty(T, w.h, dtype=dt, device="cuda")
+        self.kind = ("fp8" if w.fp8 else "eplb" if w.n_redundant > 0 else "block" if w.shared_I > 0 else "layer")
+        op = {"fp8": moe.MOE_OP_LAYER_FP8, "eplb": moe.MOE_OP_LAYER, "block": moe.MOE_OP_BLOCK,
+              "layer": moe.MOE_OP_LAYER}[self.kind]
+        self.ws = moe.alloc_workspace(cfg, op)
+        self.stream = torch.cuda.current_stream()
+        if self.kind == "eplb":   # replicas: planned once from this batch's logical expert loads (not timed)
+            logits = torch.empty(T, E, device="cuda")
+            moe.moe_router_logits(cfg, inp["x"], inp["w_r"], inp["logit_offset"], logits,
+                                  moe.alloc_workspace(cfg, moe.MOE_OP_LOGITS))
+            moe.moe_route(cfg, logits, inp["sel_bias"], self.out["topk_ids"], self.out["topk_w"])
+            counts = torch.bincount(self.out["topk_ids"].view(-1).long(), minlength=E).cpu().numpy()
+            self.plan_h = moe.moe_eplb_plan(E, N, w.n_redundant, counts)
+            self.plan = {k: torch.from_numpy(v).cuda() for k, v in self.plan_h.items() if k != "rank_load"}
+        if self.kind == "fp8":    # expert weights quantised once here (not timed)
+            self.q13 = torch.empty(inp["w13"].shape, dtype=torch.uint8, device="cuda")
+            self.s13 = torch.empty(E, 2 * w.I, dtype=torch.float32, device="cuda")
+            self.q2 = torch.empty(inp["w2"].shape, dtype=torch.uint8, device="cuda")
+            self.s2 = torch.empty(E, w.h, dtype=torch.float32, device="cuda")
+            moe.moe_quantize_fp8(inp["w13"].view(-1, w.h), self.q13.view(-1, w.h), self.s13.view(-1))
+            moe.moe_quantize_fp8(inp["w2"].view(-1, w.I), self.q2.view(-1, w.I), self.s2.view(-1))
+            del inp["w13"], inp["w2"]
+            torch.cuda.synchronize()
+
+    def call(self, y, out, ws, stream=None):
+        """The one library call of a step (device activations)."""
+        moe, inp, cfg = self.moe, self.inp, self.cfg
+        if self.kind == "fp8":
+            moe.moe_layer_forward_fp8(cfg, inp["x"], inp["w_r"], inp["logit_offset"], inp["sel_bias"], self.q13,
+                                      self.s13, self.q2, self.s2, y, out, ws, stream=stream)
+        elif self.kind == "eplb":
+            moe.moe_layer_forward_eplb(cfg, inp["x"], inp["w_r"], inp["logit_offset"], inp["sel_bias"],
+                                       inp["w13"], inp["w2"], self.plan["rep_offsets"], self.plan["rep_phys"],
+                                       self.plan["phys_to_log"], y, out, ws, stream=stream)
+        elif self.kind == "block":
+            moe.moe_block_forward(cfg, inp["x"], inp["w_r"], inp["logit_offset"], inp["sel_bias"], inp["w13"],
+                                  inp["w2"], inp["w13s"], inp["w2s"], y, out, ws, stream=stream)
+        else:
+            moe.moe_layer_forward(cfg, inp["x"], inp["w_r"], inp["logit_offset"], inp["sel_bias"], inp["w13"],
+                                  inp["w2"], y, out, ws, stream=stream)
+
+    def timed(self, steps, warmup, world=1, clocks_csv=None):
+        """W untimed steps, then exactly `steps` steps between a barrier and a
+        synchronize on both sides; every step is one library call that records
+        its own stage events.  Returns (total ms, per-stage mean ms, clocks,
+        launches)."""
+        import torch
+        import torch.distributed as dist
+
+        moe = self.moe
+        n_ev = len(moe.LAYER_STAGES) + 1
+        plain = moe.layer_out(**self.out)
+        for _ in range(warmup):
+            self.call(self.y, plain, self.ws)
+        st = moe.moe_check()
+        if st != 0:
+            raise RuntimeError(f"device error during warm-up: {moe.STATUS[st]}")
+        events = [[torch.cuda.Event(enable_timing=True) for _ in range(n_ev)] for _ in range(steps)]
+        for evs in events:          # torch creates each CUDA event on its first record
+            for e in evs:
+                e.record(self.stream)
+        outs = [moe.layer_out(stage_events=evs, **self.out) for evs in events]
+        if world > 1:
+            dist.barrier()
+        torch.cuda.synchronize()
+        launches0 = moe.moe_launch_count()   # the library counts every kernel it launches
+        with ClockSampler(torch.cuda.current_device(), csv_path=clocks_csv) as clk:
+            for o in outs:
+                self.call(self.y, o, self.ws)
+            torch.cuda.synchronize()
+        launches = moe.moe_launch_count() - launches0
+        if world > 1:
+            dist.barrier()
+        st = moe.moe_check()
+        if st != 0:
+            raise RuntimeError(f"device error in the timed region: {moe.STATUS[st]}")
+        total = events[0][0].elapsed_time(events[-1][n_ev - 1])
+        stages = {s: statistics.mean(events[i][j].elapsed_time(events[i][j + 1]) for i in range(steps))
+                  for j, s in enumerate(moe.LAYER_STAGES)}
+        return total, stages, clk.summary(), launches
+
+    def e2e(self, steps, warmup, world=1):
+        """The same steps through the public call with HOST activations: pinned x
+        in, y out, both copies inside the timed region every step, on two
+        streams that take alternate steps.  Returns (ms, bytes in, bytes out)."""
+        import torch
+        import torch.distributed as dist
+
+        moe, inp, cfg, w = self.moe, self.inp, self.cfg, self.w
+        host_call = self.kind in ("layer", "block")
+        op = moe.MOE_OP_BLOCK_HOST if self.kind == "block" else moe.MOE_OP_LAYER_HOST
+        lanes = [dict(stream=torch.cuda.Stream(), x=inp["x"].cpu().pin_memory(),
+                      y=torch.empty(w.T, w.h, dtype=self.y.dtype).pin_memory(),
+                      ws=moe.alloc_workspace(cfg, op) if host_call else moe.alloc_workspace(
+                          cfg, moe.MOE_OP_LAYER_FP8 if self.kind == "fp8" else moe.MOE_OP_LAYER),
+                      xd=None if host_call else torch.empty_like(inp["x"]),
+                      yd=None if host_call else torch.empty_like(self.y))
+                 for _ in range(2)]
+
+        def step(i):
+            ln = lanes[i % len(lanes)]
+            if self.kind == "block":
+                moe.moe_block_forward_host(cfg, ln["x"], inp["w_r"], inp["logit_offset"], inp["sel_bias"],
+                                           inp["w13"], inp["w2"], inp["w13s"], inp["w2s"], ln["y"], ln["ws"],
+                                           stream=ln["stream"])
+            elif self.kind == "layer":
+                moe.moe_layer_forward_host(cfg, ln["x"], inp["w_r"], inp["logit_offset"], inp["sel_bias"],
+                                           inp["w13"], inp["w2"], ln["y"], ln["ws"], stream=ln["stream"])
+            else:   # layer calls that take device activations: the copies on the lane's stream around them
+                with torch.cuda.stream(ln["stream"]):
+                    ln["xd"].copy_(ln["x"], non_blocking=True)
+                    self.call(ln["yd"], None, ln["ws"], stream=ln["stream"])
+                    ln["y"].copy_(ln["yd"], non_blocking=True)
+
+        for i in range(max(2, warmup)):
+            step(i)
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        if world > 1:
+            dist.barrier()
+        e0.record(self.stream)
+        for ln in lanes:
+            ln["stream"].wait_event(e0)
+        for i in range(steps):
+            step(i)
+        for ln in lanes:
+            self.stream.wait_stream(ln["stream"])
+        e1.record(self.stream)
+        torch.cuda.synchronize()
+        if moe.moe_check() != 0:
+            raise RuntimeError("device error in the end-to-end run")
+        if not torch.equal(lanes[0]["y"].to(self.y.device), self.y):
+            raise RuntimeError("the end-to-end layer output differs from the device-resident one")
+        nbytes = w.T * w.h * self.y.element_size()
+        return e0.elapsed_time(e1), nbytes, nbytes
+
+    def work(self):
+        """Algorithmic work of one step, from the layout of the last step."""
+        import numpy as np
+
+        w = self.w
+        kept = self.out["kept"].cpu().numpy().astype(np.int64)
+        stats = self.moe.stats_dict(self.out["stats"])
+        rows_kept = int(kept.sum())
+        ds = 2 if w.dtype == "bf16" else 4
+        touched = int((kept > 0).sum())
+        if self.kind == "eplb":   # replicas share their logical expert's weights: count each once
+            touched = len(set(self.plan_h["phys_to_log"][kept > 0].tolist()))
+        if w.fp8:   # E4M3 weights (+ float32 row scales); E4M3 rows in, bf16 intermediate, re-quantised, bf16 out
+            weight_bytes = touched * (3 * w.h * w.I + 4 * (2 * w.I + w.h))
+            ffn_bytes = weight_bytes + rows_kept * (w.h + 4 + 2 * w.I * 2 + w.I * 2 + 4 + 2 * w.h)
+        else:
+            weight_bytes = touched * 3 * w.h * w.I * ds
+            ffn_bytes = weight_bytes + rows_kept * (2 * w.h + 2 * w.I) * ds
+        slot = self.out["slot"].view(w.T, w.K)
+        tokens_with_rows = int((slot >= 0).any(dim=1).sum().item())
+        return {"rows_kept": rows_kept, "touched": touched, "weight_bytes": weight_bytes, "ffn_bytes": ffn_bytes,
+                "ffn_flops": 6.0 * w.h * w.I * rows_kept, "stats": stats,
+                "permute_bytes": (tokens_with_rows + rows_kept) * w.h * ds,
+                "combine_bytes": (rows_kept + w.T) * w.h * ds}
+
+    def cold_copies(self, reps=10):
+        """Permute and combine timed alone (ms, mean of `reps`), L2 flushed by
+        writing 256 MB before every repetition; the layout of the last step."""
+        import torch
+
+        moe, w, o = self.moe, self.w, self.out
+        if self.kind != "layer":
+            return None
+        xp = torch.empty(self.R, w.h, dtype=self.y.dtype, device="cuda")
+        yp = torch.empty_like(xp)
+        y = torch.empty_like(self.y)
+        flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device="cuda")
+        moe.moe_permute(self.cfg, self.inp["x"], o["slot"], o["row_src"], yp)   # expert rows to combine
+        res = {}
+        for name, fn in (("permute", lambda: moe.moe_permute(self.cfg, self.inp["x"], o["slot"], o["row_src"], xp)),
+                         ("combine", lambda: moe.moe_combine(self.cfg, yp, o["slot"], o["topk_w"], y))):
+            times = []
+            for _ in range(reps + 2):
+                flush.fill_(1.0)
+                a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                a.record(self.stream)
+                fn()
+                b.record(self.stream)
+                torch.cuda.synchronize()
+                times.append(a.elapsed_time(b))
+            res[name] = statistics.mean(times[2:])
+        if moe.moe_check() != 0:
+            raise RuntimeError("device error in the cold copies")
+        return res
+
+
+def ffn_roofline(w, work, ffn_ms, peaks, peak_kind):
+    """Roofline of the grouped FFN: HBM (algorithmic bytes / time against the
+    measured copy peak) unless its arithmetic intensity is above the ridge of
+    the measured peaks, then tensor (flops / time against the sustained bf16
+    peak, x2 for FP8)."""
+    hbm = float(peaks["hbm_gbs"])
+    tc_peak = float(peaks["bf16_tflops_sustained"]) * (2.0 if w.fp8 else 1.0)
+    ffn_s = ffn_ms / 1e3
+    gbs = work["ffn_bytes"] / ffn_s / 1e9
+    tflops = work["ffn_flops"] / ffn_s / 1e12
+    tensor_bound = work["ffn_flops"] / work["ffn_bytes"] > tc_peak * 1e12 / (hbm * 1e9)
+    return {"bound": "tensor" if tensor_bound else "hbm",
+            "achieved": tflops if tensor_bound else gbs,
+            "peak": tc_peak if tensor_bound else hbm,
+            "unit": "TFLOP/s" if tensor_bound else "GB/s",
+            "frac": tflops / tc_peak if tensor_bound else gbs / hbm,
+            "peak_source": peak_kind + (" (bf16 sustained" + (" x 2 for FP8" if w.fp8 else "") + ")"
+                                        if tensor_bound else " (HBM copy)"),
+            "achieved_gbs": gbs, "algorithmic_bytes": work["ffn_bytes"], "algorithmic_flops": work["ffn_flops"],
+            "tensor_tflops": tflops, "tensor_frac_of_sustained": tflops / tc_peak}
+
+
+def sweep_entry(w, weights_from, peaks, peak_kind, min_seconds):
+    """One workload of the sweep: its own warm-up, enough timed steps for at
+    least `min_seconds`, the e2e leg, the FFN roofline and clocks."""
+    import torch
+
+    lay = Layer(w, weights_from)
+    t0, _, _, _ = lay.timed(3, 3)
+    steps = int(min(400, max(20, math.ceil(min_seconds * 1e3 / max(t0 / 3, 1e-3)))))
+    total, stages, clocks, launches = lay.timed(steps, 2)
+    e2e_ms, _, _ = lay.e2e(steps, 3)
+    work = lay.work()
+    roof = ffn_roofline(w, work, stages["ffn"], peaks, peak_kind)
+    ent = {"config": workload_config(w), "steps": steps, "ms_per_step": total / steps,
+           "tokens_per_s": w.T * steps / (total / 1e3), "e2e_tokens_per_s": w.T * steps / (e2e_ms / 1e3),
+           "stages_ms": stages, "gpu_launches_per_step": launches / steps,
+           "ffn_roofline": {k: roof[k] for k in ("bound", "achieved", "peak", "unit", "frac", "peak_source")},
+           "clocks": clocks}
+    st = work["stats"]
+    if w.capacity > 0:
+        ent["dropped"] = st["dropped"]
+        ent["kept_rows"] = work["rows_kept"]
+    if w.name.startswith("deepseek_v3_decode"):
+        E, K, T = w.E, w.K, w.T
+        ent["experts_touched"] = work["touched"]
+        ent["experts_touched_frac"] = work["touched"] / E
+        # balls into bins: E (1 - exp(-T K / E)) ("专家并行 / 总览", eq.
+        # par-ep-active-experts, summed over the chips); exact for K distinct
+        # experts per token drawn uniformly: E (1 - (1 - K/E)^T)
+        ent["experts_touched_expected_frac"] = 1.0 - math.exp(-T * K / E)
+        ent["experts_touched_expected_frac_exact"] = 1.0 - (1.0 - K / E) ** T
+        ent["weight_gbs_touched"] = work["weight_bytes"] / (stages["ffn"] / 1e3) / 1e9
+        ent["weight_bytes_touched"] = work["weight_bytes"]
+    del lay
+    torch.cuda.empty_cache()
+    return ent
+
+
+def run_ours(args, rank, world, local_rank):
+    import torch
 
     torch.cuda.set_device(local_rank)
-    w = workloads.ALL.get(args.workload) or workloads.EXTRA[args.workload]
-    cfg = moe.config_from(w)
-    inp = device.layer_inputs(w)
-    dt = inp["x"].dtype
-    R = moe.moe_rows(cfg)
-    T, K, E, N = w.T, w.K, w.E, w.ep_size
-    i32 = dict(dtype=torch.int32, device="cuda")
-    logits = torch.empty(T, E, device="cuda")
-    ids = torch.empty(T, K, **i32)
-    wts = torch.empty(T, K, device="cuda")
-    lay = moe.alloc_layout(cfg)
-    ws_layout = moe.alloc_workspace(cfg, moe.MOE_OP_LAYOUT)
-    ws_ffn = moe.alloc_workspace(cfg, moe.MOE_OP_FFN)
-    ws_logits = moe.alloc_workspace(cfg, moe.MOE_OP_LOGITS)
-    xp = torch.empty(R, w.h, dtype=dt, device="cuda")
-    yp = torch.empty(R, w.h, dtype=dt, device="cuda")
-    y = torch.empty(T, w.h, dtype=dt, device="cuda")
-    stream = torch.cuda.current_stream()
-    shared = w.shared_I > 0  # the whole block: routed layer plus the shared expert
-    if shared:
-        ys = torch.empty(T, w.h, dtype=dt, device="cuda")
-        ws_shared = moe.alloc_workspace(cfg, moe.MOE_OP_SHARED)
-    eplb = w.n_redundant > 0  # replicas: plan once from this batch's logical expert loads (not timed)
-    if eplb:
-        moe.moe_router_logits(cfg, inp["x"], inp["w_r"], inp["logit_offset"], logits, ws_logits)
-        moe.moe_route(cfg, logits, inp["sel_bias"], ids, wts)
-        counts = torch.bincount(ids.view(-1).long(), minlength=E).cpu().numpy()
-        plan_h = moe.moe_eplb_plan(E, N, w.n_redundant, counts)
-        plan = {k: torch.from_numpy(v).cuda() for k, v in plan_h.items() if k != "rank_load"}
-        pids = torch.empty(T, K, **i32)
-    fp8 = w.fp8  # FP8 experts: weights quantised once here (not timed)
-    if fp8:
-        q13 = torch.empty(inp["w13"].shape, dtype=torch.uint8, device="cuda")
-        s13 = torch.empty(E, 2 * w.I, dtype=torch.float32, device="cuda")
-        q2 = torch.empty(inp["w2"].shape, dtype=torch.uint8, device="cuda")
-        s2 = torch.empty(E, w.h, dtype=torch.float32, device="cuda")
-        moe.moe_quantize_fp8(inp["w13"].view(-1, w.h), q13.view(-1, w.h), s13.view(-1))
-        moe.moe_quantize_fp8(inp["w2"].view(-1, w.I), q2.view(-1, w.I), s2.view(-1))
-        del inp["w13"], inp["w2"]
-        torch.cuda.synchronize()
-        xq = torch.empty(R, w.h, dtype=torch.uint8, device="cuda")
-        sxp = torch.empty(R, dtype=torch.float32, device="cuda")
-        ws_ffn = moe.alloc_workspace(cfg, moe.MOE_OP_FFN_FP8)
-    # `--fused-permute`: the FFN gathers its rows from x (moe_grouped_ffn_gather)
-    # instead of the layer's explicit permute
-    gather = args.fused_permute and not fp8 and not eplb
-    stages = (("logits", "route") + (("eplb_map",) if eplb else ()) + ("layout",)
-              + (("ffn",) if gather else ("permute", "ffn")) + (("shared",) if shared else ()) + ("combine",))
-    n_ev = len(stages) + 1
-
-    def step(ev=None):
-        n = [0]
-
-        def rec():
-            if ev is not None:
-                ev[n[0]].record(stream)
-            n[0] += 1
-
-        rec()
-        moe.moe_router_logits(cfg, inp["x"], inp["w_r"], inp["logit_offset"], logits, ws_logits)
-        rec()
-        moe.moe_route(cfg, logits, inp["sel_bias"], ids, wts)
-        rec()
-        lids = ids
-        if eplb:
-            moe.moe_eplb_map(cfg, ids, plan["rep_offsets"], plan["rep_phys"], pids)
-            rec()
-            lids = pids
-        moe.moe_dispatch_layout(cfg, lids, lay.counts, lay.kept, lay.offsets, lay.slot, lay.row_src, lay.n_ij,
-                                lay.rank_bytes, lay.stats, ws_layout)
-        rec()
-        if fp8:
-            moe.moe_permute_fp8(cfg, inp["x"], lay.slot, xq, sxp)
-            rec()
-        elif not gather:
-            moe.moe_permute(cfg, inp["x"], lay.slot, lay.row_src, xp)
-            rec()
-        if fp8:
-            moe.moe_grouped_ffn_fp8(cfg, xq, sxp, lay.offsets, lay.kept, q13, s13, q2, s2, yp, ws_ffn)
-        elif gather:  # the permutation fused into the FFN: rows read from x through row_src
-            moe.moe_grouped_ffn_gather(cfg, inp["x"], lay.row_src, lay.offsets, lay.kept, inp["w13"], inp["w2"],
-                                       yp, ws_ffn)
-        elif eplb:
-            moe.moe_grouped_ffn_mapped(cfg, xp, lay.offsets, lay.kept, plan["phys_to_log"], inp["w13"], inp["w2"],
-                                       yp, ws_ffn)
-        else:
-            moe.moe_grouped_ffn(cfg, xp, lay.offsets, lay.kept, inp["w13"], inp["w2"], yp, ws_ffn)
-        rec()
-        if shared:
-            moe.moe_shared_ffn(cfg, inp["x"], inp["w13s"], inp["w2s"], ys, ws_shared)
-            rec()
-            moe.moe_combine_add(cfg, yp, lay.slot, wts, ys, y)
-        else:
-            moe.moe_combine(cfg, yp, lay.slot, wts, y)
-        rec()
-
-    for _ in range(args.warmup):
-        step()
-    st = moe.moe_check()
-    if st != 0:
-        raise RuntimeError(f"device error during warm-up: {moe.STATUS[st]}")
-    events = [[torch.cuda.Event(enable_timing=True) for _ in range(n_ev)] for _ in range(args.steps)]
-    if world > 1:
-        dist.barrier()
-    torch.cuda.synchronize()
-    launches0 = moe.moe_launch_count()  # the library counts every kernel it launches
-    with ClockSampler(local_rank, args.clocks_csv) as clk:
-        for i in range(args.steps):
-            step(events[i])
-        torch.cuda.synchronize()
-    timed_launches = moe.moe_launch_count() - launches0
-    if world > 1:
-        dist.barrier()
-    st = moe.moe_check()
-    if st != 0:
-        raise RuntimeError(f"device error in the timed region: {moe.STATUS[st]}")
-    total_ms = events[0][0].elapsed_time(events[-1][n_ev - 1])
-    per_stage = {s: statistics.mean(events[i][j].elapsed_time(events[i][j + 1]) for i in range(args.steps))
-                 for j, s in enumerate(stages)}
+    w = find_workload(args.workload)
+    lay = Layer(w)
+    total_ms, stages, clocks, launches = lay.timed(args.steps, args.warmup, world, args.clocks_csv)
     total_ms = max_over_ranks(total_ms, world, "cuda")
-    clocks = clk.summary()
-
-    # ---- end to end through the public call with host buffers.  Two streams
-    # take alternate steps, each with its own workspace and pinned buffers, so
-    # the host<->device copies of one step overlap the compute of the other.
-    op_host = (moe.MOE_OP_BLOCK_HOST if shared else moe.MOE_OP_LAYER if eplb else moe.MOE_OP_LAYER_FP8 if fp8
-               else moe.MOE_OP_LAYER_HOST)
-    dev_io = eplb or fp8  # layer calls that take device activations: copies on the lane's stream around them
-    lanes = [dict(stream=torch.cuda.Stream(), x=inp["x"].cpu().pin_memory(),
-                  y=torch.empty(T, w.h, dtype=dt).pin_memory(), ws=moe.alloc_workspace(cfg, op_host),
-                  xd=torch.empty_like(inp["x"]) if dev_io else None, yd=torch.empty_like(y) if dev_io else None)
-             for _ in range(2)]
-
-    def e2e_step(i):
-        ln = lanes[i % len(lanes)]
-        if fp8:
-            with torch.cuda.stream(ln["stream"]):
-                ln["xd"].copy_(ln["x"], non_blocking=True)
-                moe.moe_layer_forward_fp8(cfg, ln["xd"], inp["w_r"], inp["logit_offset"], inp["sel_bias"], q13, s13,
-                                          q2, s2, ln["yd"], None, ln["ws"], stream=ln["stream"])
-                ln["y"].copy_(ln["yd"], non_blocking=True)
-        elif eplb:
-            with torch.cuda.stream(ln["stream"]):
-                ln["xd"].copy_(ln["x"], non_blocking=True)
-                moe.moe_layer_forward_eplb(cfg, ln["xd"], inp["w_r"], inp["logit_offset"], inp["sel_bias"],
-                                           inp["w13"], inp["w2"], plan["rep_offsets"], plan["rep_phys"],
-                                           plan["phys_to_log"], ln["yd"], None, ln["ws"], stream=ln["stream"])
-                ln["y"].copy_(ln["yd"], non_blocking=True)
-        elif shared:
-            moe.moe_block_forward_host(cfg, ln["x"], inp["w_r"], inp["logit_offset"], inp["sel_bias"], inp["w13"],
-                                       inp["w2"], inp["w13s"], inp["w2s"], ln["y"], ln["ws"], stream=ln["stream"])
-        else:
-            moe.moe_layer_forward_host(cfg, ln["x"], inp["w_r"], inp["logit_offset"], inp["sel_bias"], inp["w13"],
-                                       inp["w2"], ln["y"], ln["ws"], stream=ln["stream"])
-
-    for i in range(max(2, args.warmup)):
-        e2e_step(i)
-    torch.cuda.synchronize()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    if world > 1:
-        dist.barrier()
-    e0.record(stream)
-    for ln in lanes:
-        ln["stream"].wait_event(e0)
-    for i in range(args.steps):
-        e2e_step(i)
-    for ln in lanes:
-        stream.wait_stream(ln["stream"])
-    e1.record(stream)
-    torch.cuda.synchronize()
-    e2e_ms = e0.elapsed_time(e1)
+    e2e_ms, h2d, d2h = lay.e2e(args.steps, args.warmup, world)
     e2e_ms = max_over_ranks(e2e_ms, world, "cuda")
-    if moe.moe_check() != 0:
-        raise RuntimeError("device error in the end-to-end run")
-    if not torch.equal(lanes[0]["y"].to(y.device), y):
-        raise RuntimeError("the end-to-end layer output differs from the device-resident one")
-
+    cold = lay.cold_copies() if rank == 0 else None
     if rank != 0:
-        return None
+        return None, None
 
-    # ---- algorithmic work of the step (from the layout of the last step)
-    kept = lay.kept.cpu().numpy().astype(np.int64)
-    stats = moe.stats_dict(lay.stats)
-    rows_kept = int(kept.sum())
-    ds = 2 if w.dtype == "bf16" else 4
-    touched = int((kept > 0).sum())
-    if eplb:  # replicas share their logical expert's weights: count each touched logical expert once
-        touched = len(set(plan_h["phys_to_log"][kept > 0].tolist()))
-    if fp8:  # E4M3 weights (+ float32 row scales); E4M3 rows in, bf16 intermediate out, re-quantised, bf16 out
-        weight_bytes = touched * (3 * w.h * w.I + 4 * (2 * w.I + w.h))
-        ffn_bytes = weight_bytes + rows_kept * (w.h + 4 + 2 * w.I * 2 + w.I * 2 + 4 + 2 * w.h)
-    else:
-        weight_bytes = touched * 3 * w.h * w.I * ds
-        ffn_bytes = weight_bytes + rows_kept * (2 * w.h + 2 * w.I) * ds
-    ffn_flops = 6.0 * w.h * w.I * rows_kept
-    tokens_with_rows = int((lay.slot.view(T, K) >= 0).any(dim=1).sum().item())
-    permute_bytes = (tokens_with_rows + rows_kept) * w.h * ds  # not moved when the FFN gathers from x
-    combine_bytes = (rows_kept + T) * w.h * ds
+    work = lay.work()
     peaks, peak_kind = measured_peaks()
-    hbm = float(peaks["hbm_gbs"])
-    # FP8 dense tensor peak taken as twice the measured bf16 one (the nominal ratio)
-    tc_peak = float(peaks["bf16_tflops_sustained"]) * (2.0 if fp8 else 1.0)
-    ffn_s = per_stage["ffn"] / 1e3
-    ffn_gbs = ffn_bytes / ffn_s / 1e9
-    # the FFN is compute-bound when its arithmetic intensity is above the ridge of
-    # the measured peaks (Mixtral: ~1000 rows per expert), else bound by HBM
-    tensor_bound = ffn_flops / ffn_bytes > tc_peak * 1e12 / (hbm * 1e9)
+    roof = ffn_roofline(w, work, stages["ffn"], peaks, peak_kind)
     # FFN_TRAFFIC_RATIO was captured on the bf16 weights-as-M kernel (experts
     # expected to see at most 160 rows); other variants report no traffic
-    expected_rows = (min(w.capacity, T) if w.capacity > 0 else -(-T * K // (E + w.n_redundant)))
-    traffic_known = not fp8 and w.dtype == "bf16" and expected_rows <= 160
-    ffn_tflops = ffn_flops / ffn_s / 1e12
+    expected_rows = (min(w.capacity, w.T) if w.capacity > 0 else -(-w.T * w.K // (w.E + w.n_redundant)))
+    traffic_known = not w.fp8 and w.dtype == "bf16" and expected_rows <= 160
+    roof = {"kernel": "grouped SwiGLU FFN (gate/up + down tcgen05 GEMMs)", **roof,
+            "traffic": FFN_TRAFFIC_RATIO * work["ffn_bytes"] if traffic_known else None,
+            "traffic_source": ("ncu DRAM bytes / algorithmic bytes on deepseek_v3_e32_T512, scaled to this "
+                               "launch's algorithmic bytes") if traffic_known else
+                              "not captured for this FFN variant since its last change"}
     ms = total_ms / args.steps
+    st = work["stats"]
     out = {
         "metric": METRIC,
-        "value": job_throughput(T, world, args.steps, total_ms),
+        "value": job_throughput(w.T, world, args.steps, total_ms),
         "unit": "tokens/s",
         "n_gpus": world,
         "steps": args.steps,
@@ -371,36 +516,49 @@ def run_ours(args, rank, world, local_rank):
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
-        "dtype": "e4m3" if fp8 else w.dtype,
+        "dtype": "e4m3" if w.fp8 else w.dtype,
         "data": "synthetic: seeded counter-based generator (x~N(0,1), weights~N(0,1/h)), no dataset",
         "config": workload_config(w),
-        "e2e": {"value": job_throughput(T, world, args.steps, e2e_ms), "unit": "tokens/s",
-                "h2d_bytes_per_step": T * w.h * ds, "d2h_bytes_per_step": T * w.h * ds},
-        "gpu_launches": timed_launches,
-        "roofline": {"kernel": "grouped SwiGLU FFN (gate/up + down tcgen05 GEMMs)",
-                     "bound": "tensor" if tensor_bound else "hbm",
-                     "achieved": ffn_tflops if tensor_bound else ffn_gbs,
-                     "peak": tc_peak if tensor_bound else hbm,
-                     "unit": "TFLOP/s" if tensor_bound else "GB/s",
-                     "frac": ffn_tflops / tc_peak if tensor_bound else ffn_gbs / hbm,
-                     "peak_source": peak_kind + (" (bf16 sustained" + (" x 2 for FP8" if fp8 else "") + ")"
-                                                 if tensor_bound else " (HBM copy)"),
-                     "achieved_gbs": ffn_gbs, "algorithmic_bytes": ffn_bytes, "algorithmic_flops": ffn_flops,
-                     "traffic": FFN_TRAFFIC_RATIO * ffn_bytes if traffic_known else None,
-                     "traffic_source": ("ncu DRAM bytes / algorithmic bytes on deepseek_v3_e32_T512, scaled to this "
-                                        "launch's algorithmic bytes") if traffic_known else
-                                       "not captured for this FFN variant since its last change",
-                     "tensor_tflops": ffn_tflops,
-                     "tensor_frac_of_sustained": ffn_tflops / tc_peak},
-        "stages_ms": per_stage,
-        "permute_gbs": permute_bytes / (per_stage["permute"] / 1e3) / 1e9 if "permute" in per_stage else None,
-        "permute_fused_into_ffn": gather,
-        "combine_gbs": combine_bytes / (per_stage["combine"] / 1e3) / 1e9,
-        "layout": {"dropped": stats["dropped"], "experts_touched": stats["experts_touched"],
-                   "balancedness": stats["balancedness"], "offdiag_rows": stats["offdiag_rows"]},
+        "e2e": {"value": job_throughput(w.T, world, args.steps, e2e_ms), "unit": "tokens/s",
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "gpu_launches": launches,
+        "step_call": "one library call per step (" + {"layer": "moe_layer_forward", "block": "moe_block_forward",
+                                                       "eplb": "moe_layer_forward_eplb",
+                                                       "fp8": "moe_layer_forward_fp8"}[lay.kind]
+                     + "), stage times from the events it records between its stages",
+        "roofline": roof,
+        "stages_ms": stages,
+        "permute_gbs": work["permute_bytes"] / (stages["permute"] / 1e3) / 1e9 if stages["permute"] > 0 else None,
+        "combine_gbs": work["combine_bytes"] / (stages["combine"] / 1e3) / 1e9,
+        "layout": {"dropped": st["dropped"], "experts_touched": st["experts_touched"],
+                   "balancedness": st["balancedness"], "offdiag_rows": st["offdiag_rows"]},
         "clocks": clocks,
     }
-    return out
+    if cold is not None:
+        out["copies"] = {
+            "warm": {"permute_gbs": out["permute_gbs"], "combine_gbs": out["combine_gbs"],
+                     "note": "in the step: x was just read by the router logits, so part of it is in L2"},
+            "cold": {"permute_gbs": work["permute_bytes"] / (cold["permute"] / 1e3) / 1e9,
+                     "combine_gbs": work["combine_bytes"] / (cold["combine"] / 1e3) / 1e9,
+                     "permute_ms": cold["permute"], "combine_ms": cold["combine"],
+                     "note": "each call alone, 256 MB written before every repetition to flush L2"}}
+    return out, lay
+
+
+def run_sweep(args, headline_layer, peaks, peak_kind):
+    """The pages' other workloads, each measured the same way as the headline."""
+    import torch
+
+    res = {}
+    base = headline_layer.inp if headline_layer.w.name == "deepseek_v3" else None
+    for name in SWEEP:
+        if name == args.workload:
+            continue
+        w = find_workload(name)
+        reuse = base if (base is not None and name.startswith("deepseek_v3_decode")) else None
+        res[name] = sweep_entry(w, reuse, peaks, peak_kind, args.sweep_seconds)
+        torch.cuda.empty_cache()
+    return res
 
 
 # ---------------------------------------------------------------------------- the oracle (CPU)
@@ -413,10 +571,24 @@ def blas_threads():
         return os.cpu_count()
 
 
+def host_cpu():
+    model = platform.processor() or "unknown"
+    try:
+        for line in open("/proc/cpuinfo"):
+            if line.startswith("model name"):
+                model = line.split(":", 1)[1].strip()
+                break
+    except OSError:
+        pass
+    return {"nproc": len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count(),
+            "cpu_model": model}
+
+
 def oracle_sample_time(w, sample_tokens: int, seed: int):
     """Seconds the oracle takes for the whole index path on all T tokens plus the
     FFN and combine of ``sample_tokens`` tokens, and the tokens/s extrapolated
-    from that sample.  Input generation (synth) is outside the timed parts."""
+    from that sample.  Input generation (synth) is outside the timed parts.
+    Also returns the oracle's routing of every token (ids, near-tie margins)."""
     import numpy as np
 
     import oracle
@@ -428,7 +600,7 @@ def oracle_sample_time(w, sample_tokens: int, seed: int):
     off = workloads.host_logit_offset(w)
     t0 = time.perf_counter()
     L = oracle.router_logits(x, wr, w.dtype, off)
-    ids, wts, _, _ = oracle.route(L, w, bias)
+    ids, wts, keys, allowed = oracle.route(L, w, bias)
     lay = oracle.dispatch_layout(ids, w)
     t_index = time.perf_counter() - t0
     rng = np.random.default_rng(seed)
@@ -458,13 +630,25 @@ def oracle_sample_time(w, sample_tokens: int, seed: int):
         oracle.combine(yp, lay["slot"], wts, w, tokens=list(tokens))
     t_sample = time.perf_counter() - t1
     total = t_index + t_sample * (w.T / len(tokens))
-    return {"value": w.T / total, "index_s": t_index, "sample_s": t_sample, "tokens": len(tokens)}
+    return {"value": w.T / total, "index_s": t_index, "sample_s": t_sample, "tokens": len(tokens),
+            "experts": len(need), "ids": ids, "margin": oracle.near_tie_margin(keys, allowed, w)}
+
+
+def routing_report(gpu_ids, ref):
+    """Tokens the GPU routed differently from the oracle (same seeded inputs),
+    against the oracle's near-ties (relative key gap < 1e-4)."""
+    import numpy as np
+
+    diff = (np.asarray(gpu_ids) != ref["ids"]).any(axis=1)
+    near = ref["margin"] < 1e-4
+    return {"tokens": int(len(diff)), "near_tie_tokens": int(near.sum()), "mismatched_tokens": int(diff.sum()),
+            "mismatched_away_from_near_tie": int((diff & ~near).sum()),
+            "rule": "a token may route differently from the oracle only where its keys nearly tie "
+                    "(relative gap < 1e-4 between adjacent keys of the top K+1 or at the group boundary)"}
 
 
 def run_reference(args):
-    from synth import workloads
-
-    w = workloads.ALL.get(args.workload) or workloads.EXTRA[args.workload]
+    w = find_workload(args.workload)
     vals = []
     for i in range(args.warmup + args.steps):
         r = oracle_sample_time(w, args.ref_sample, seed=i)
@@ -478,7 +662,7 @@ def run_reference(args):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * w.T / v, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic (same generator as ours)",
         "config": workload_config(w),
-        "cpu_baseline": {"value": v, "unit": "tokens/s", "cores": blas_threads(), "kind": "oracle",
+        "cpu_baseline": {"value": v, "unit": "tokens/s", "cores": blas_threads(), **host_cpu(), "kind": "oracle",
                          "sample": sample},
         "e2e": {"value": v, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
@@ -487,16 +671,16 @@ def run_reference(args):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=100)
+    ap.add_argument("--steps", type=int, default=120)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--workload", default="deepseek_v3")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--ref-sample", type=int, default=1, help="tokens whose FFN the oracle evaluates per step")
-    ap.add_argument("--cpu-sample", type=int, default=8, help="tokens in the cpu_baseline sample")
+    ap.add_argument("--cpu-sample", type=int, default=24, help="tokens in the cpu_baseline sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--clocks-csv", default=None, help="where to keep the nvidia-smi samples of the timed region")
-    ap.add_argument("--fused-permute", action="store_true",
-                    help="gather the FFN's rows from x instead of permuting (bf16 weights-as-M layers)")
+    ap.add_argument("--no-sweep", action="store_true", help="measure the headline workload only")
+    ap.add_argument("--sweep-seconds", type=float, default=0.3, help="timed seconds per sweep workload")
+    ap.add_argument("--clocks-csv", default=None, help="where to keep the clock samples of the timed region")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3) if args.impl == "ours" else args.warmup
 
@@ -514,17 +698,21 @@ def main():
         import torch.distributed as dist
         torch.cuda.set_device(local_rank)
         dist.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
-    out = run_ours(args, rank, world, local_rank)
+    out, lay = run_ours(args, rank, world, local_rank)
     if rank == 0 and out is not None:
+        if world == 1 and not args.no_sweep:
+            peaks, peak_kind = measured_peaks()
+            out["workloads"] = run_sweep(args, lay, peaks, peak_kind)
         if world == 1 and not args.no_cpu_baseline:
-            from synth import workloads
-            w = workloads.ALL.get(args.workload) or workloads.EXTRA[args.workload]
+            w = find_workload(args.workload)
+            gpu_ids = lay.out["topk_ids"].cpu().numpy()
             r = oracle_sample_time(w, args.cpu_sample, seed=1234)
             out["cpu_baseline"] = {
-                "value": r["value"], "unit": "tokens/s", "cores": blas_threads(), "kind": "oracle",
+                "value": r["value"], "unit": "tokens/s", "cores": blas_threads(), **host_cpu(), "kind": "oracle",
                 "sample": (f"routing, layout and index outputs for all tokens ({r['index_s']:.1f} s) plus FFN and "
-                           f"combine of {r['tokens']} random tokens ({r['sample_s']:.1f} s), extrapolated to the "
-                           f"full batch")}
+                           f"combine of {r['tokens']} random tokens touching {r['experts']} experts "
+                           f"({r['sample_s']:.1f} s), extrapolated to the full batch")}
+            out["routing"] = routing_report(gpu_ids, r)
         print(json.dumps(out), flush=True)
     if world > 1:
         import torch.distributed as dist

@@ -5,7 +5,7 @@ its ctypes binding plus buffer helpers.  PyTorch supplies device memory and
 streams only.
 """
 from ._lib import (  # noqa: F401
-    EXPORTS, LIB_PATH, MOE_BF16, MOE_F32, MOE_OP_BLOCK, MOE_OP_BLOCK_HOST, MOE_OP_FFN, MOE_OP_FFN_FP8,
+    EXPORTS, LAYER_STAGES, LIB_PATH, MOE_BF16, MOE_F32, MOE_OP_BLOCK, MOE_OP_BLOCK_HOST, MOE_OP_FFN, MOE_OP_FFN_FP8,
     MOE_OP_LAYER, MOE_OP_LAYER_FP8, MOE_OP_LOGITS, moe_grouped_ffn_fp8, moe_grouped_ffn_gather, moe_launch_count, moe_layer_forward_fp8, moe_permute_fp8, moe_quantize_fp8,
     MOE_OP_LAYER_HOST, MOE_OP_LAYOUT, MOE_OP_SHARED, MOE_SIGMOID, MOE_SOFTMAX, STATUS, MoeConfig, MoeError,
     MoeLayerOut, MoeLayoutStats, config_from, layer_out, lib, make_config, moe_block_forward,

@@ -63,7 +63,11 @@ class MoeLayoutStats(ctypes.Structure):
 
 class MoeLayerOut(ctypes.Structure):
     _fields_ = [(n, c_void_p) for n in ("logits", "topk_ids", "topk_w", "counts", "kept", "offsets", "slot",
-                                         "row_src", "n_ij", "rank_bytes", "stats")]
+                                         "row_src", "n_ij", "rank_bytes", "stats", "stage_events")]
+
+
+# Stages of the layer calls (moe_layer_stage); stage_events holds one event more.
+LAYER_STAGES = ("logits", "route", "eplb_map", "layout", "permute", "ffn", "shared", "combine")
 
 
 def _load() -> ctypes.CDLL:
@@ -342,8 +346,19 @@ def moe_launch_count() -> int:
     return int(lib.moe_launch_count())
 
 
-def layer_out(**tensors) -> MoeLayerOut:
+def layer_out(stage_events=None, **tensors) -> MoeLayerOut:
+    """Optional outputs of the layer calls.  ``stage_events``: MOE_LAYER_STAGES + 1
+    torch.cuda.Event objects, each already recorded once (torch creates the
+    CUDA event on its first record); the layer records them around its stages."""
     o = MoeLayerOut()
     for k, v in tensors.items():
         setattr(o, k, _ptr(v))
+    if stage_events is not None:
+        if len(stage_events) != len(LAYER_STAGES) + 1:
+            raise ValueError(f"stage_events needs {len(LAYER_STAGES) + 1} events")
+        handles = [e.cuda_event for e in stage_events]
+        if not all(handles):
+            raise ValueError("record every stage event once before passing it (torch creates it lazily)")
+        o._events = (c_void_p * len(handles))(*handles)   # kept alive with the struct
+        o.stage_events = ctypes.cast(o._events, c_void_p)
     return o

@@ -108,8 +108,30 @@ typedef struct moe_layout_stats {
   float balancedness;       /* sum_j recv_j / (N_EP * max_j recv_j); 1 if nothing received */
 } moe_layout_stats;
 
+/* Stages of the layer calls, in execution order.  A stage a configuration does
+ * not have (the replica map without replicas, the shared expert outside the
+ * block) takes no time. */
+enum moe_layer_stage {
+  MOE_STAGE_LOGITS = 0,
+  MOE_STAGE_ROUTE = 1,
+  MOE_STAGE_EPLB_MAP = 2,
+  MOE_STAGE_LAYOUT = 3,
+  MOE_STAGE_PERMUTE = 4,
+  MOE_STAGE_FFN = 5,
+  MOE_STAGE_SHARED = 6,
+  MOE_STAGE_COMBINE = 7,
+  MOE_LAYER_STAGES = 8
+};
+
 /* Optional device outputs of moe_layer_forward.  Any NULL member is kept in the
- * workspace instead.  Shapes as in the individual calls below. */
+ * workspace instead.  Shapes as in the individual calls below.
+ *
+ * stage_events: NULL, or MOE_LAYER_STAGES + 1 cudaEvent_t handles (created by
+ * the caller, owned by the caller).  The layer records stage_events[0] on its
+ * stream before its first kernel and stage_events[s + 1] after stage s
+ * (moe_layer_stage), so cudaEventElapsedTime(stage_events[s],
+ * stage_events[s + 1]) is the device time of stage s inside the one call.
+ * Ignored by the host-buffer calls. */
 typedef struct moe_layer_out {
   float* logits;            /* [T, E] */
   int32_t* topk_ids;        /* [T, K] */
@@ -122,6 +144,7 @@ typedef struct moe_layer_out {
   int64_t* n_ij;            /* [N_EP, N_EP] */
   int64_t* rank_bytes;      /* [2, N_EP]: sent then received bytes per chip */
   moe_layout_stats* stats;  /* [1] */
+  void* const* stage_events; /* [MOE_LAYER_STAGES + 1] cudaEvent_t, or NULL */
 } moe_layer_out;
 
 /* Human-readable name of a status code (static string). */
