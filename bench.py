@@ -106,6 +106,55 @@ REASON_BITS = {"hw_slowdown": 0x8, "hw_thermal_slowdown": 0x40, "sw_thermal_slow
                "sw_power_cap": 0x4}
 
 
+class Nvml:
+    """Read-only NVML queries through the driver's libnvidia-ml (ctypes): SM
+    clock, its maximum, power draw and the active clock-event reasons."""
+
+    CLOCK_SM = 1
+
+    def __init__(self):
+        import ctypes
+        self.c = ctypes
+        self.lib = ctypes.CDLL("libnvidia-ml.so.1")
+        self._ok(self.lib.nvmlInit_v2(), "nvmlInit_v2")
+        fn = getattr(self.lib, "nvmlDeviceGetCurrentClocksEventReasons", None)
+        self._reasons = fn if fn is not None else self.lib.nvmlDeviceGetCurrentClocksThrottleReasons
+
+    @staticmethod
+    def _ok(rc, what):
+        if rc != 0:
+            raise RuntimeError(f"{what}: NVML error {rc}")
+
+    def handle_by_uuid(self, uuid):
+        h = self.c.c_void_p()
+        self._ok(self.lib.nvmlDeviceGetHandleByUUID(self.c.c_char_p(uuid.encode()), self.c.byref(h)), "by uuid")
+        return h
+
+    def handle_by_index(self, index):
+        h = self.c.c_void_p()
+        self._ok(self.lib.nvmlDeviceGetHandleByIndex_v2(self.c.c_uint(index), self.c.byref(h)), "by index")
+        return h
+
+    def _uint(self, fn, *args):
+        v = self.c.c_uint()
+        self._ok(fn(*args, self.c.byref(v)), fn.__name__)
+        return v.value
+
+    def sm_clock(self, h):
+        return self._uint(self.lib.nvmlDeviceGetClockInfo, h, self.c.c_int(self.CLOCK_SM))
+
+    def max_sm_clock(self, h):
+        return self._uint(self.lib.nvmlDeviceGetMaxClockInfo, h, self.c.c_int(self.CLOCK_SM))
+
+    def power_w(self, h):
+        return self._uint(self.lib.nvmlDeviceGetPowerUsage, h) / 1e3
+
+    def reasons(self, h):
+        v = self.c.c_ulonglong()
+        self._ok(self._reasons(h, self.c.byref(v)), "clock event reasons")
+        return int(v.value)
+
+
 class ClockSampler:
     """Samples the SM clock, power and clock-event reasons of one GPU while the
     timed region runs: through NVML every `period_s` (read-only queries), or
@@ -120,32 +169,27 @@ class ClockSampler:
         self._stop = threading.Event()
 
     def _nvml_handle(self):
-        import pynvml
-        import torch
-        pynvml.nvmlInit()
+        nv = Nvml()
         try:
-            uuid = str(torch.cuda.get_device_properties(self.index).uuid)
-            return pynvml.nvmlDeviceGetHandleByUUID("GPU-" + uuid)
+            import torch
+            return nv, nv.handle_by_uuid("GPU-" + str(torch.cuda.get_device_properties(self.index).uuid))
         except Exception:  # noqa: BLE001
-            return pynvml.nvmlDeviceGetHandleByIndex(self.index)
+            return nv, nv.handle_by_index(self.index)
 
-    def _loop(self, h):
-        import pynvml
-        mx = pynvml.nvmlDeviceGetMaxClockInfo(h, pynvml.NVML_CLOCK_SM)
+    def _loop(self, nv, h):
+        mx = nv.max_sm_clock(h)
         while not self._stop.is_set():
             try:
-                self.rows.append((float(pynvml.nvmlDeviceGetClockInfo(h, pynvml.NVML_CLOCK_SM)), float(mx),
-                                  pynvml.nvmlDeviceGetPowerUsage(h) / 1e3,
-                                  int(pynvml.nvmlDeviceGetCurrentClocksEventReasons(h))))
+                self.rows.append((float(nv.sm_clock(h)), float(mx), nv.power_w(h), nv.reasons(h)))
             except Exception:  # noqa: BLE001
                 pass
             time.sleep(self.period)
 
     def __enter__(self):
         try:
-            h = self._nvml_handle()
+            nv, h = self._nvml_handle()
             self.kind = f"nvml every {self.period * 1e3:.0f} ms"
-            self.thread = threading.Thread(target=self._loop, args=(h,), daemon=True)
+            self.thread = threading.Thread(target=self._loop, args=(nv, h), daemon=True)
             self.thread.start()
         except Exception as e:  # noqa: BLE001
             self.kind = f"nvidia-smi every 100 ms (NVML unavailable: {type(e).__name__}: {e})"

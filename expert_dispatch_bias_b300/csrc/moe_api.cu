@@ -506,7 +506,7 @@ moe_status make_tensor_map(CUtensorMap* map, const void* base, uint64_t inner, u
 // 1: the weights-as-M FFN runs on SM pairs (ffn_pair.cuh); 0: one SM per tile
 // (ffn_grouped.cuh).
 #ifndef MOE_FFN_PAIR
-#define MOE_FFN_PAIR 1
+#define MOE_FFN_PAIR 0
 #endif
 
 // The grouped FFN with token rows as M (128-row m-blocks of an expert's
