@@ -23,7 +23,6 @@
 #include "simt_gemm.cuh"
 #include "tc_gemm.cuh"
 #include "ffn_grouped.cuh"
-#include "ffn_pair.cuh"
 #include "fp8.cuh"
 
 using namespace moe;
@@ -503,11 +502,6 @@ moe_status make_tensor_map(CUtensorMap* map, const void* base, uint64_t inner, u
 #ifndef MOE_FFN_SWAP_MAX_ROWS
 #define MOE_FFN_SWAP_MAX_ROWS 160
 #endif
-// 1: the weights-as-M FFN runs on SM pairs (ffn_pair.cuh); 0: one SM per tile
-// (ffn_grouped.cuh).
-#ifndef MOE_FFN_PAIR
-#define MOE_FFN_PAIR 0
-#endif
 
 // The grouped FFN with token rows as M (128-row m-blocks of an expert's
 // segment) and weight rows as N (256 columns: 128 gate + 128 up units, or 256
@@ -619,79 +613,6 @@ moe_status launch_ffn_grouped(const moe_config& c, const void* xp, const int32_t
   return MOE_OK;
 }
 
-// The grouped FFN on SM pairs (ffn_pair.cuh): token tiles of up to 256 rows
-// split between the two CTAs of a cluster, a ring of 4 stages of 32 KB of
-// weights plus 16 KB of token rows per CTA.
-constexpr int kFpTileRows = 256, kFpStages = 4;
-
-// Clusters of two that can be resident at once (one CTA per SM): the grid of
-// the persistent pair kernels.  Looked up once per kernel and device.
-template <typename Kern>
-int pair_clusters(Kern kernel, size_t smem) {
-  static std::atomic<int> cache[64];
-  int dev = 0;
-  cudaGetDevice(&dev);
-  if (dev < 0 || dev >= 64) dev = 0;
-  int n = cache[dev].load(std::memory_order_relaxed);
-  if (n > 0) return n;
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(2 * (unsigned)device_info().sms, 1, 1);
-  cfg.blockDim = dim3(kFpThreads, 1, 1);
-  cfg.dynamicSmemBytes = smem;
-  if (cudaOccupancyMaxActiveClusters(&n, kernel, &cfg) != cudaSuccess || n < 1) {
-    (void)cudaGetLastError();
-    n = device_info().sms / 2;   // one CTA per SM fits by construction
-  }
-  cache[dev].store(n, std::memory_order_relaxed);
-  return n;
-}
-
-template <int BT, int S>
-moe_status launch_ffn_pair(const moe_config& c, const void* xp, const int32_t* offsets, const int32_t* kept,
-                           const int32_t* w_map, int n_w, const void* w13, const void* w2, void* yp, void* inter,
-                           cudaStream_t st) {
-  using SH = FpShape<BT, S>;
-  const int64_t R = rows_of(c);
-  CUtensorMap w1m, w2m;
-  FgTokenMaps x1, x2;
-  MOE_TRY(make_tensor_map(&w1m, w13, c.h, (uint64_t)n_w * 2 * c.I, 128));
-  MOE_TRY(make_tensor_map(&w2m, w2, c.I, (uint64_t)n_w * c.h, 128));
-  for (int i = 0; i < 4; ++i) {
-    MOE_TRY(make_tensor_map(&x1.m[i], xp, c.h, R, 128u >> i));
-    MOE_TRY(make_tensor_map(&x2.m[i], inter, c.I, R, 128u >> i));
-  }
-  FgParams p1{};
-  p1.offsets = offsets;
-  p1.kept = kept;
-  p1.E = nphys(c);
-  p1.w_map = w_map;
-  p1.f_tiles = (c.I + 127) / 128;
-  p1.k_blocks = c.h / kTcBK;
-  p1.a_rows = 2LL * c.I;
-  p1.up_rows = c.I;
-  p1.n_valid = c.I;
-  p1.out = static_cast<__nv_bfloat16*>(inter);
-  p1.ldo = c.I;
-  FgParams p2 = p1;
-  p2.f_tiles = (c.h + 255) / 256;
-  p2.k_blocks = c.I / kTcBK;
-  p2.a_rows = c.h;
-  p2.up_rows = 0;
-  p2.n_valid = c.h;
-  p2.out = static_cast<__nv_bfloat16*>(yp);
-  p2.ldo = c.h;
-  auto k1 = ffn_pair_kernel<kTcSwiglu, BT, S>;
-  auto k2 = ffn_pair_kernel<kTcStore, BT, S>;
-  CUDA_TRY(allow_smem(k1, SH::kDynSmem));
-  CUDA_TRY(allow_smem(k2, SH::kDynSmem));
-  const int g1 = 2 * pair_clusters(k1, SH::kDynSmem), g2 = 2 * pair_clusters(k2, SH::kDynSmem);
-  k1<<<g1, kFpThreads, SH::kDynSmem, st>>>(w1m, x1, p1);
-  CUDA_TRY(launched());
-  k2<<<g2, kFpThreads, SH::kDynSmem, st>>>(w2m, x2, p2);
-  CUDA_TRY(launched());
-  return MOE_OK;
-}
-
 // Rows an expert is expected to receive: the capacity when there is one, else
 // the mean T*K/E.
 int64_t expected_rows_per_expert(const moe_config& c) {
@@ -708,11 +629,7 @@ moe_status launch_ffn_tc(const moe_config& c, const void* xp, const int32_t* off
   if ((int64_t)n_w * 2 * c.I >= INT32_MAX || (int64_t)n_w * c.h >= INT32_MAX) return MOE_ERR_UNSUPPORTED;
   if (expected_rows_per_expert(c) > MOE_FFN_SWAP_MAX_ROWS)
     return launch_ffn_tokens_m(c, xp, offsets, kept, w_map, n_w, w13, w2, yp, inter, st);
-#if MOE_FFN_PAIR
-  return launch_ffn_pair<kFpTileRows, kFpStages>(c, xp, offsets, kept, w_map, n_w, w13, w2, yp, inter, st);
-#else
   return launch_ffn_grouped<kFgTileRows, kFgWStages, kFgXStages>(c, xp, offsets, kept, w_map, n_w, w13, w2, yp, inter, st);
-#endif
 }
 
 // Router logits of a bf16 layer on the tensor cores: one segment of T rows

@@ -86,13 +86,12 @@ def test_ffn_full_size_sampled_experts(name):
 
 # Expert row counts straddling every boundary of the token tiles (sub-blocks of
 # at most 128 rows, MMA widths rounded to 16, tiles of 128, 160 or 256 rows
-# chosen from the mean rows per expert, longer segments split evenly).  "pair":
-# the boundaries of the SM-pair kernel (MMA width rounded to 32, each CTA
-# loading half of it in boxes of 128/64/32/16 rows, one or both TMEM slots,
-# tiles of up to 256 rows); the empty experts keep the mean rows per expert in
-# the weights-as-M regime.
+# chosen from the mean rows per expert, longer segments split evenly).
+# "wide": more boundaries of the weights-as-M kernel (multiples of 32 and their
+# neighbours, tiles split in two and three); the empty experts keep the mean
+# rows per expert in the weights-as-M regime.
 BOUNDARY_COUNTS = {
-    "pair": [0, 1, 31, 32, 33, 63, 64, 65, 96, 97, 128, 129, 160, 192, 193, 224, 255, 256, 257, 320, 511, 512, 513,
+    "wide": [0, 1, 31, 32, 33, 63, 64, 65, 96, 97, 128, 129, 160, 192, 193, 224, 255, 256, 257, 320, 511, 512, 513,
              700] + [0] * 8,
     "tile128": [0, 1, 15, 16, 17, 33, 64, 127, 128, 129, 200],
     "tile160": [0, 1, 15, 16, 17, 127, 128, 129, 144, 160, 161, 255, 256, 257, 300, 511],
