@@ -27,7 +27,10 @@
 //   warp 0      one thread issues the TMA loads of the two 128x64 weight boxes
 //               of every k-block into a WS-deep weight ring;
 //   warp 6      issues the loads of the tile's token rows (boxes of 128, 64, 32
-//               and 16 rows, or four-row gathers) into an XS-deep token ring;
+//               and 16 rows) into an XS-deep token ring; when the rows are
+//               gathered from x (GATHER), warps 6..6+XS-1 each own one token
+//               stage and fill it with 16-byte cp.async copies of the rows
+//               that row_src names;
 //   warp 1      allocates 512 TMEM columns; one thread issues tcgen05.mma
 //               (M=128, N = the tile's rows rounded up to 16, K=16), two per
 //               k-step, once both rings hold the k-block;
@@ -48,6 +51,13 @@
 namespace moe {
 
 constexpr int kFgThreads = 224;
+
+// Threads of a grouped-FFN CTA: 7 warps, plus XS - 1 more when the token rows
+// are gathered (one gather warp per token stage).
+template <bool GATHER, int XS>
+struct FgThreads {
+  static constexpr int value = GATHER ? kFgThreads + 32 * (XS - 1) : kFgThreads;
+};
 constexpr int kFgXsStride = 40;  // bf16 per row of a warp's 32x32 transpose buffer (80 B: conflict-free 16-B reads)
 
 template <int BT, int WS, int XS>
@@ -76,6 +86,8 @@ struct FgParams {
   const float* w_scale;     // FP8: scale of every weight row [experts * a_rows]
   const float* x_scale;     // FP8: scale of every token row [R]
   const int32_t* row_src;   // gather: token of every permuted row [R] (rows are read from x)
+  const uint8_t* gather_x;  // gather: x [T, ldx_bytes]
+  int64_t ldx_bytes;        // gather: bytes per row of x
 };
 
 // Tensor maps of the token rows with boxes of 128, 64, 32 and 16 rows.
@@ -113,15 +125,9 @@ __device__ __forceinline__ FgTile fg_decode(int t, const int32_t* mbp, const FgP
 
 __device__ __forceinline__ uint32_t round16(int n) { return (uint32_t)((n + 15) & ~15); }
 
-// Four rows y0..y3 (one-row box of the map, 128 bytes each) of a 2-D tensor
-// at column x into consecutive 128-byte rows of shared memory.
-__device__ __forceinline__ void tma_gather4(void* smem_dst, const CUtensorMap* map, int x, int y0, int y1, int y2,
-                                            int y3, uint64_t* bar) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes [%0], [%1, {%2, "
-      "%3, %4, %5, %6}], [%7];" ::"r"(smem_u32(smem_dst)),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y0), "r"(y1), "r"(y2), "r"(y3), "r"(smem_u32(bar))
-      : "memory");
+// 16-byte copy global -> shared through the LSU path (L1 bypassed).
+__device__ __forceinline__ void cp_async16(uint32_t smem_dst, const void* gsrc) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_dst), "l"(gsrc) : "memory");
 }
 
 // Epilogue of one 32-token chunk: v (and u, SwiGLU) hold this warp's 32
@@ -194,10 +200,13 @@ __device__ __forceinline__ void fg_drain(uint32_t t_lane, uint32_t col0, uint32_
 
 // FP8: E4M3 operands (tcgen05.mma kind::f8f6f4), 128-element k-blocks (the
 // same 128-byte rows), results scaled by weight-row and token scales.
-// GATHER: the token rows are read straight from x through row_src (tile::gather4
-// of a one-row box), so the permutation needs no buffer of its own.
+// GATHER: the token rows are read straight from x through row_src, so the
+// permutation needs no buffer of its own.  Warp 6 + g fills token stage g with
+// 16-byte cp.async copies into the 128-byte-swizzled layout the MMA expects,
+// waits for its own copies, makes them visible to the tensor core's (async
+// proxy) reads with fence.proxy.async, and then arrives on the stage's barrier.
 template <int EPI, int BT, int WS, int XS, bool FP8 = false, bool GATHER = false>
-__global__ void __launch_bounds__(kFgThreads, 1)
+__global__ void __launch_bounds__(FgThreads<GATHER, XS>::value, 1)
     ffn_grouped_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_constant__ FgTokenMaps maps,
                        FgParams p) {
   const CUtensorMap* map_x = maps.m;
@@ -209,7 +218,7 @@ __global__ void __launch_bounds__(kFgThreads, 1)
   __shared__ volatile uint32_t abort_flag;
   __shared__ int32_t mbp[1025];
   __shared__ int32_t scan_scratch[33];
-  __shared__ int32_t src_rows[GATHER ? BT : 1];  // gather: source token of each row of the current tile
+  __shared__ int32_t src_rows[GATHER ? XS : 1][GATHER ? BT : 1];  // gather: per warp, source token of each row
 
   uint8_t* ring_w = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(dyn_smem) + 1023) & ~uintptr_t(1023));
   uint8_t* ring_x = ring_w + (size_t)WS * S::kWStage;
@@ -217,7 +226,8 @@ __global__ void __launch_bounds__(kFgThreads, 1)
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
   // ---- per-expert token-tile prefix (every CTA computes it from kept)
-  for (int e = tid; e < p.E; e += kFgThreads) mbp[e] = (p.kept[e] + BT - 1) / BT;
+  constexpr int NT = FgThreads<GATHER, XS>::value;
+  for (int e = tid; e < p.E; e += NT) mbp[e] = (p.kept[e] + BT - 1) / BT;
   __syncthreads();
   const int32_t total_tt = block_exclusive_scan(mbp, p.E, scan_scratch);
   if (tid == 0) mbp[p.E] = total_tt;
@@ -229,7 +239,7 @@ __global__ void __launch_bounds__(kFgThreads, 1)
       mbar_init(&wempty[s], 1);
     }
     for (int s = 0; s < XS; ++s) {
-      mbar_init(&xfull[s], 1);
+      mbar_init(&xfull[s], GATHER ? 32 : 1);   // gather: every lane of the stage's warp arrives
       mbar_init(&xempty[s], 1);
     }
     for (int a = 0; a < 2; ++a) {
@@ -287,69 +297,96 @@ __global__ void __launch_bounds__(kFgThreads, 1)
           if ((armed >> s) & 1u) mbar_wait(&wfull[s], (armed_parity >> s) & 1u);
       }
     }
-  } else if (warp == 6) {
+  } else if (!GATHER && warp == 6) {
     // ------------------------------------------------------------ token producer
-    // Lane 0 arms each stage; the copies are issued by lane 0 (boxes) or by
-    // every lane (GATHER, after the warp staged the tile's source rows).  Exit
-    // tests are taken by lane 0 and broadcast, so the warp never diverges
-    // around __syncwarp.
-    int stage = 0;
-    uint32_t phase = 0;
-    uint32_t armed = 0, armed_parity = 0;
-    for (int t = blockIdx.x; t < total_tiles; t += gridDim.x) {
-      if (__shfl_sync(0xffffffffu, abort_flag != 0 ? 1 : 0, 0)) break;
-      const FgTile tl = fg_decode<BT>(t, mbp, p);
-      const int n16 = (int)round16(tl.n);
-      if (GATHER) {
-        __syncwarp();  // every gather of the previous tile has been issued
-        for (int i = lane; i < n16; i += 32) {
-          // rows past the tile's end repeat its first row (computed, masked on store)
-          const int32_t src = p.row_src[tl.r0 + (i < tl.n ? i : 0)];
-          src_rows[i] = src >= 0 ? src : 0;
-        }
-        __syncwarp();
-      }
-      const uint32_t x_bytes = (uint32_t)n16 * (uint32_t)(kTcBK * 2);
-      bool ok = true;
-      for (int kb = 0; kb < p.k_blocks; ++kb) {
-        int w_ok = 1;
-        if (lane == 0 && !mbar_wait(&xempty[stage], phase ^ 1u, &abort_flag)) {
-          abort_flag = 1;
-          raise_error(kErrTimeout);
-          w_ok = 0;
-        }
-        if (!__shfl_sync(0xffffffffu, w_ok, 0)) {
-          ok = false;
-          break;
-        }
-        uint8_t* sx = ring_x + (size_t)stage * S::kXStage;
-        const int kx = kb * (FP8 ? 128 : kTcBK);
-        if (lane == 0) mbar_expect_tx(&xfull[stage], x_bytes);
-        if (GATHER) {
-          __syncwarp();  // the stage is armed before any gather can complete on it
-          for (int i = 4 * lane; i < n16; i += 4 * 32)
-            tma_gather4(sx + i * (kTcBK * 2), &map_x[0], kx, src_rows[i], src_rows[i + 1], src_rows[i + 2],
-                        src_rows[i + 3], &xfull[stage]);
-        } else if (lane == 0) {
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      uint32_t armed = 0, armed_parity = 0;
+      for (int t = blockIdx.x; t < total_tiles && !abort_flag; t += gridDim.x) {
+        const FgTile tl = fg_decode<BT>(t, mbp, p);
+        const int n16 = (int)round16(tl.n);
+        const uint32_t x_bytes = (uint32_t)n16 * (uint32_t)(kTcBK * 2);
+        for (int kb = 0; kb < p.k_blocks; ++kb) {
+          if (!mbar_wait(&xempty[stage], phase ^ 1u, &abort_flag)) {
+            abort_flag = 1;
+            raise_error(kErrTimeout);
+            break;
+          }
+          uint8_t* sx = ring_x + (size_t)stage * S::kXStage;
+          const int kx = kb * (FP8 ? 128 : kTcBK);
+          mbar_expect_tx(&xfull[stage], x_bytes);
           // round16(n) rows as boxes of 128 rows, then at most one each of 64, 32 and 16
           int b = 0;
           for (; b + 128 <= n16; b += 128) tma_load_2d(sx + b * (kTcBK * 2), &map_x[0], kx, tl.r0 + b, &xfull[stage]);
           if ((n16 - b) & 64) { tma_load_2d(sx + b * (kTcBK * 2), &map_x[1], kx, tl.r0 + b, &xfull[stage]); b += 64; }
           if ((n16 - b) & 32) { tma_load_2d(sx + b * (kTcBK * 2), &map_x[2], kx, tl.r0 + b, &xfull[stage]); b += 32; }
           if ((n16 - b) & 16) tma_load_2d(sx + b * (kTcBK * 2), &map_x[3], kx, tl.r0 + b, &xfull[stage]);
-        }
-        armed |= 1u << stage;
-        armed_parity = (armed_parity & ~(1u << stage)) | (phase << stage);
-        if (++stage == XS) {
-          stage = 0;
-          phase ^= 1u;
+          armed |= 1u << stage;
+          armed_parity = (armed_parity & ~(1u << stage)) | (phase << stage);
+          if (++stage == XS) {
+            stage = 0;
+            phase ^= 1u;
+          }
         }
       }
-      if (!ok) break;
+      if (abort_flag) {
+        for (int s = 0; s < XS; ++s)
+          if ((armed >> s) & 1u) mbar_wait(&xfull[s], (armed_parity >> s) & 1u);
+      }
     }
-    if (lane == 0 && abort_flag) {
-      for (int s = 0; s < XS; ++s)
-        if ((armed >> s) & 1u) mbar_wait(&xfull[s], (armed_parity >> s) & 1u);
+  } else if (GATHER && warp >= 6 && warp < 6 + XS) {
+    // ------------------------------------------------------------ token gather (warp 6 + g fills stage g)
+    // k-block j of the CTA's sequence uses token stage j % XS, so this warp
+    // takes every XS-th k-block.  Its copies are complete (cp.async.wait_group)
+    // and fenced before it arrives, so nothing is in flight when it exits.
+    const int g = warp - 6;
+    int32_t* srow = src_rows[g];
+    uint8_t* sx = ring_x + (size_t)g * S::kXStage;
+    const uint32_t sx_u32 = smem_u32(sx);
+    uint32_t phase = 0;
+    int j = 0;   // k-blocks of the sequence before the current one
+    bool ok = true;
+    for (int t = blockIdx.x; t < total_tiles && ok; t += gridDim.x) {
+      if (__shfl_sync(0xffffffffu, abort_flag != 0 ? 1 : 0, 0)) break;
+      const FgTile tl = fg_decode<BT>(t, mbp, p);
+      const int n16 = (int)round16(tl.n);
+      // the first k-block of this tile that is ours
+      int kb = ((g - j) % XS + XS) % XS;
+      if (kb < p.k_blocks) {
+        __syncwarp();
+        for (int i = lane; i < n16; i += 32) {
+          // rows past the tile's end repeat its first row (computed, masked on store)
+          const int32_t src = p.row_src[tl.r0 + (i < tl.n ? i : 0)];
+          srow[i] = src >= 0 ? src : 0;
+        }
+        __syncwarp();
+      }
+      for (; kb < p.k_blocks; kb += XS) {
+        // every lane waits (each of its copies must follow the MMAs' reads of
+        // the stage); the warp gives up together if any lane's wait ran out
+        const bool w_ok = mbar_wait(&xempty[g], phase ^ 1u, &abort_flag);
+        if (!__all_sync(0xffffffffu, w_ok)) {
+          if (lane == 0) {
+            abort_flag = 1;
+            raise_error(kErrTimeout);
+          }
+          ok = false;
+          break;
+        }
+        // pair i = (row i / 8, 16-byte chunk i % 8) of the k-block's 128-byte row pieces
+        const uint8_t* xk = p.gather_x + (size_t)kb * (kTcBK * 2);
+        for (int i = lane; i < n16 * 8; i += 32) {
+          const int r = i >> 3, c = i & 7;
+          cp_async16(sx_u32 + (uint32_t)(r * 128 + ((c ^ (r & 7)) << 4)),
+                     xk + (size_t)srow[r] * (size_t)p.ldx_bytes + c * 16);
+        }
+        asm volatile("cp.async.commit_group;\n\tcp.async.wait_group 0;" ::: "memory");
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        mbar_arrive(&xfull[g]);
+        phase ^= 1u;
+      }
+      j += p.k_blocks;
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer

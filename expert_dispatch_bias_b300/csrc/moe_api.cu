@@ -573,10 +573,8 @@ moe_status launch_ffn_grouped(const moe_config& c, const void* xp, const int32_t
   MOE_TRY(make_tensor_map(&w1m, w13, c.h, (uint64_t)n_w * 2 * c.I, 128));
   MOE_TRY(make_tensor_map(&w2m, w2, c.I, (uint64_t)n_w * c.h, 128));
   for (int i = 0; i < 4; ++i) {
-    if (row_src != nullptr)
-      MOE_TRY(make_tensor_map(&x1.m[i], xp, c.h, c.T, 1));  // rows of x, gathered four at a time
-    else
-      MOE_TRY(make_tensor_map(&x1.m[i], xp, c.h, R, 128u >> i));
+    // gathered rows are copied from x by the kernel's gather warps: no map of x
+    MOE_TRY(make_tensor_map(&x1.m[i], xp, c.h, row_src != nullptr ? (uint64_t)c.T : (uint64_t)R, 128u >> i));
     MOE_TRY(make_tensor_map(&x2.m[i], inter, c.I, R, 128u >> i));
   }
   FgParams p1{};
@@ -600,13 +598,15 @@ moe_status launch_ffn_grouped(const moe_config& c, const void* xp, const int32_t
   p2.out = static_cast<__nv_bfloat16*>(yp);
   p2.ldo = c.h;
   p1.row_src = row_src;
+  p1.gather_x = static_cast<const uint8_t*>(xp);
+  p1.ldx_bytes = (int64_t)c.h * 2;
   p2.row_src = nullptr;
-  auto k1 = row_src != nullptr ? ffn_grouped_kernel<kTcSwiglu, BT, WS, XS, false, true>
-                               : ffn_grouped_kernel<kTcSwiglu, BT, WS, XS>;
+  const bool gather = row_src != nullptr;
+  auto k1 = gather ? ffn_grouped_kernel<kTcSwiglu, BT, WS, XS, false, true> : ffn_grouped_kernel<kTcSwiglu, BT, WS, XS>;
   auto k2 = ffn_grouped_kernel<kTcStore, BT, WS, XS>;
   CUDA_TRY(allow_smem(k1, S::kDynSmem));
   CUDA_TRY(allow_smem(k2, S::kDynSmem));
-  k1<<<grid, kFgThreads, S::kDynSmem, st>>>(w1m, x1, p1);
+  k1<<<grid, gather ? FgThreads<true, XS>::value : kFgThreads, S::kDynSmem, st>>>(w1m, x1, p1);
   CUDA_TRY(launched());
   k2<<<grid, kFgThreads, S::kDynSmem, st>>>(w2m, x2, p2);
   CUDA_TRY(launched());
@@ -804,11 +804,12 @@ moe_status launch_permute_fp8(const moe_config& c, const void* x, const int32_t*
 
 // The grouped FFN reading its rows straight from x through row_src: bf16,
 // weights-as-M layers only (experts expected to see at most
-// MOE_FFN_SWAP_MAX_ROWS rows).  The layer calls do not use it: on B300 the
-// four-row TMA gathers cost about as much per instruction as a whole box, and
-// the gathered FFN measured no faster than permute + FFN at a few rows per
-// expert and up to 1.8x slower at DeepSeek-V3 prefill (144 rows per tile,
-// h = 7168).  It saves the permuted copy of x (R x h).
+// MOE_FFN_SWAP_MAX_ROWS rows).  Gather warps copy the rows with 16-byte
+// cp.async (the four-row TMA gathers tried first cost about as much per
+// instruction as a whole box: 1.75x slower at DeepSeek-V3 prefill).  The rows
+// are gathered once per feature tile, which at DeepSeek-V3 T=4096 measured a
+// few percent slower than the explicit permute + FFN, so the layer calls keep
+// the permute.  It saves the permuted copy of x (R x h).
 moe_status launch_ffn_gather(const moe_config& c, const void* x, const int32_t* row_src, const int32_t* offsets,
                              const int32_t* kept, const int32_t* w_map, int n_w, const void* w13, const void* w2,
                              void* yp, void* inter, cudaStream_t st) {

@@ -257,14 +257,16 @@ moe_status moe_grouped_ffn(const moe_config* cfg, const void* xp, const int32_t*
                            void* workspace, size_t workspace_bytes, void* stream);
 
 /* moe_permute and moe_grouped_ffn in one: the gate/up GEMM reads every row of
- * an expert's segment straight from x through row_src (TMA gathers of four
- * rows), so no permuted copy of x is written or read ("index lists instead of
- * routing buffers": [lqhl] "Expert-Parallelism", design routes, route 5).
- * x [T,h] bf16; row_src [R] from moe_dispatch_layout; other arguments as in
- * moe_grouped_ffn; bf16 layers whose experts are expected to see at most 160
- * rows (else MOE_ERR_UNSUPPORTED).  It saves the R x h permuted copy of x; on
- * B300 it runs no faster than moe_permute + moe_grouped_ffn (slower with many
- * rows per expert), so the layer calls permute explicitly. */
+ * an expert's segment straight from x through row_src (16-byte copies into the
+ * tensor cores' shared-memory layout), so no permuted copy of x is written or
+ * read ("index lists instead of routing buffers": [lqhl] "Expert-Parallelism",
+ * design routes, route 5).  x [T,h] bf16; row_src [R] from
+ * moe_dispatch_layout; other arguments as in moe_grouped_ffn; bf16 layers
+ * whose experts are expected to see at most 160 rows (else
+ * MOE_ERR_UNSUPPORTED).  It saves the R x h permuted copy of x (470 MB at the
+ * DeepSeek-V3 shape); the rows are gathered once per feature tile, and on B300
+ * that costs a few percent more than moe_permute + moe_grouped_ffn, so the
+ * layer calls permute explicitly. */
 moe_status moe_grouped_ffn_gather(const moe_config* cfg, const void* x, const int32_t* row_src,
                                   const int32_t* offsets, const int32_t* kept, const void* w13, const void* w2,
                                   void* yp, void* workspace, size_t workspace_bytes, void* stream);
