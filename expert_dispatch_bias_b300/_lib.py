@@ -19,7 +19,7 @@ MOE_F32, MOE_BF16 = 0, 1
 MOE_SOFTMAX, MOE_SIGMOID = 0, 1
 MOE_OP_LAYOUT, MOE_OP_FFN, MOE_OP_LAYER, MOE_OP_LAYER_HOST = 0, 1, 2, 3
 MOE_OP_SHARED, MOE_OP_BLOCK, MOE_OP_BLOCK_HOST = 4, 5, 6
-MOE_OP_FFN_FP8, MOE_OP_LAYER_FP8, MOE_OP_LOGITS = 7, 8, 9
+MOE_OP_FFN_FP8, MOE_OP_LAYER_FP8, MOE_OP_LOGITS, MOE_OP_FFN_COMBINE = 7, 8, 9, 10
 
 STATUS = {
     0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED", 3: "MOE_ERR_ALIGNMENT",
@@ -36,7 +36,7 @@ EXPORTS = (
     "moe_shared_ffn", "moe_combine_add", "moe_block_forward", "moe_block_forward_host",
     "moe_eplb_plan", "moe_eplb_map", "moe_grouped_ffn_mapped", "moe_layer_forward_eplb",
     "moe_quantize_fp8", "moe_permute_fp8", "moe_grouped_ffn_fp8", "moe_layer_forward_fp8",
-    "moe_grouped_ffn_gather", "moe_launch_count",
+    "moe_grouped_ffn_gather", "moe_grouped_ffn_combine", "moe_launch_count",
 )
 
 
@@ -106,6 +106,7 @@ def _load() -> ctypes.CDLL:
         "moe_grouped_ffn_fp8": (c_int32, [cfgp] + [c_void_p] * 10 + [c_size_t, c_void_p]),
         "moe_layer_forward_fp8": (c_int32, [cfgp] + [c_void_p] * 11 + [c_size_t, c_void_p]),
         "moe_grouped_ffn_gather": (c_int32, [cfgp] + [c_void_p] * 8 + [c_size_t, c_void_p]),
+        "moe_grouped_ffn_combine": (c_int32, [cfgp] + [c_void_p] * 11 + [c_size_t, c_void_p]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -214,6 +215,15 @@ def moe_grouped_ffn(cfg, xp, offsets, kept, w13, w2, yp, workspace, stream=None)
     _check(lib.moe_grouped_ffn(ctypes.byref(cfg), _ptr(xp), _ptr(offsets), _ptr(kept), _ptr(w13), _ptr(w2),
                                _ptr(yp), _ptr(workspace), workspace.numel() * workspace.element_size(),
                                _stream(stream)), "moe_grouped_ffn")
+
+
+def moe_grouped_ffn_combine(cfg, xp, offsets, kept, w13, w2, row_src, slot, topk_w, yp, y, workspace,
+                            stream=None) -> None:
+    """workspace: moe_workspace_size(cfg, MOE_OP_FFN_COMBINE) bytes, zero-filled (alloc_workspace)."""
+    _check(lib.moe_grouped_ffn_combine(ctypes.byref(cfg), _ptr(xp), _ptr(offsets), _ptr(kept), _ptr(w13), _ptr(w2),
+                                       _ptr(row_src), _ptr(slot), _ptr(topk_w), _ptr(yp), _ptr(y), _ptr(workspace),
+                                       workspace.numel() * workspace.element_size(), _stream(stream)),
+           "moe_grouped_ffn_combine")
 
 
 def moe_grouped_ffn_gather(cfg, x, row_src, offsets, kept, w13, w2, yp, workspace, stream=None) -> None:

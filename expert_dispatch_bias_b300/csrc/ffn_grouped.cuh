@@ -88,6 +88,15 @@ struct FgParams {
   const int32_t* row_src;   // gather: token of every permuted row [R] (rows are read from x)
   const uint8_t* gather_x;  // gather: x [T, ldx_bytes]
   int64_t ldx_bytes;        // gather: bytes per row of x
+  // combine fused into the down epilogue (dropless layers): the token of every
+  // row (row_src), each token's K slots and weights, the output y [T, n_valid]
+  // and one arrival counter per (token, 32-feature group), zero between calls
+  const int32_t* slot;      // [T, K]
+  const float* topk_w;      // [T, K]
+  int K;
+  int groups;               // n_valid / 32
+  __nv_bfloat16* y;
+  uint32_t* arrive;         // [T, groups]
 };
 
 // Tensor maps of the token rows with boxes of 128, 64, 32 and 16 rows.
@@ -133,7 +142,34 @@ __device__ __forceinline__ void cp_async16(uint32_t smem_dst, const void* gsrc) 
 // Epilogue of one 32-token chunk: v (and u, SwiGLU) hold this warp's 32
 // features x 32 tokens; the bf16 results are transposed through the warp's
 // shared buffer and each lane stores the 64-byte piece of token row r0 + c + lane.
-template <int EPI, bool FP8>
+// The last of a token's K arrivals for one 32-feature group: y[t, feat0..+31]
+// = sum over k = 0..K-1 of topk_w[t,k] * yp[slot[t,k], feat0..+31], float32
+// fused multiply-adds in k order from 0 (the arithmetic of combine_kernel), the
+// staged rows read from L2.
+__device__ __forceinline__ void fg_combine_group(int64_t t, int feat0, const FgParams& p) {
+  float acc[32];
+#pragma unroll
+  for (int i = 0; i < 32; ++i) acc[i] = 0.0f;
+  for (int k = 0; k < p.K; ++k) {
+    const int32_t s = p.slot[t * p.K + k];
+    const float w = p.topk_w[t * p.K + k];
+    const uint4* src = reinterpret_cast<const uint4*>(p.out + (int64_t)s * p.ldo + feat0);
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const uint4 v = __ldcg(src + q);
+      const uint32_t wds[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const __nv_bfloat162 b = *reinterpret_cast<const __nv_bfloat162*>(&wds[i]);
+        acc[8 * q + 2 * i] = fmaf(w, __low2float(b), acc[8 * q + 2 * i]);
+        acc[8 * q + 2 * i + 1] = fmaf(w, __high2float(b), acc[8 * q + 2 * i + 1]);
+      }
+    }
+  }
+  store_bf16_row<32>(p.y + t * (int64_t)p.ldo + feat0, acc);
+}
+
+template <int EPI, bool FP8, bool COMB = false>
 __device__ __forceinline__ void fg_chunk(const uint32_t* v, const uint32_t* u, int c, int n, int r0, int feat0,
                                          bool feat_ok, const FgParams& p, __nv_bfloat16* xs, float wsg, float wsu) {
   const int lane = threadIdx.x & 31;
@@ -160,6 +196,18 @@ __device__ __forceinline__ void fg_chunk(const uint32_t* v, const uint32_t* u, i
     uint4* dst = reinterpret_cast<uint4*>(p.out + (int64_t)(r0 + c + lane) * p.ldo + feat0);
 #pragma unroll
     for (int i = 0; i < 4; ++i) dst[i] = src[i];
+    if (COMB) {
+      // the row's piece is staged; count its arrival, and the K-th arrival
+      // for this token and feature group sums the K staged pieces
+      const int64_t t = p.row_src[r0 + c + lane];
+      uint32_t* ctr = p.arrive + t * p.groups + (feat0 >> 5);
+      __threadfence();
+      if (atomicAdd(ctr, 1u) == (uint32_t)(p.K - 1)) {
+        __threadfence();
+        *ctr = 0u;   // every arrival of this call has come: ready for the next call
+        fg_combine_group(t, feat0, p);
+      }
+    }
   }
   __syncwarp();
 }
@@ -168,7 +216,7 @@ __device__ __forceinline__ void fg_chunk(const uint32_t* v, const uint32_t* u, i
 // (columns col0.., and col_up.. for the SwiGLU's up half), two chunks in
 // flight: the next chunk's tcgen05.ld runs while this one is transposed and
 // stored.
-template <int EPI, bool FP8>
+template <int EPI, bool FP8, bool COMB = false>
 __device__ __forceinline__ void fg_drain(uint32_t t_lane, uint32_t col0, uint32_t col_up, int n, int r0,
                                          int feat0, bool feat_ok, const FgParams& p, __nv_bfloat16* xs,
                                          float wsg = 1.0f, float wsu = 1.0f) {
@@ -185,7 +233,7 @@ __device__ __forceinline__ void fg_drain(uint32_t t_lane, uint32_t col0, uint32_
       tmem_ld<32>(t_lane + col0 + c + 32, vb);
       if (kUp) tmem_ld<32>(t_lane + col_up + c + 32, ub);
     }
-    fg_chunk<EPI, FP8>(va, ua, c, n, r0, feat0, feat_ok, p, xs, wsg, wsu);
+    fg_chunk<EPI, FP8, COMB>(va, ua, c, n, r0, feat0, feat_ok, p, xs, wsg, wsu);
     if (c + 32 >= n) break;
     tmem_ld_wait();
     tmem_regs_ready(vb);
@@ -194,7 +242,7 @@ __device__ __forceinline__ void fg_drain(uint32_t t_lane, uint32_t col0, uint32_
       tmem_ld<32>(t_lane + col0 + c + 64, va);
       if (kUp) tmem_ld<32>(t_lane + col_up + c + 64, ua);
     }
-    fg_chunk<EPI, FP8>(vb, ub, c + 32, n, r0, feat0, feat_ok, p, xs, wsg, wsu);
+    fg_chunk<EPI, FP8, COMB>(vb, ub, c + 32, n, r0, feat0, feat_ok, p, xs, wsg, wsu);
   }
 }
 
@@ -205,7 +253,10 @@ __device__ __forceinline__ void fg_drain(uint32_t t_lane, uint32_t col0, uint32_
 // 16-byte cp.async copies into the 128-byte-swizzled layout the MMA expects,
 // waits for its own copies, makes them visible to the tensor core's (async
 // proxy) reads with fence.proxy.async, and then arrives on the stage's barrier.
-template <int EPI, int BT, int WS, int XS, bool FP8 = false, bool GATHER = false>
+// COMBINE (down projection, dropless): the weighted combine fused into the
+// epilogue (fg_chunk): expert rows are still staged in out (yp), and the last
+// arrival of every (token, 32-feature group) writes y.
+template <int EPI, int BT, int WS, int XS, bool FP8 = false, bool GATHER = false, bool COMBINE = false>
 __global__ void __launch_bounds__(FgThreads<GATHER, XS>::value, 1)
     ffn_grouped_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_constant__ FgTokenMaps maps,
                        FgParams p) {
@@ -490,12 +541,12 @@ __global__ void __launch_bounds__(FgThreads<GATHER, XS>::value, 1)
         const int f0 = 256 * tl.ft + 32 * quarter;
         const float ws0 = (FP8 && f0 + 32 <= p.n_valid) ? p.w_scale[wrow + f0 + lane] : 1.0f;
         const float ws1 = (FP8 && f0 + 160 <= p.n_valid) ? p.w_scale[wrow + f0 + 128 + lane] : 1.0f;
-        fg_drain<kTcStore, FP8>(t_lane, c0, 0, tl.n, tl.r0, f0, f0 + 32 <= p.n_valid, p, xs, ws0);
+        fg_drain<kTcStore, FP8, COMBINE>(t_lane, c0, 0, tl.n, tl.r0, f0, f0 + 32 <= p.n_valid, p, xs, ws0);
         if (big) {  // D0 alone fills slot 0: hand it back before draining D1
           tc_fence_before();
           mbar_arrive(&tmem_empty[0]);
         }
-        fg_drain<kTcStore, FP8>(t_lane, c1, 0, tl.n, tl.r0, f0 + 128, f0 + 160 <= p.n_valid, p, xs, ws1);
+        fg_drain<kTcStore, FP8, COMBINE>(t_lane, c1, 0, tl.n, tl.r0, f0 + 128, f0 + 160 <= p.n_valid, p, xs, ws1);
       }
       tc_fence_before();
       if (big) {

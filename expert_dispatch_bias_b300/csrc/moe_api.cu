@@ -233,6 +233,11 @@ moe_status static_layout_scratch(void** out) {
 }
 
 size_t ffn_ws_bytes(const moe_config& c) { return align_up((size_t)rows_of(c) * c.I * ds_of(c), 256) + 256; }
+// moe_grouped_ffn_combine: the FFN's workspace, then one arrival counter per
+// (token, 32-feature group).
+size_t ffn_combine_ws_bytes(const moe_config& c) {
+  return ffn_ws_bytes(c) + align_up((size_t)c.T * (c.h / 32) * 4, 256);
+}
 
 // ------------------------------------------------------------------ launchers
 moe_status launch_logits_simt(const moe_config& c, const void* x, const void* w_r, const float* off, float* logits,
@@ -559,12 +564,22 @@ moe_status launch_ffn_tokens_m(const moe_config& c, const void* xp, const int32_
 // and 256-row tiles with 4 + 2 (5.13) starve the MMA of token k-blocks, whose
 // L2 latency under this load needs four in flight.
 constexpr int kFgTileRows = 160, kFgWStages = 4, kFgXStages = 4;
+// The weighted combine fused into the down projection (dropless layers).
+struct FusedCombine {
+  const int32_t* row_src;
+  const int32_t* slot;
+  const float* topk_w;
+  void* y;
+  uint32_t* arrive;   // [T, h/32], zero between calls
+};
+
 // row_src non-null: the gate/up GEMM gathers its rows from x = xp through row_src
-// (no permuted copy of x); else xp holds the permuted rows.
+// (no permuted copy of x); else xp holds the permuted rows.  comb non-null: the
+// down projection also writes the combine into comb->y.
 template <int BT, int WS, int XS>
 moe_status launch_ffn_grouped(const moe_config& c, const void* xp, const int32_t* offsets, const int32_t* kept,
                               const int32_t* w_map, int n_w, const void* w13, const void* w2, void* yp, void* inter,
-                              cudaStream_t st, const int32_t* row_src = nullptr) {
+                              cudaStream_t st, const int32_t* row_src = nullptr, const FusedCombine* comb = nullptr) {
   using S = FgShape<BT, WS, XS>;
   const int64_t R = rows_of(c);
   const int grid = device_info().sms;
@@ -601,9 +616,19 @@ moe_status launch_ffn_grouped(const moe_config& c, const void* xp, const int32_t
   p1.gather_x = static_cast<const uint8_t*>(xp);
   p1.ldx_bytes = (int64_t)c.h * 2;
   p2.row_src = nullptr;
+  if (comb != nullptr) {
+    p2.row_src = comb->row_src;
+    p2.slot = comb->slot;
+    p2.topk_w = comb->topk_w;
+    p2.K = c.K;
+    p2.groups = c.h / 32;
+    p2.y = static_cast<__nv_bfloat16*>(comb->y);
+    p2.arrive = comb->arrive;
+  }
   const bool gather = row_src != nullptr;
   auto k1 = gather ? ffn_grouped_kernel<kTcSwiglu, BT, WS, XS, false, true> : ffn_grouped_kernel<kTcSwiglu, BT, WS, XS>;
-  auto k2 = ffn_grouped_kernel<kTcStore, BT, WS, XS>;
+  auto k2 = comb != nullptr ? ffn_grouped_kernel<kTcStore, BT, WS, XS, false, false, true>
+                            : ffn_grouped_kernel<kTcStore, BT, WS, XS>;
   CUDA_TRY(allow_smem(k1, S::kDynSmem));
   CUDA_TRY(allow_smem(k2, S::kDynSmem));
   k1<<<grid, gather ? FgThreads<true, XS>::value : kFgThreads, S::kDynSmem, st>>>(w1m, x1, p1);
@@ -1046,6 +1071,7 @@ moe_status moe_workspace_size(const moe_config* cfg, int32_t op, size_t* bytes) 
     case MOE_OP_FFN_FP8: *bytes = ffn_fp8_ws_bytes(*cfg); return MOE_OK;
     case MOE_OP_LAYER_FP8: *bytes = carve_layer(*cfg, nullptr, false, false, true).total; return MOE_OK;
     case MOE_OP_LOGITS: *bytes = logits_ws_bytes(*cfg); return MOE_OK;
+    case MOE_OP_FFN_COMBINE: *bytes = ffn_combine_ws_bytes(*cfg); return MOE_OK;
   }
   return MOE_ERR_INVALID_ARG;
 }
@@ -1160,6 +1186,40 @@ moe_status moe_grouped_ffn(const moe_config* cfg, const void* xp, const int32_t*
   if (workspace_bytes < ffn_ws_bytes(*cfg)) return MOE_ERR_WORKSPACE_TOO_SMALL;
   return launch_ffn(*cfg, xp, offsets, kept, nullptr, nphys(*cfg), w13, w2, yp, static_cast<char*>(workspace) + 256,
                     as_stream(stream));
+}
+
+moe_status moe_grouped_ffn_combine(const moe_config* cfg, const void* xp, const int32_t* offsets,
+                                   const int32_t* kept, const void* w13, const void* w2, const int32_t* row_src,
+                                   const int32_t* slot, const float* topk_w, void* yp, void* y, void* workspace,
+                                   size_t workspace_bytes, void* stream) {
+  MOE_TRY(validate(cfg));
+  if (cfg->dtype != MOE_BF16 || cfg->capacity != 0 || cfg->n_redundant != 0) return MOE_ERR_UNSUPPORTED;
+  if (expected_rows_per_expert(*cfg) > MOE_FFN_SWAP_MAX_ROWS) return MOE_ERR_UNSUPPORTED;
+  if ((int64_t)cfg->E * 2 * cfg->I >= INT32_MAX || (int64_t)cfg->E * cfg->h >= INT32_MAX) return MOE_ERR_UNSUPPORTED;
+  if (cfg->T > 0) {
+    MOE_TRY(check_dtype_ptr(xp));
+    MOE_TRY(check_dtype_ptr(yp));
+    MOE_TRY(check_dtype_ptr(y));
+    MOE_TRY(check_ptr(row_src, 4));
+    MOE_TRY(check_ptr(slot, 4));
+    MOE_TRY(check_ptr(topk_w, 4));
+  }
+  MOE_TRY(check_ptr(offsets, 4));
+  MOE_TRY(check_ptr(kept, 4));
+  MOE_TRY(check_dtype_ptr(w13));
+  MOE_TRY(check_dtype_ptr(w2));
+  MOE_TRY(check_ptr(workspace, 256));
+  if (workspace_bytes < ffn_combine_ws_bytes(*cfg)) return MOE_ERR_WORKSPACE_TOO_SMALL;
+  if (cfg->T == 0) return MOE_OK;
+  FusedCombine fc;
+  fc.row_src = row_src;
+  fc.slot = slot;
+  fc.topk_w = topk_w;
+  fc.y = y;
+  fc.arrive = reinterpret_cast<uint32_t*>(static_cast<char*>(workspace) + ffn_ws_bytes(*cfg));
+  return launch_ffn_grouped<kFgTileRows, kFgWStages, kFgXStages>(*cfg, xp, offsets, kept, nullptr, cfg->E, w13, w2, yp,
+                                                                 static_cast<char*>(workspace) + 256,
+                                                                 as_stream(stream), nullptr, &fc);
 }
 
 moe_status moe_combine(const moe_config* cfg, const void* yp, const int32_t* slot, const float* topk_w, void* y,

@@ -69,7 +69,8 @@ typedef enum {
   MOE_OP_BLOCK_HOST = 6,  /* moe_block_forward_host */
   MOE_OP_FFN_FP8 = 7,     /* moe_grouped_ffn_fp8 */
   MOE_OP_LAYER_FP8 = 8,   /* moe_layer_forward_fp8 */
-  MOE_OP_LOGITS = 9       /* moe_router_logits */
+  MOE_OP_LOGITS = 9,      /* moe_router_logits */
+  MOE_OP_FFN_COMBINE = 10 /* moe_grouped_ffn_combine */
 } moe_op;
 
 /* Layer description.  Limits: T >= 0; h % 64 == 0; I % 64 == 0; 1 <= E <= 1024;
@@ -270,6 +271,27 @@ moe_status moe_grouped_ffn(const moe_config* cfg, const void* xp, const int32_t*
 moe_status moe_grouped_ffn_gather(const moe_config* cfg, const void* x, const int32_t* row_src,
                                   const int32_t* offsets, const int32_t* kept, const void* w13, const void* w2,
                                   void* yp, void* workspace, size_t workspace_bytes, void* stream);
+
+/* moe_grouped_ffn and moe_combine in one: the weighted combine is fused into
+ * the down projection's epilogue ([serving] "MoE 服務專家並行的未來": fused
+ * dispatch-compute-combine kernels; [lqhl] "Expert-Parallelism", design
+ * routes, route 5).  Every expert output row is still staged in yp; each
+ * stored 32-feature piece of a row counts one arrival for its (token, feature
+ * group), and the K-th arrival computes y[t, group] = sum_k topk_w[t,k] *
+ * yp[slot[t,k], group] with float32 fused multiply-adds in k order and stores
+ * it in bf16: bit-identical to moe_combine on the same yp.  Arguments as in
+ * moe_grouped_ffn, plus row_src [R], slot [T,K] and topk_w [T,K] from
+ * moe_dispatch_layout / moe_route, and y [T,h] bf16.  bf16, dropless
+ * (capacity 0), no replicas, experts expected to see at most 160 rows (else
+ * MOE_ERR_UNSUPPORTED).  workspace >= moe_workspace_size(MOE_OP_FFN_COMBINE),
+ * zero-filled once by moe_workspace_init: its arrival counters are left at
+ * zero by every call that completes (re-initialise it after
+ * MOE_ERR_DEVICE_TIMEOUT).  Calls that overlap on the GPU must not share a
+ * workspace. */
+moe_status moe_grouped_ffn_combine(const moe_config* cfg, const void* xp, const int32_t* offsets,
+                                   const int32_t* kept, const void* w13, const void* w2, const int32_t* row_src,
+                                   const int32_t* slot, const float* topk_w, void* yp, void* y, void* workspace,
+                                   size_t workspace_bytes, void* stream);
 
 /* Weighted combine ([compass] "技術原理" step 4; [overview] glossary "Combine"):
  * y[t] = sum_{k: slot[t,k] >= 0} topk_w[t,k] * yp[slot[t,k]], float32 sum in k order,
