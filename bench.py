@@ -166,6 +166,7 @@ class ClockSampler:
         self.csv_path = csv_path
         self.rows = []          # (sm_mhz, max_mhz, power_w, reasons bitmask)
         self.kind = None
+        self.thread = None
         self._stop = threading.Event()
 
     def _nvml_handle(self):
@@ -231,12 +232,16 @@ class ClockSampler:
                     f.write(f"{r[0]:.0f},{r[1]:.0f},{r[2]:.1f},0x{r[3]:x}\n")
 
     def summary(self):
+        """Median SM clock and the reasons seen.  NVML samples are taken only
+        while the timed region runs, so every one of them is under load (its
+        power reading averages over a longer window and lags a short region);
+        nvidia-smi's are filtered by power draw as well."""
         if not self.rows:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "source": self.kind}
-        loaded = [r for r in self.rows if r[2] > 300.0] or self.rows
+        loaded = self.rows if self.thread is not None else ([r for r in self.rows if r[2] > 300.0] or self.rows)
         reasons = sorted({n for r in loaded for n, bit in REASON_BITS.items() if r[3] & bit})
         return {"sm_mhz": statistics.median(r[0] for r in loaded), "sm_max_mhz": max(r[1] for r in self.rows),
-                "samples": len(self.rows), "samples_under_load": len([r for r in self.rows if r[2] > 300.0]),
+                "samples": len(self.rows), "samples_under_load": len(loaded),
                 "power_w_max": max(r[2] for r in self.rows), "reasons": reasons, "source": self.kind}
 
 

@@ -21,6 +21,7 @@ def test_routing_report_counts_near_ties_and_mismatches():
 def test_clock_summary_uses_loaded_samples_and_reasons():
     c = bench.ClockSampler(0)
     c.kind = "test"
+    c.thread = None   # samples as nvidia-smi takes them: filtered by power
     c.rows = [(1000.0, 2032.0, 150.0, 0x0), (2032.0, 2032.0, 900.0, 0x0), (1980.0, 2032.0, 1100.0, 0x4),
               (2032.0, 2032.0, 950.0, 0x0)]
     s = c.summary()
