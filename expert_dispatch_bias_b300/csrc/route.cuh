@@ -157,13 +157,39 @@ __device__ __forceinline__ RouteSel route_select(const float* key, const RoutePa
     }
   }
 
-  // ---- top-K by repeated warp arg-max; one more round measures the gap to
-  // the first expert left out
-  bool avail[PER];
+  // ---- top-K.  Each lane sorts its allowed keys once (key descending, then
+  // lower id); then K+1 rounds of a warp arg-max over the lanes' first keys,
+  // the winning lane dropping its first key; the last round measures the gap
+  // to the first expert left out.  Sorting once replaces a rescan of all PER
+  // keys in every round.
+  float sk[PER];
+  int si[PER];
+  {
+    // the experts of a lane are PER consecutive ids: one group per lane when a
+    // group holds whole lanes' runs, else a group per expert
+    const int g0 = (lane * PER) / gsize;
 #pragma unroll
-  for (int i = 0; i < PER; ++i) {
-    const int e = lane * PER + i;
-    avail[i] = e < p.E && ((gmask >> (e / gsize)) & 1u);
+    for (int i = 0; i < PER; ++i) {
+      const int e = lane * PER + i;
+      const int g = (gsize % PER == 0) ? g0 : e / gsize;
+      const bool ok = e < p.E && ((gmask >> g) & 1u);
+      sk[i] = ok ? key[i] : -INFINITY;
+      si[i] = ok ? e : NONE;
+    }
+  }
+  // odd-even transposition sort; an allowed entry goes before a disallowed one
+#pragma unroll
+  for (int round = 0; round < PER; ++round) {
+#pragma unroll
+    for (int i = round & 1; i + 1 < PER; i += 2) {
+      const bool swap = si[i + 1] != NONE && (si[i] == NONE || beats(sk[i + 1], si[i + 1], sk[i], si[i]));
+      const float tk = swap ? sk[i + 1] : sk[i];
+      const int ti = swap ? si[i + 1] : si[i];
+      sk[i + 1] = swap ? sk[i] : sk[i + 1];
+      si[i + 1] = swap ? si[i] : si[i + 1];
+      sk[i] = tk;
+      si[i] = ti;
+    }
   }
   r.my_id = 0;
   r.min_gap = INFINITY;
@@ -172,16 +198,8 @@ __device__ __forceinline__ RouteSel route_select(const float* key, const RoutePa
   r.gsize = gsize;
   float prev = 0.0f;
   for (int k = 0; k <= p.K; ++k) {
-    float bk = -INFINITY;
-    int bi = NONE;
-#pragma unroll
-    for (int i = 0; i < PER; ++i) {
-      const int e = lane * PER + i;
-      if (avail[i] && (bi == NONE || beats(key[i], e, bk, bi))) {
-        bk = key[i];
-        bi = e;
-      }
-    }
+    float bk = sk[0];
+    int bi = si[0];
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) {
       const float ok = __shfl_xor_sync(full, bk, o);
@@ -198,9 +216,15 @@ __device__ __forceinline__ RouteSel route_select(const float* key, const RoutePa
       r.kth1 = bk;
       break;
     }
+    if (si[0] == bi) {  // this lane held the winner: drop it
 #pragma unroll
-    for (int i = 0; i < PER; ++i)
-      if (lane * PER + i == bi) avail[i] = false;
+      for (int i = 0; i + 1 < PER; ++i) {
+        sk[i] = sk[i + 1];
+        si[i] = si[i + 1];
+      }
+      sk[PER - 1] = -INFINITY;
+      si[PER - 1] = NONE;
+    }
     if (lane == k) r.my_id = bi;
   }
   return r;
