@@ -23,7 +23,6 @@
 #include "simt_gemm.cuh"
 #include "tc_gemm.cuh"
 #include "ffn_grouped.cuh"
-#include "tc_pair.cuh"
 #include "fp8.cuh"
 
 using namespace moe;
@@ -556,96 +555,10 @@ moe_status launch_ffn_tokens_m_one(const moe_config& c, const void* xp, const in
   return MOE_OK;
 }
 
-// The same GEMMs on SM pairs (tc_pair.cuh): 256-row tiles whose two CTAs share
-// one M = 256 MMA, each loading its 128 token rows and half of the 256 weight
-// rows, in a 6-deep ring of 32 KB stages.
-constexpr int kTpStages = 6;
-
-// Clusters of two that can be resident at once (one CTA per SM): the grid of
-// the persistent pair kernels.  Looked up once per kernel and device.
-template <typename Kern>
-int pair_clusters(Kern kernel, size_t smem, int threads) {
-  static std::atomic<int> cache[64];
-  int dev = 0;
-  cudaGetDevice(&dev);
-  if (dev < 0 || dev >= 64) dev = 0;
-  int n = cache[dev].load(std::memory_order_relaxed);
-  if (n > 0) return n;
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(2 * (unsigned)device_info().sms, 1, 1);
-  cfg.blockDim = dim3((unsigned)threads, 1, 1);
-  cfg.dynamicSmemBytes = smem;
-  if (cudaOccupancyMaxActiveClusters(&n, kernel, &cfg) != cudaSuccess || n < 1) {
-    (void)cudaGetLastError();
-    n = device_info().sms / 2;   // one CTA per SM fits by construction
-  }
-  cache[dev].store(n, std::memory_order_relaxed);
-  return n;
-}
-
-// Tokens-as-M GEMMs of an FFN on SM pairs: gate/up (SwiGLU into inter), then
-// down (into out).  offsets null: one dense segment of `rows` rows (the shared
-// expert); w_map/n_w as in launch_ffn_tc.
-moe_status launch_ffn_tokens_m_pair(const void* xp, const int32_t* offsets, const int32_t* kept, int segments,
-                                    int64_t rows, int h, int I, const int32_t* w_map, int n_w, const void* w13,
-                                    const void* w2, void* yp, void* inter, cudaStream_t st) {
-  using S = TpShape<kTpStages>;
-  CUtensorMap a1, b1, a2, b2;
-  MOE_TRY(make_tensor_map(&a1, xp, h, rows, kTcBM));
-  MOE_TRY(make_tensor_map(&b1, w13, h, (uint64_t)n_w * 2 * I, 128));
-  MOE_TRY(make_tensor_map(&a2, inter, I, rows, kTcBM));
-  MOE_TRY(make_tensor_map(&b2, w2, I, (uint64_t)n_w * h, 128));
-  TcParams p1{};
-  p1.offsets = offsets;
-  p1.kept = kept;
-  p1.E = offsets ? segments : 1;
-  p1.dense_rows = offsets ? 0 : (int)rows;
-  p1.w_map = w_map;
-  p1.n_tiles = (I + 127) / 128;
-  p1.k_blocks = h / kTcBK;
-  p1.b_rows = offsets ? 2LL * I : 0;
-  p1.up_rows = I;
-  p1.n_valid = I;
-  p1.out = inter;
-  p1.ldo = I;
-  TcParams p2 = p1;
-  p2.n_tiles = (h + 255) / 256;
-  p2.k_blocks = I / kTcBK;
-  p2.b_rows = offsets ? h : 0;
-  p2.up_rows = 0;
-  p2.n_valid = h;
-  p2.out = yp;
-  p2.ldo = h;
-  auto k1 = tc_pair_kernel<kTcSwiglu, kTpStages>;
-  auto k2 = tc_pair_kernel<kTcStore, kTpStages>;
-  CUDA_TRY(allow_smem(k1, S::kDynSmem));
-  CUDA_TRY(allow_smem(k2, S::kDynSmem));
-  // no more pairs than tiles (each pair takes whole 256 x 256 tiles)
-  const int64_t pairs_rows = offsets ? ((rows + 255) / 256 + segments) : (rows + 255) / 256;
-  int64_t g1 = std::min<int64_t>(pair_clusters(k1, S::kDynSmem, kTpThreads), pairs_rows * p1.n_tiles);
-  int64_t g2 = std::min<int64_t>(pair_clusters(k2, S::kDynSmem, kTpThreads), pairs_rows * p2.n_tiles);
-  k1<<<(unsigned)(2 * std::max<int64_t>(g1, 1)), kTpThreads, S::kDynSmem, st>>>(a1, b1, p1);
-  CUDA_TRY(launched());
-  k2<<<(unsigned)(2 * std::max<int64_t>(g2, 1)), kTpThreads, S::kDynSmem, st>>>(a2, b2, p2);
-  CUDA_TRY(launched());
-  return MOE_OK;
-}
-
-// 1: the tokens-as-M GEMMs (routed FFN of many rows per expert, shared expert)
-// run on SM pairs (tc_pair.cuh); 0: one SM per tile (tc_gemm.cuh).
-#ifndef MOE_TOKENS_M_PAIR
-#define MOE_TOKENS_M_PAIR 1
-#endif
-
 moe_status launch_ffn_tokens_m(const moe_config& c, const void* xp, const int32_t* offsets, const int32_t* kept,
                                const int32_t* w_map, int n_w, const void* w13, const void* w2, void* yp, void* inter,
                                cudaStream_t st) {
-#if MOE_TOKENS_M_PAIR
-  return launch_ffn_tokens_m_pair(xp, offsets, kept, nphys(c), rows_of(c), c.h, c.I, w_map, n_w, w13, w2, yp, inter,
-                                  st);
-#else
   return launch_ffn_tokens_m_one(c, xp, offsets, kept, w_map, n_w, w13, w2, yp, inter, st);
-#endif
 }
 
 // The grouped FFN: gate/up GEMM with the SwiGLU epilogue into the bf16
@@ -986,9 +899,6 @@ moe_status launch_shared_ffn(const moe_config& c, const void* x, const void* w13
     CUDA_TRY(launched());
     return MOE_OK;
   }
-#if MOE_TOKENS_M_PAIR
-  return launch_ffn_tokens_m_pair(x, nullptr, nullptr, 1, c.T, c.h, Is, nullptr, 1, w13s, w2s, ys, inter, st);
-#else
   using S = TcShape<kFfnBN, kFfnStages>;
   CUtensorMap a1, b1, a2, b2;
   MOE_TRY(make_tensor_map(&a1, x, c.h, c.T, kTcBM));
@@ -1027,7 +937,6 @@ moe_status launch_shared_ffn(const moe_config& c, const void* x, const void* w13
   k2<<<g2, kTcThreads, S::kDynSmem, st>>>(a2, b2, p2);
   CUDA_TRY(launched());
   return MOE_OK;
-#endif
 }
 
 // Device copy of an EPLB plan (moe_eplb_plan's outputs), or all null.
