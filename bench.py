@@ -57,7 +57,8 @@ FFN_TRAFFIC_RATIO = 1.0002
 FALLBACK_PEAKS = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0}
 # The other workloads of the pages, measured after the headline one.
 SWEEP = ("mixtral_8x7b", "switch_base", "deepseek_v3_decode_T32", "deepseek_v3_decode_T256",
-         "deepseek_v3_decode_T1024")
+         "deepseek_v3_decode_T1024", "deepseek_v3_block", "deepseek_v3_eplb", "deepseek_v3_fp8")
+COOL_S = 2.0   # idle before each sweep workload's timed region (the power average recovers)
 L2_FLUSH_BYTES = 256 << 20   # written between cold repetitions (L2 is 126 MB)
 
 
@@ -260,10 +261,11 @@ class Layer:
         self.cfg = cfg = moe.config_from(w)
         reuse = weights_from is not None
         self.inp = inp = device.layer_inputs(w, weights=not reuse)
-        if reuse:   # same expert shapes and seed: the same weights
-            for k in ("w13", "w2", "w13s", "w2s"):
-                if k in weights_from:
-                    inp[k] = weights_from[k]
+        if reuse:   # same expert shapes and seed: the same routed-expert weights
+            for k in ("w13", "w2"):
+                inp[k] = weights_from[k]
+            if w.shared_I > 0:
+                inp.update(device.shared_weights(w))
         dt = inp["x"].dtype
         self.R = R = moe.moe_rows(cfg)
         T, K, E, N = w.T, w.K, w.E, w.ep_size
@@ -497,6 +499,7 @@ def sweep_entry(w, weights_from, peaks, peak_kind, min_seconds):
     lay = Layer(w, weights_from)
     t0, _, _, _ = lay.timed(3, 3)
     steps = int(min(400, max(20, math.ceil(min_seconds * 1e3 / max(t0 / 3, 1e-3)))))
+    time.sleep(COOL_S)   # every workload starts cool, as the headline does on a fresh GPU
     total, stages, clocks, launches = lay.timed(steps, 2)
     e2e_ms, _, _ = lay.e2e(steps, 3)
     work = lay.work()
@@ -604,10 +607,58 @@ def run_sweep(args, headline_layer, peaks, peak_kind):
         if name == args.workload:
             continue
         w = find_workload(name)
-        reuse = base if (base is not None and name.startswith("deepseek_v3_decode")) else None
+        # the DeepSeek-V3 variants (decode, block, replicas, FP8) share the headline's routed-expert weights
+        same_experts = base is not None and name.startswith("deepseek_v3_") and w.h == 7168 and w.E == 256
+        reuse = base if same_experts else None
         res[name] = sweep_entry(w, reuse, peaks, peak_kind, args.sweep_seconds)
         torch.cuda.empty_cache()
     return res
+
+
+# ---------------------------------------------------------------------------- profiling launches
+def run_profile_launches():
+    """The launches profiled for the kernels outside the layer's default path,
+    each once, untimed (for a profiler; rank 0, one GPU): moe_route on the
+    DeepSeek-V3 T=4096 logits, then on the 32-expert DeepSeek-V3-shaped layer
+    (deepseek_v3_e32_T512, 2.8 GB of weights) moe_grouped_ffn_gather (gathered
+    gate/up, down) and moe_grouped_ffn_combine (gate/up, down with the fused
+    combine).  Layout from uniformly drawn expert ids, by the library."""
+    import torch
+
+    import expert_dispatch_bias_b300 as moe
+    import synth
+    from synth import device
+
+    w = find_workload("deepseek_v3")
+    cfg = moe.config_from(w)
+    inp = device.layer_inputs(w, weights=False)
+    L = torch.empty(w.T, w.E, device="cuda")
+    moe.moe_router_logits(cfg, inp["x"], inp["w_r"], None, L, moe.alloc_workspace(cfg, moe.MOE_OP_LOGITS))
+    ids = torch.empty(w.T, w.K, dtype=torch.int32, device="cuda")
+    wts = torch.empty(w.T, w.K, device="cuda")
+    moe.moe_route(cfg, L, inp["sel_bias"], ids, wts)
+    del inp
+    w = find_workload("deepseek_v3_e32_T512")
+    cfg = moe.config_from(w)
+    inp = device.layer_inputs(w)
+    ids = torch.from_numpy(synth.uniform_topk_ids(5, synth.TID_TEST + 80, w.T, w.E, w.K)).cuda()
+    lay = moe.alloc_layout(cfg)
+    moe.moe_dispatch_layout(cfg, ids, lay.counts, lay.kept, lay.offsets, lay.slot, lay.row_src, lay.n_ij,
+                            lay.rank_bytes, lay.stats, moe.alloc_workspace(cfg, moe.MOE_OP_LAYOUT))
+    R = moe.moe_rows(cfg)
+    xp = torch.zeros(R, w.h, dtype=torch.bfloat16, device="cuda")
+    yp = torch.zeros(R, w.h, dtype=torch.bfloat16, device="cuda")
+    y = torch.zeros(w.T, w.h, dtype=torch.bfloat16, device="cuda")
+    tw = torch.full((w.T, w.K), 1.0 / w.K, device="cuda")
+    moe.moe_permute(cfg, inp["x"], lay.slot, lay.row_src, xp)
+    moe.moe_grouped_ffn_gather(cfg, inp["x"], lay.row_src, lay.offsets, lay.kept, inp["w13"], inp["w2"], yp,
+                               moe.alloc_workspace(cfg, moe.MOE_OP_FFN))
+    moe.moe_grouped_ffn_combine(cfg, xp, lay.offsets, lay.kept, inp["w13"], inp["w2"], lay.row_src, lay.slot, tw,
+                                yp, y, moe.alloc_workspace(cfg, moe.MOE_OP_FFN_COMBINE))
+    st = moe.moe_check()
+    if st != 0:
+        raise RuntimeError(f"device error in the profiled launches: {moe.STATUS[st]}")
+    print(json.dumps({"profile_launches": "ok"}), flush=True)
 
 
 # ---------------------------------------------------------------------------- the oracle (CPU)
@@ -730,6 +781,8 @@ def main():
     ap.add_argument("--no-sweep", action="store_true", help="measure the headline workload only")
     ap.add_argument("--sweep-seconds", type=float, default=0.3, help="timed seconds per sweep workload")
     ap.add_argument("--clocks-csv", default=None, help="where to keep the clock samples of the timed region")
+    ap.add_argument("--profile-launches", action="store_true",
+                    help="run the launches profiled for kernels outside the layer's default path, untimed, and exit")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3) if args.impl == "ours" else args.warmup
 
@@ -740,6 +793,10 @@ def main():
     if args.impl == "reference":
         if rank == 0:
             print(json.dumps(run_reference(args)), flush=True)
+        return
+    if args.profile_launches:
+        if rank == 0:
+            run_profile_launches()
         return
 
     if world > 1:

@@ -43,6 +43,14 @@ def fill_uniform(t: torch.Tensor, seed: int, tensor_id: int, lo: float, hi: floa
     return t
 
 
+def shared_weights(w: workloads.Workload, device="cuda") -> dict:
+    """The shared expert's w13s [2*shared_I, h] and w2s [h, shared_I] on the device."""
+    dt = torch.float32 if w.dtype == "f32" else torch.bfloat16
+    s = workloads.sigma_in(w)
+    return {"w13s": fill_normal(torch.empty(2 * w.shared_I, w.h, dtype=dt, device=device), w.seed, synth.TID_W13S, s),
+            "w2s": fill_normal(torch.empty(w.h, w.shared_I, dtype=dt, device=device), w.seed, synth.TID_W2S, s)}
+
+
 def layer_inputs(w: workloads.Workload, device="cuda", weights=True) -> dict:
     """The workload's inputs on the device: x, w_r, w13, w2, sel_bias, logit_offset."""
     dt = torch.float32 if w.dtype == "f32" else torch.bfloat16
@@ -57,9 +65,7 @@ def layer_inputs(w: workloads.Workload, device="cuda", weights=True) -> dict:
         out["w13"] = fill_normal(torch.empty(w.E, 2 * w.I, w.h, dtype=dt, device=device), w.seed, synth.TID_W13, s)
         out["w2"] = fill_normal(torch.empty(w.E, w.h, w.I, dtype=dt, device=device), w.seed, synth.TID_W2, s)
     if weights and w.shared_I > 0:
-        out["w13s"] = fill_normal(torch.empty(2 * w.shared_I, w.h, dtype=dt, device=device), w.seed,
-                                  synth.TID_W13S, s)
-        out["w2s"] = fill_normal(torch.empty(w.h, w.shared_I, dtype=dt, device=device), w.seed, synth.TID_W2S, s)
+        out.update(shared_weights(w, device))
     if w.sel_bias is not None:
         out["sel_bias"] = fill_uniform(torch.empty(w.E, dtype=torch.float32, device=device), w.seed,
                                        synth.TID_SEL_BIAS, *w.sel_bias)
