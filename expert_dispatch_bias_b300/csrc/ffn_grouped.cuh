@@ -25,22 +25,27 @@
 // tiles ordered (expert, feature tile, token tile), so the token tiles sharing
 // a weight tile run on neighbouring SMs and the second read hits L2:
 //   warp 0      one thread issues the TMA loads of the two 128x64 weight boxes
-//               of every k-block into a WS-deep weight ring;
+//               of every k-block into the weight part of an ST-deep ring;
 //   warp 6      issues the loads of the tile's token rows (boxes of 128, 64, 32
-//               and 16 rows) into an XS-deep token ring; when the rows are
-//               gathered from x (GATHER), warps 6..6+XS-1 each own one token
-//               stage and fill it with 16-byte cp.async copies of the rows
-//               that row_src names;
+//               and 16 rows) into the token part of the same stage; when the
+//               rows are gathered from x (GATHER), warps 6..6+ST-1 each own one
+//               stage and fill its token part with 16-byte cp.async copies of
+//               the rows that row_src names;
 //   warp 1      allocates 512 TMEM columns; one thread issues tcgen05.mma
 //               (M=128, N = the tile's rows rounded up to 16, K=16), two per
-//               k-step, once both rings hold the k-block;
+//               k-step, once the stage holds the k-block;
 //   warps 2..5  drain the accumulators with tcgen05.ld (warp w reads TMEM lanes
 //               32*(w%4).. = 32 features), transpose 32 features x 32 tokens
 //               through shared memory and store 64-byte row pieces.
-// The weights stream from DRAM while the token rows are mostly L2 hits; the two
-// rings are separate so that each is refilled as soon as its own slot frees and
-// their depths can be chosen apart (the launcher's choice and the measurements
-// behind it are beside kFgTileRows).
+// The weights stream from DRAM while the token rows are mostly L2 hits.  A
+// stage has one full barrier (the weight producer's arrival with its bytes and
+// the token side's) and one empty barrier (one tcgen05.commit), so the issuing
+// thread waits once and commits once per k-block.  That thread is the MMA
+// pipe's only feeder, and with N <= 160 a k-block's eight MMAs take about 500
+// cycles: every cycle it spends elsewhere leaves the pipe idle.  So it tests
+// the next stage's barrier while the current MMAs run and keeps the
+// descriptors as base + stage offsets (the launcher's choice of tile and ring
+// and the measurements behind it are beside kFgTileRows).
 // Rows past a tile's end are computed and masked on store.  Every wait is
 // bounded; a wait that runs out raises the sticky error, and the CTA drains its
 // copies and MMAs, frees TMEM and exits.
@@ -52,15 +57,17 @@ namespace moe {
 
 constexpr int kFgThreads = 224;
 
-// Threads of a grouped-FFN CTA: 7 warps, plus XS - 1 more when the token rows
-// are gathered (one gather warp per token stage).
-template <bool GATHER, int XS>
+// Threads of a grouped-FFN CTA: 7 warps, plus ST - 1 more when the token rows
+// are gathered (one gather warp per stage).
+template <bool GATHER, int ST>
 struct FgThreads {
-  static constexpr int value = GATHER ? kFgThreads + 32 * (XS - 1) : kFgThreads;
+  static constexpr int value = GATHER ? kFgThreads + 32 * (ST - 1) : kFgThreads;
 };
 constexpr int kFgXsStride = 40;  // bf16 per row of a warp's 32x32 transpose buffer (80 B: conflict-free 16-B reads)
 
-template <int BT, int WS, int XS>
+// A stage holds one k-block: the two weight boxes, then (in a second array)
+// the token rows.
+template <int BT, int ST>
 struct FgShape {
   static_assert(BT % 16 == 0 && BT >= 128 && BT <= 256, "token tiles of 128..256 rows");
   static constexpr uint32_t kWBytes = 128 * kTcBK * 2;            // one 128-row weight box: 16 KB
@@ -68,7 +75,7 @@ struct FgShape {
   static constexpr uint32_t kXStage = BT * kTcBK * 2;             // BT token rows of 128 bytes
   static_assert(kXStage % 1024 == 0, "token stages start on 1024-byte swizzle atoms");
   static constexpr size_t kXsBytes = 4 * 32 * kFgXsStride * 2;    // transpose buffers of the 4 epilogue warps
-  static constexpr size_t kDynSmem = (size_t)WS * kWStage + (size_t)XS * kXStage + kXsBytes + 1024;
+  static constexpr size_t kDynSmem = (size_t)ST * (kWStage + kXStage) + kXsBytes + 1024;
 };
 
 struct FgParams {
@@ -246,38 +253,59 @@ __device__ __forceinline__ void fg_drain(uint32_t t_lane, uint32_t col0, uint32_
   }
 }
 
+// The two MMAs of one K=16 step: D0 += A0 X^T and D1 += A1 X^T (k-th step of
+// the stage: descriptors advance 32 bytes = 2 units).
+template <bool FP8>
+__device__ __forceinline__ void fg_mma_step(uint32_t c0, uint32_t c1, uint64_t dw0, uint64_t dw1, uint64_t dx,
+                                            uint32_t idesc, uint32_t acc, int k) {
+  if (FP8) {
+    umma_e4m3(c0, dw0 + 2 * k, dx + 2 * k, idesc, acc);
+    umma_e4m3(c1, dw1 + 2 * k, dx + 2 * k, idesc, acc);
+  } else {
+    umma_bf16(c0, dw0 + 2 * k, dx + 2 * k, idesc, acc);
+    umma_bf16(c1, dw1 + 2 * k, dx + 2 * k, idesc, acc);
+  }
+}
+
 // FP8: E4M3 operands (tcgen05.mma kind::f8f6f4), 128-element k-blocks (the
 // same 128-byte rows), results scaled by weight-row and token scales.
 // GATHER: the token rows are read straight from x through row_src, so the
-// permutation needs no buffer of its own.  Warp 6 + g fills token stage g with
-// 16-byte cp.async copies into the 128-byte-swizzled layout the MMA expects,
-// waits for its own copies, makes them visible to the tensor core's (async
-// proxy) reads with fence.proxy.async, and then arrives on the stage's barrier.
+// permutation needs no buffer of its own.  Warp 6 + g fills the token part of
+// stage g with 16-byte cp.async copies into the 128-byte-swizzled layout the
+// MMA expects, waits for its own copies, makes them visible to the tensor
+// core's (async proxy) reads with fence.proxy.async, and then arrives on the
+// stage's full barrier (all 32 lanes).
 // COMBINE (down projection, dropless): the weighted combine fused into the
 // epilogue (fg_chunk): expert rows are still staged in out (yp), and the last
 // arrival of every (token, 32-feature group) writes y.
-template <int EPI, int BT, int WS, int XS, bool FP8 = false, bool GATHER = false, bool COMBINE = false>
-__global__ void __launch_bounds__(FgThreads<GATHER, XS>::value, 1)
+// After an abort the producers may have armed a stage's full barrier on one
+// side only; once every role has stopped, thread 0 adds the missing side's
+// arrivals and waits for the last armed phase of every stage, so no copy is
+// still landing when the CTA's shared memory is released.
+template <int EPI, int BT, int ST, bool FP8 = false, bool GATHER = false, bool COMBINE = false>
+__global__ void __launch_bounds__(FgThreads<GATHER, ST>::value, 1)
     ffn_grouped_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_constant__ FgTokenMaps maps,
                        FgParams p) {
   const CUtensorMap* map_x = maps.m;
-  using S = FgShape<BT, WS, XS>;
+  using S = FgShape<BT, ST>;
+  constexpr uint32_t kXArrivals = GATHER ? 32u : 1u;   // token-side arrivals per stage fill
   extern __shared__ uint8_t dyn_smem[];
-  __shared__ __align__(8) uint64_t wfull[WS], wempty[WS], xfull[XS], xempty[XS];
+  __shared__ __align__(8) uint64_t full[ST], empty[ST];
   __shared__ __align__(8) uint64_t tmem_full[2], tmem_empty[2], drain_bar;
   __shared__ uint32_t tmem_holder;
   __shared__ volatile uint32_t abort_flag;
+  __shared__ volatile uint32_t armed_w[ST], armed_x[ST];   // fills of each stage by each side
   __shared__ int32_t mbp[1025];
   __shared__ int32_t scan_scratch[33];
-  __shared__ int32_t src_rows[GATHER ? XS : 1][GATHER ? BT : 1];  // gather: per warp, source token of each row
+  __shared__ int32_t src_rows[GATHER ? ST : 1][GATHER ? BT : 1];  // gather: per warp, source token of each row
 
   uint8_t* ring_w = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(dyn_smem) + 1023) & ~uintptr_t(1023));
-  uint8_t* ring_x = ring_w + (size_t)WS * S::kWStage;
-  __nv_bfloat16* xs_all = reinterpret_cast<__nv_bfloat16*>(ring_x + (size_t)XS * S::kXStage);
+  uint8_t* ring_x = ring_w + (size_t)ST * S::kWStage;
+  __nv_bfloat16* xs_all = reinterpret_cast<__nv_bfloat16*>(ring_x + (size_t)ST * S::kXStage);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
   // ---- per-expert token-tile prefix (every CTA computes it from kept)
-  constexpr int NT = FgThreads<GATHER, XS>::value;
+  constexpr int NT = FgThreads<GATHER, ST>::value;
   for (int e = tid; e < p.E; e += NT) mbp[e] = (p.kept[e] + BT - 1) / BT;
   __syncthreads();
   const int32_t total_tt = block_exclusive_scan(mbp, p.E, scan_scratch);
@@ -285,13 +313,11 @@ __global__ void __launch_bounds__(FgThreads<GATHER, XS>::value, 1)
   const int total_tiles = total_tt * p.f_tiles;
 
   if (tid == 0) {
-    for (int s = 0; s < WS; ++s) {
-      mbar_init(&wfull[s], 1);
-      mbar_init(&wempty[s], 1);
-    }
-    for (int s = 0; s < XS; ++s) {
-      mbar_init(&xfull[s], GATHER ? 32 : 1);   // gather: every lane of the stage's warp arrives
-      mbar_init(&xempty[s], 1);
+    for (int s = 0; s < ST; ++s) {
+      mbar_init(&full[s], 1 + kXArrivals);
+      mbar_init(&empty[s], 1);
+      armed_w[s] = 0;
+      armed_x[s] = 0;
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(&tmem_full[a], 1);
@@ -317,7 +343,6 @@ __global__ void __launch_bounds__(FgThreads<GATHER, XS>::value, 1)
     if (lane == 0) {
       int stage = 0;
       uint32_t phase = 0;
-      uint32_t armed = 0, armed_parity = 0;
       for (int t = blockIdx.x; t < total_tiles && !abort_flag; t += gridDim.x) {
         const FgTile tl = fg_decode<BT>(t, mbp, p);
         // weight rows of the tile's two 128-row boxes
@@ -325,27 +350,22 @@ __global__ void __launch_bounds__(FgThreads<GATHER, XS>::value, 1)
         const int64_t a0 = we * p.a_rows + (EPI == kTcSwiglu ? 128 * tl.ft : 256 * tl.ft);
         const int64_t a1 = EPI == kTcSwiglu ? a0 + p.up_rows : a0 + 128;
         for (int kb = 0; kb < p.k_blocks; ++kb) {
-          if (!mbar_wait(&wempty[stage], phase ^ 1u, &abort_flag)) {
+          if (!mbar_wait(&empty[stage], phase ^ 1u, &abort_flag)) {
             abort_flag = 1;
             raise_error(kErrTimeout);
             break;
           }
           uint8_t* sw = ring_w + (size_t)stage * S::kWStage;
           const int kx = kb * (FP8 ? 128 : kTcBK);
-          mbar_expect_tx(&wfull[stage], S::kWStage);
-          tma_load_2d(sw, &map_w, kx, (int)a0, &wfull[stage]);
-          tma_load_2d(sw + S::kWBytes, &map_w, kx, (int)a1, &wfull[stage]);
-          armed |= 1u << stage;
-          armed_parity = (armed_parity & ~(1u << stage)) | (phase << stage);
-          if (++stage == WS) {
+          mbar_expect_tx(&full[stage], S::kWStage);
+          tma_load_2d(sw, &map_w, kx, (int)a0, &full[stage]);
+          tma_load_2d(sw + S::kWBytes, &map_w, kx, (int)a1, &full[stage]);
+          armed_w[stage] = armed_w[stage] + 1u;
+          if (++stage == ST) {
             stage = 0;
             phase ^= 1u;
           }
         }
-      }
-      if (abort_flag) {  // let every armed copy land before shared memory is released
-        for (int s = 0; s < WS; ++s)
-          if ((armed >> s) & 1u) mbar_wait(&wfull[s], (armed_parity >> s) & 1u);
       }
     }
   } else if (!GATHER && warp == 6) {
@@ -353,44 +373,38 @@ __global__ void __launch_bounds__(FgThreads<GATHER, XS>::value, 1)
     if (lane == 0) {
       int stage = 0;
       uint32_t phase = 0;
-      uint32_t armed = 0, armed_parity = 0;
       for (int t = blockIdx.x; t < total_tiles && !abort_flag; t += gridDim.x) {
         const FgTile tl = fg_decode<BT>(t, mbp, p);
         const int n16 = (int)round16(tl.n);
         const uint32_t x_bytes = (uint32_t)n16 * (uint32_t)(kTcBK * 2);
         for (int kb = 0; kb < p.k_blocks; ++kb) {
-          if (!mbar_wait(&xempty[stage], phase ^ 1u, &abort_flag)) {
+          if (!mbar_wait(&empty[stage], phase ^ 1u, &abort_flag)) {
             abort_flag = 1;
             raise_error(kErrTimeout);
             break;
           }
           uint8_t* sx = ring_x + (size_t)stage * S::kXStage;
           const int kx = kb * (FP8 ? 128 : kTcBK);
-          mbar_expect_tx(&xfull[stage], x_bytes);
+          mbar_expect_tx(&full[stage], x_bytes);
           // round16(n) rows as boxes of 128 rows, then at most one each of 64, 32 and 16
           int b = 0;
-          for (; b + 128 <= n16; b += 128) tma_load_2d(sx + b * (kTcBK * 2), &map_x[0], kx, tl.r0 + b, &xfull[stage]);
-          if ((n16 - b) & 64) { tma_load_2d(sx + b * (kTcBK * 2), &map_x[1], kx, tl.r0 + b, &xfull[stage]); b += 64; }
-          if ((n16 - b) & 32) { tma_load_2d(sx + b * (kTcBK * 2), &map_x[2], kx, tl.r0 + b, &xfull[stage]); b += 32; }
-          if ((n16 - b) & 16) tma_load_2d(sx + b * (kTcBK * 2), &map_x[3], kx, tl.r0 + b, &xfull[stage]);
-          armed |= 1u << stage;
-          armed_parity = (armed_parity & ~(1u << stage)) | (phase << stage);
-          if (++stage == XS) {
+          for (; b + 128 <= n16; b += 128) tma_load_2d(sx + b * (kTcBK * 2), &map_x[0], kx, tl.r0 + b, &full[stage]);
+          if ((n16 - b) & 64) { tma_load_2d(sx + b * (kTcBK * 2), &map_x[1], kx, tl.r0 + b, &full[stage]); b += 64; }
+          if ((n16 - b) & 32) { tma_load_2d(sx + b * (kTcBK * 2), &map_x[2], kx, tl.r0 + b, &full[stage]); b += 32; }
+          if ((n16 - b) & 16) tma_load_2d(sx + b * (kTcBK * 2), &map_x[3], kx, tl.r0 + b, &full[stage]);
+          armed_x[stage] = armed_x[stage] + 1u;
+          if (++stage == ST) {
             stage = 0;
             phase ^= 1u;
           }
         }
       }
-      if (abort_flag) {
-        for (int s = 0; s < XS; ++s)
-          if ((armed >> s) & 1u) mbar_wait(&xfull[s], (armed_parity >> s) & 1u);
-      }
     }
-  } else if (GATHER && warp >= 6 && warp < 6 + XS) {
+  } else if (GATHER && warp >= 6 && warp < 6 + ST) {
     // ------------------------------------------------------------ token gather (warp 6 + g fills stage g)
-    // k-block j of the CTA's sequence uses token stage j % XS, so this warp
-    // takes every XS-th k-block.  Its copies are complete (cp.async.wait_group)
-    // and fenced before it arrives, so nothing is in flight when it exits.
+    // k-block j of the CTA's sequence uses stage j % ST, so this warp takes
+    // every ST-th k-block.  Its copies are complete (cp.async.wait_group) and
+    // fenced before it arrives, so nothing is in flight when it exits.
     const int g = warp - 6;
     int32_t* srow = src_rows[g];
     uint8_t* sx = ring_x + (size_t)g * S::kXStage;
@@ -403,7 +417,7 @@ __global__ void __launch_bounds__(FgThreads<GATHER, XS>::value, 1)
       const FgTile tl = fg_decode<BT>(t, mbp, p);
       const int n16 = (int)round16(tl.n);
       // the first k-block of this tile that is ours
-      int kb = ((g - j) % XS + XS) % XS;
+      int kb = ((g - j) % ST + ST) % ST;
       if (kb < p.k_blocks) {
         __syncwarp();
         for (int i = lane; i < n16; i += 32) {
@@ -413,10 +427,10 @@ __global__ void __launch_bounds__(FgThreads<GATHER, XS>::value, 1)
         }
         __syncwarp();
       }
-      for (; kb < p.k_blocks; kb += XS) {
+      for (; kb < p.k_blocks; kb += ST) {
         // every lane waits (each of its copies must follow the MMAs' reads of
         // the stage); the warp gives up together if any lane's wait ran out
-        const bool w_ok = mbar_wait(&xempty[g], phase ^ 1u, &abort_flag);
+        const bool w_ok = mbar_wait(&empty[g], phase ^ 1u, &abort_flag);
         if (!__all_sync(0xffffffffu, w_ok)) {
           if (lane == 0) {
             abort_flag = 1;
@@ -434,7 +448,9 @@ __global__ void __launch_bounds__(FgThreads<GATHER, XS>::value, 1)
         }
         asm volatile("cp.async.commit_group;\n\tcp.async.wait_group 0;" ::: "memory");
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-        mbar_arrive(&xfull[g]);
+        mbar_arrive(&full[g]);
+        __syncwarp();
+        if (lane == 0) armed_x[g] = armed_x[g] + 1u;
         phase ^= 1u;
       }
       j += p.k_blocks;
@@ -442,58 +458,48 @@ __global__ void __launch_bounds__(FgThreads<GATHER, XS>::value, 1)
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
-      int ws = 0, xs_ = 0;
-      uint32_t wph = 0, xph = 0;
+      // descriptors of stage 0's operands; stage s adds s stage sizes (start
+      // addresses stay below 256 KB, so the 14-bit address field never carries)
+      const uint64_t dwb = umma_desc_sw128(smem_u32(ring_w)), dxb = umma_desc_sw128(smem_u32(ring_x));
+      int st = 0;
+      uint32_t ph = 0;
+      bool ready = false;        // full[st] already seen complete by the early test
+      bool ok = true;
       int slot = 0;              // TMEM slot of the next tile of at most 128 rows
       uint32_t slot_phase = 0;   // bit s: uses of slot s so far, mod 2
-      for (int t = blockIdx.x; t < total_tiles && !abort_flag; t += gridDim.x) {
+      for (int t = blockIdx.x; t < total_tiles && ok && !abort_flag; t += gridDim.x) {
         const FgTile tl = fg_decode<BT>(t, mbp, p);
         const bool big = tl.n > 128;
         const uint32_t idesc = FP8 ? umma_idesc_e4m3(128, (int)round16(tl.n)) : umma_idesc_bf16(128, (int)round16(tl.n));
         // big: D0 = slot 0, D1 = slot 1; else D0, D1 = the two halves of `slot`
         const int s0 = big ? 0 : slot;
         const uint32_t c0 = tmem_base + (uint32_t)(s0 * 256), c1 = big ? tmem_base + 256u : c0 + 128u;
-        bool ok = mbar_wait(&tmem_empty[s0], ((slot_phase >> s0) & 1u) ^ 1u, &abort_flag);
+        ok = mbar_wait(&tmem_empty[s0], ((slot_phase >> s0) & 1u) ^ 1u, &abort_flag);
         if (ok && big) ok = mbar_wait(&tmem_empty[1], ((slot_phase >> 1) & 1u) ^ 1u, &abort_flag);
-        if (!ok) {
-          abort_flag = 1;
-          raise_error(kErrTimeout);
-          break;
-        }
+        if (!ok) break;
         tc_fence_after();
         for (int kb = 0; kb < p.k_blocks; ++kb) {
-          if (!mbar_wait(&wfull[ws], wph, &abort_flag) || !mbar_wait(&xfull[xs_], xph, &abort_flag)) {
-            abort_flag = 1;
-            raise_error(kErrTimeout);
+          if (!ready && !mbar_wait(&full[st], ph, &abort_flag)) {
             ok = false;
             break;
           }
           tc_fence_after();
-          // descriptors of the stage's operands; a K=16 step advances 32 bytes (2 units)
-          const uint64_t dw0 = umma_desc_sw128(smem_u32(ring_w + (size_t)ws * S::kWStage));
+          const uint64_t dw0 = dwb + (uint64_t)((uint32_t)st * (S::kWStage >> 4));
           const uint64_t dw1 = dw0 + (S::kWBytes >> 4);
-          const uint64_t dx = umma_desc_sw128(smem_u32(ring_x + (size_t)xs_ * S::kXStage));
-#pragma unroll
-          for (int k = 0; k < kTcBK / 16; ++k) {
-            const uint32_t acc = (kb | k) != 0 ? 1u : 0u;
-            if (FP8) {
-              umma_e4m3(c0, dw0 + 2 * k, dx + 2 * k, idesc, acc);
-              umma_e4m3(c1, dw1 + 2 * k, dx + 2 * k, idesc, acc);
-            } else {
-              umma_bf16(c0, dw0 + 2 * k, dx + 2 * k, idesc, acc);
-              umma_bf16(c1, dw1 + 2 * k, dx + 2 * k, idesc, acc);
-            }
-          }
-          umma_commit(&wempty[ws]);
-          umma_commit(&xempty[xs_]);
-          if (++ws == WS) {
-            ws = 0;
-            wph ^= 1u;
-          }
-          if (++xs_ == XS) {
-            xs_ = 0;
-            xph ^= 1u;
-          }
+          const uint64_t dx = dxb + (uint64_t)((uint32_t)st * (S::kXStage >> 4));
+          const int nst = st + 1 == ST ? 0 : st + 1;
+          const uint32_t nph = st + 1 == ST ? ph ^ 1u : ph;
+          static_assert(kTcBK / 16 == 4, "four K=16 steps per k-block");
+          fg_mma_step<FP8>(c0, c1, dw0, dw1, dx, idesc, kb != 0 ? 1u : 0u, 0);
+          fg_mma_step<FP8>(c0, c1, dw0, dw1, dx, idesc, 1u, 1);
+          // test the next stage while these MMAs run: a barrier that has
+          // completed stays so until this thread releases the stage
+          ready = mbar_try_wait(&full[nst], nph);
+          fg_mma_step<FP8>(c0, c1, dw0, dw1, dx, idesc, 1u, 2);
+          fg_mma_step<FP8>(c0, c1, dw0, dw1, dx, idesc, 1u, 3);
+          umma_commit(&empty[st]);
+          st = nst;
+          ph = nph;
         }
         if (!ok) break;
         umma_commit(&tmem_full[s0]);
@@ -504,6 +510,10 @@ __global__ void __launch_bounds__(FgThreads<GATHER, XS>::value, 1)
         } else {
           slot ^= 1;
         }
+      }
+      if (!ok) {
+        abort_flag = 1;
+        raise_error(kErrTimeout);
       }
       umma_commit(&drain_bar);
       mbar_wait(&drain_bar, 0u);
@@ -563,6 +573,20 @@ __global__ void __launch_bounds__(FgThreads<GATHER, XS>::value, 1)
 
   tc_fence_before();
   __syncthreads();
+  if (abort_flag) {
+    // every role has stopped: give each stage's last armed phase the arrival
+    // of the side that did not arm it, then wait until its copies have landed
+    if (tid == 0) {
+      for (int s = 0; s < ST; ++s) {
+        const uint32_t w = armed_w[s], x = armed_x[s];
+        if (w > x) mbar_arrive_n(&full[s], kXArrivals);
+        else if (x > w) mbar_arrive(&full[s]);
+        const uint32_t n = w > x ? w : x;
+        if (n > 0) mbar_wait(&full[s], (n - 1u) & 1u);
+      }
+    }
+    __syncthreads();
+  }
   if (warp == 1) {
     tc_fence_after();
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base), "r"(512) : "memory");

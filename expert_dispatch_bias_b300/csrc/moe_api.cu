@@ -564,12 +564,13 @@ moe_status launch_ffn_tokens_m(const moe_config& c, const void* xp, const int32_
 // The grouped FFN: gate/up GEMM with the SwiGLU epilogue into the bf16
 // intermediate, then the down GEMM into yp, both with the expert weights as
 // the MMA's M operand and the expert's token rows as N (ffn_grouped.cuh).
-// Token tiles of up to 160 rows; a ring of 4 weight k-blocks (32 KB each) and
-// one of 4 token k-blocks (20 KB each).  Measured at DeepSeek-V3 T=4096: 3.94
-// ms; rings of 5 + 2 (5.20 ms), 4 + 3 (4.13), 128-row tiles with 5 + 3 (4.30)
-// and 256-row tiles with 4 + 2 (5.13) starve the MMA of token k-blocks, whose
-// L2 latency under this load needs four in flight.
-constexpr int kFgTileRows = 160, kFgWStages = 4, kFgXStages = 4;
+// Token tiles of up to 160 rows; a ring of 4 stages, each a k-block of weights
+// (32 KB) and of token rows (20 KB).  Measured at DeepSeek-V3 T=4096 with
+// separately sized weight and token rings: 4 + 4 stages 3.94 ms; 5 + 2 (5.20
+// ms), 4 + 3 (4.13), 128-row tiles with 5 + 3 (4.30) and 256-row tiles with
+// 4 + 2 (5.13) starve the MMA of token k-blocks, whose L2 latency under this
+// load needs four in flight.  Equal depths let one barrier pair serve a stage.
+constexpr int kFgTileRows = 160, kFgStages = 4;
 // The weighted combine fused into the down projection (dropless layers).
 struct FusedCombine {
   const int32_t* row_src;
@@ -582,11 +583,11 @@ struct FusedCombine {
 // row_src non-null: the gate/up GEMM gathers its rows from x = xp through row_src
 // (no permuted copy of x); else xp holds the permuted rows.  comb non-null: the
 // down projection also writes the combine into comb->y.
-template <int BT, int WS, int XS>
+template <int BT, int ST>
 moe_status launch_ffn_grouped(const moe_config& c, const void* xp, const int32_t* offsets, const int32_t* kept,
                               const int32_t* w_map, int n_w, const void* w13, const void* w2, void* yp, void* inter,
                               cudaStream_t st, const int32_t* row_src = nullptr, const FusedCombine* comb = nullptr) {
-  using S = FgShape<BT, WS, XS>;
+  using S = FgShape<BT, ST>;
   const int64_t R = rows_of(c);
   const int grid = device_info().sms;
   CUtensorMap w1m, w2m;
@@ -632,12 +633,12 @@ moe_status launch_ffn_grouped(const moe_config& c, const void* xp, const int32_t
     p2.arrive = comb->arrive;
   }
   const bool gather = row_src != nullptr;
-  auto k1 = gather ? ffn_grouped_kernel<kTcSwiglu, BT, WS, XS, false, true> : ffn_grouped_kernel<kTcSwiglu, BT, WS, XS>;
-  auto k2 = comb != nullptr ? ffn_grouped_kernel<kTcStore, BT, WS, XS, false, false, true>
-                            : ffn_grouped_kernel<kTcStore, BT, WS, XS>;
+  auto k1 = gather ? ffn_grouped_kernel<kTcSwiglu, BT, ST, false, true> : ffn_grouped_kernel<kTcSwiglu, BT, ST>;
+  auto k2 = comb != nullptr ? ffn_grouped_kernel<kTcStore, BT, ST, false, false, true>
+                            : ffn_grouped_kernel<kTcStore, BT, ST>;
   CUDA_TRY(allow_smem(k1, S::kDynSmem));
   CUDA_TRY(allow_smem(k2, S::kDynSmem));
-  k1<<<grid, gather ? FgThreads<true, XS>::value : kFgThreads, S::kDynSmem, st>>>(w1m, x1, p1);
+  k1<<<grid, gather ? FgThreads<true, ST>::value : kFgThreads, S::kDynSmem, st>>>(w1m, x1, p1);
   CUDA_TRY(launched());
   k2<<<grid, kFgThreads, S::kDynSmem, st>>>(w2m, x2, p2);
   CUDA_TRY(launched());
@@ -660,7 +661,7 @@ moe_status launch_ffn_tc(const moe_config& c, const void* xp, const int32_t* off
   if ((int64_t)n_w * 2 * c.I >= INT32_MAX || (int64_t)n_w * c.h >= INT32_MAX) return MOE_ERR_UNSUPPORTED;
   if (expected_rows_per_expert(c) > MOE_FFN_SWAP_MAX_ROWS)
     return launch_ffn_tokens_m(c, xp, offsets, kept, w_map, n_w, w13, w2, yp, inter, st);
-  return launch_ffn_grouped<kFgTileRows, kFgWStages, kFgXStages>(c, xp, offsets, kept, w_map, n_w, w13, w2, yp, inter, st);
+  return launch_ffn_grouped<kFgTileRows, kFgStages>(c, xp, offsets, kept, w_map, n_w, w13, w2, yp, inter, st);
 }
 
 // Router logits of a bf16 layer on the tensor cores: one segment of T rows
@@ -773,7 +774,7 @@ moe_status launch_ffn_fp8(const moe_config& c, const uint8_t* xq, const float* s
   __nv_bfloat16* inter = reinterpret_cast<__nv_bfloat16*>(w);
   uint8_t* interq = reinterpret_cast<uint8_t*>(w + align_up((size_t)R * c.I * 2, 256));
   float* sinter = reinterpret_cast<float*>(w + align_up((size_t)R * c.I * 2, 256) + align_up((size_t)R * c.I, 256));
-  using S = FgShape<kFgTileRows, kFgWStages, kFgXStages>;
+  using S = FgShape<kFgTileRows, kFgStages>;
   CUtensorMap w1m, w2m;
   FgTokenMaps x1, x2;
   MOE_TRY(make_tensor_map(&w1m, w13q, c.h, (uint64_t)n_w * 2 * c.I, 128, true));
@@ -807,8 +808,8 @@ moe_status launch_ffn_fp8(const moe_config& c, const uint8_t* xq, const float* s
   p2.w_scale = s2;
   p2.x_scale = sinter;
   const int grid = device_info().sms;
-  auto k1 = ffn_grouped_kernel<kTcSwiglu, kFgTileRows, kFgWStages, kFgXStages, true>;
-  auto k2 = ffn_grouped_kernel<kTcStore, kFgTileRows, kFgWStages, kFgXStages, true>;
+  auto k1 = ffn_grouped_kernel<kTcSwiglu, kFgTileRows, kFgStages, true>;
+  auto k2 = ffn_grouped_kernel<kTcStore, kFgTileRows, kFgStages, true>;
   CUDA_TRY(allow_smem(k1, S::kDynSmem));
   CUDA_TRY(allow_smem(k2, S::kDynSmem));
   k1<<<grid, kFgThreads, S::kDynSmem, st>>>(w1m, x1, p1);
@@ -847,7 +848,7 @@ moe_status launch_ffn_gather(const moe_config& c, const void* x, const int32_t* 
   if (rows_of(c) == 0 || c.T == 0) return MOE_OK;
   if (c.dtype != MOE_BF16 || expected_rows_per_expert(c) > MOE_FFN_SWAP_MAX_ROWS) return MOE_ERR_UNSUPPORTED;
   if ((int64_t)n_w * 2 * c.I >= INT32_MAX || (int64_t)n_w * c.h >= INT32_MAX) return MOE_ERR_UNSUPPORTED;
-  return launch_ffn_grouped<kFgTileRows, kFgWStages, kFgXStages>(c, x, offsets, kept, w_map, n_w, w13, w2, yp, inter, st,
+  return launch_ffn_grouped<kFgTileRows, kFgStages>(c, x, offsets, kept, w_map, n_w, w13, w2, yp, inter, st,
                                                     row_src);
 }
 
@@ -1223,7 +1224,7 @@ moe_status moe_grouped_ffn_combine(const moe_config* cfg, const void* xp, const 
   fc.topk_w = topk_w;
   fc.y = y;
   fc.arrive = reinterpret_cast<uint32_t*>(static_cast<char*>(workspace) + ffn_ws_bytes(*cfg));
-  return launch_ffn_grouped<kFgTileRows, kFgWStages, kFgXStages>(*cfg, xp, offsets, kept, nullptr, cfg->E, w13, w2, yp,
+  return launch_ffn_grouped<kFgTileRows, kFgStages>(*cfg, xp, offsets, kept, nullptr, cfg->E, w13, w2, yp,
                                                                  static_cast<char*>(workspace) + 256,
                                                                  as_stream(stream), nullptr, &fc);
 }

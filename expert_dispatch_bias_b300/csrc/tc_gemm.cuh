@@ -342,8 +342,12 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
       constexpr uint32_t idesc = umma_idesc_bf16(kTcBM, BN);
+      // descriptor of stage 0's A tile; stage s adds s stage sizes (start
+      // addresses stay below 256 KB, so the 14-bit address field never carries)
+      const uint64_t d0 = umma_desc_sw128(smem_u32(tiles));
       int stage = 0;
       uint32_t phase = 0;
+      bool ready = false;   // full_bar[stage] already seen complete by the early test
       int acc = 0;
       uint32_t acc_phase = 0;
       for (int t = blockIdx.x; t < total_tiles && !abort_flag; t += gridDim.x) {
@@ -358,25 +362,30 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         int kb0, kb1;
         tc_k_range(t % KS, KS, p.k_blocks, &kb0, &kb1);
         for (int kb = kb0; kb < kb1; ++kb) {
-          if (!mbar_wait(&full_bar[stage], phase, &abort_flag)) {
+          if (!ready && !mbar_wait(&full_bar[stage], phase, &abort_flag)) {
             abort_flag = 1;
             raise_error(kErrTimeout);
             ok = false;
             break;
           }
           tc_fence_after();
-          const uint32_t sa = smem_u32(tiles + (size_t)stage * S::kStageBytes);
-          const uint32_t sb = sa + S::kABytes;
-#pragma unroll
-          for (int k = 0; k < kTcBK / 16; ++k) {
-            umma_bf16(d_tmem, umma_desc_sw128(sa + k * 32), umma_desc_sw128(sb + k * 32), idesc,
-                      (kb != kb0 || k != 0) ? 1u : 0u);
-          }
+          // a K=16 step advances 32 bytes (2 descriptor units) in both tiles
+          const uint64_t da = d0 + (uint64_t)((uint32_t)stage * (S::kStageBytes >> 4));
+          const uint64_t db = da + (S::kABytes >> 4);
+          const int next = stage + 1 == STAGES ? 0 : stage + 1;
+          const uint32_t next_phase = stage + 1 == STAGES ? phase ^ 1u : phase;
+          static_assert(kTcBK / 16 == 4, "four K=16 steps per k-block");
+          umma_bf16(d_tmem, da, db, idesc, kb != kb0 ? 1u : 0u);
+          umma_bf16(d_tmem, da + 2, db + 2, idesc, 1u);
+          // test the next stage while these MMAs run (the single issuing thread
+          // is the pipe's only feeder); a completed phase stays complete until
+          // this thread releases the stage
+          ready = mbar_try_wait(&full_bar[next], next_phase);
+          umma_bf16(d_tmem, da + 4, db + 4, idesc, 1u);
+          umma_bf16(d_tmem, da + 6, db + 6, idesc, 1u);
           umma_commit(&empty_bar[stage]);
-          if (++stage == STAGES) {
-            stage = 0;
-            phase ^= 1u;
-          }
+          stage = next;
+          phase = next_phase;
         }
         if (!ok) break;
         umma_commit(&tmem_full[acc]);
