@@ -49,11 +49,11 @@ if ROOT not in sys.path:
 METRIC = "MoE-layer tokens/s at DeepSeek-V3 shape; permute GB/s & GEMM % of peak"
 # DRAM bytes (read + write) of the grouped FFN's two launches over its
 # algorithmic bytes, from one ncu capture of the 32-expert DeepSeek-V3-shaped
-# layer (deepseek_v3_e32_T512: 2.9703 GB measured / 2.9696 GB algorithmic, the
-# kernel with separate weight and token rings).  Both scale with the touched
+# layer (deepseek_v3_e32_T512: 2.9698 GB measured / 2.9696 GB algorithmic, the
+# kernel with one barrier pair per ring stage).  Both scale with the touched
 # experts and kept rows, so a full launch's traffic is this ratio times its
 # algorithmic bytes.  Re-measure whenever the kernel changes.
-FFN_TRAFFIC_RATIO = 1.0002
+FFN_TRAFFIC_RATIO = 1.0001
 FALLBACK_PEAKS = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0}
 # The other workloads of the pages, measured after the headline one.
 SWEEP = ("mixtral_8x7b", "switch_base", "deepseek_v3_decode_T32", "deepseek_v3_decode_T256",
