@@ -230,7 +230,9 @@ moe_status moe_dispatch_layout(const moe_config* cfg, const int32_t* topk_ids, i
  * is refused with MOE_ERR_WORKSPACE_TOO_SMALL before any launch.  The call
  * allocates nothing: no cudaMalloc, no cudaFree.  Its first call on a device
  * looks up the array's device address for that device (cudaGetSymbolAddress),
- * so make that first call before any stream capture.  Every call clears the
+ * so make that first call before any stream capture; the address is kept for
+ * the life of the process, so after cudaDeviceReset on a device this call must
+ * not be used on that device again.  Every call clears the
  * part of the array that must start at zero.  All calls on a device share the
  * one array: two calls that overlap on the GPU (different streams, no ordering
  * between them) race and give wrong results; serialise them. */
