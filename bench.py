@@ -13,8 +13,9 @@ of expert weights at the DeepSeek-V3 shape) is far larger than the 126 MB L2.
 
 ``e2e`` repeats the measurement through moe_layer_forward_host: the
 host->device copy of x from pinned memory, the layer and the device->host
-copy of y are all inside its timed region, every step; two streams take
-alternate steps so one step's copies overlap the other's compute.
+copy of y are all inside its timed region, every step; three streams take
+the steps in turn, so one step's host->device copy, another's layer and a
+third's device->host copy can run at the same time.
 
 After the headline workload the same run measures every other workload of
 the pages (Mixtral, Switch-Base, the DeepSeek-V3 decode sweep) into
@@ -54,6 +55,10 @@ METRIC = "MoE-layer tokens/s at DeepSeek-V3 shape; permute GB/s & GEMM % of peak
 # experts and kept rows, so a full launch's traffic is this ratio times its
 # algorithmic bytes.  Re-measure whenever the kernel changes.
 FFN_TRAFFIC_RATIO = 1.0001
+# Streams of the end-to-end run: with three, the copy in, the layer and the
+# copy out of three different steps overlap (two leave a step's copy in
+# waiting for the copy out of the step before it on the same stream).
+E2E_LANES = 3
 FALLBACK_PEAKS = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0}
 # The other workloads of the pages, measured after the headline one.
 SWEEP = ("mixtral_8x7b", "switch_base", "deepseek_v3_decode_T32", "deepseek_v3_decode_T256",
@@ -360,8 +365,8 @@ class Layer:
 
     def e2e(self, steps, warmup, world=1):
         """The same steps through the public call with HOST activations: pinned x
-        in, y out, both copies inside the timed region every step, on two
-        streams that take alternate steps.  Returns (ms, bytes in, bytes out)."""
+        in, y out, both copies inside the timed region every step, on three
+        streams that take the steps in turn.  Returns (ms, bytes in, bytes out)."""
         import torch
         import torch.distributed as dist
 
@@ -374,7 +379,7 @@ class Layer:
                           cfg, moe.MOE_OP_LAYER_FP8 if self.kind == "fp8" else moe.MOE_OP_LAYER),
                       xd=None if host_call else torch.empty_like(inp["x"]),
                       yd=None if host_call else torch.empty_like(self.y))
-                 for _ in range(2)]
+                 for _ in range(E2E_LANES)]
 
         def step(i):
             ln = lanes[i % len(lanes)]
@@ -391,7 +396,7 @@ class Layer:
                     self.call(ln["yd"], None, ln["ws"], stream=ln["stream"])
                     ln["y"].copy_(ln["yd"], non_blocking=True)
 
-        for i in range(max(2, warmup)):
+        for i in range(max(E2E_LANES, warmup)):
             step(i)
         torch.cuda.synchronize()
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
