@@ -325,9 +325,12 @@ class Layer:
 
     def timed(self, steps, warmup, world=1, clocks_csv=None):
         """W untimed steps, then exactly `steps` steps between a barrier and a
-        synchronize on both sides; every step is one library call that records
-        its own stage events.  Returns (total ms, per-stage mean ms, clocks,
-        launches)."""
+        synchronize on both sides, one library call each, timed by one event
+        before the first and one after the last (events between the kernels
+        would stop a kernel from starting while its predecessor finishes).
+        Then the same number of steps again, each recording its stage events,
+        for the per-stage means.  Returns (total ms, per-stage mean ms,
+        clocks, launches)."""
         import torch
         import torch.distributed as dist
 
@@ -344,13 +347,16 @@ class Layer:
             for e in evs:
                 e.record(self.stream)
         outs = [moe.layer_out(stage_events=evs, **self.out) for evs in events]
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         if world > 1:
             dist.barrier()
         torch.cuda.synchronize()
         launches0 = moe.moe_launch_count()   # the library counts every kernel it launches
         with ClockSampler(torch.cuda.current_device(), csv_path=clocks_csv) as clk:
-            for o in outs:
-                self.call(self.y, o, self.ws)
+            e0.record(self.stream)
+            for _ in range(steps):
+                self.call(self.y, plain, self.ws)
+            e1.record(self.stream)
             torch.cuda.synchronize()
         launches = moe.moe_launch_count() - launches0
         if world > 1:
@@ -358,7 +364,13 @@ class Layer:
         st = moe.moe_check()
         if st != 0:
             raise RuntimeError(f"device error in the timed region: {moe.STATUS[st]}")
-        total = events[0][0].elapsed_time(events[-1][n_ev - 1])
+        total = e0.elapsed_time(e1)
+        for o in outs:
+            self.call(self.y, o, self.ws)
+        torch.cuda.synchronize()
+        st = moe.moe_check()
+        if st != 0:
+            raise RuntimeError(f"device error in the stage-timed steps: {moe.STATUS[st]}")
         stages = {s: statistics.mean(events[i][j].elapsed_time(events[i][j + 1]) for i in range(steps))
                   for j, s in enumerate(moe.LAYER_STAGES)}
         return total, stages, clk.summary(), launches

@@ -286,6 +286,7 @@ template <int EPI, int BT, int ST, bool FP8 = false, bool GATHER = false, bool C
 __global__ void __launch_bounds__(FgThreads<GATHER, ST>::value, 1)
     ffn_grouped_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_constant__ FgTokenMaps maps,
                        FgParams p) {
+  pdl_wait();
   const CUtensorMap* map_x = maps.m;
   using S = FgShape<BT, ST>;
   constexpr uint32_t kXArrivals = GATHER ? 32u : 1u;   // token-side arrivals per stage fill

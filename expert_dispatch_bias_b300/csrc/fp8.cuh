@@ -75,6 +75,7 @@ __device__ __forceinline__ float quant_row_warp(const T* src, int cols, uint8_t*
 template <typename T>
 __global__ void __launch_bounds__(256) quant_rows_kernel(const T* src, int64_t rows, int cols, uint8_t* codes,
                                                          float* scales) {
+  pdl_wait();
   const int64_t warps = (int64_t)gridDim.x * (blockDim.x >> 5);
   for (int64_t r = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); r < rows; r += warps) {
     uint8_t* dst = codes + r * cols;
@@ -88,6 +89,7 @@ __global__ void __launch_bounds__(256) quant_rows_kernel(const T* src, int64_t r
 template <typename T>
 __global__ void __launch_bounds__(256) quant_permute_kernel(const T* x, const int32_t* slot, int64_t T_, int K,
                                                             int h, uint8_t* xq, float* sx) {
+  pdl_wait();
   const int64_t warps = (int64_t)gridDim.x * (blockDim.x >> 5);
   const int lane = threadIdx.x & 31;
   for (int64_t t = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); t < T_; t += warps) {

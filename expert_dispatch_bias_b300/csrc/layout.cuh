@@ -120,6 +120,7 @@ struct LayoutParams {
 };
 
 __global__ void __launch_bounds__(kLayoutThreads) layout_rank_kernel(LayoutParams p) {
+  pdl_wait();
   extern __shared__ int32_t sm[];
   int32_t* cnt = sm;                          // [kLayoutWarps][E] per-warp counts, then warp prefixes
   int32_t* tile_agg = sm + kLayoutWarps * p.E;  // [E]
@@ -247,6 +248,7 @@ __global__ void __launch_bounds__(kLayoutThreads) layout_rank_kernel(LayoutParam
 }
 
 __global__ void __launch_bounds__(kFinalizeThreads) layout_finalize_kernel(LayoutParams p) {
+  pdl_wait();
   extern __shared__ int32_t off[];  // [E + 1]
   __shared__ int32_t scratch[33];
   __shared__ bool s_last;
@@ -378,6 +380,7 @@ __host__ __device__ inline size_t layout_small_smem(int E, int n_ep) {
 }
 
 __global__ void __launch_bounds__(kLayoutSmallThreads) layout_small_kernel(LayoutParams p) {
+  pdl_wait();
   extern __shared__ int32_t sm[];
   const int E = p.E, N = p.n_ep;
   int32_t* cnt = sm;                 // [32][E]: per-warp counts, then prefixes over warps
@@ -534,6 +537,7 @@ __global__ void __launch_bounds__(kLayoutSmallThreads) layout_small_kernel(Layou
 // [0, E) or a plan entry outside [0, P) raises the bad-index error and writes -1.
 __global__ void eplb_map_kernel(const int32_t* ids, int64_t A, int K, int E, int P, const int32_t* rep_offsets,
                                 const int32_t* rep_phys, int32_t* out) {
+  pdl_wait();
   for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < A; i += (int64_t)gridDim.x * blockDim.x) {
     const int e = ids[i];
     int32_t v = -1;

@@ -11,6 +11,7 @@
 
 #include <algorithm>
 #include <atomic>
+#include <utility>
 #include <vector>
 
 #include <cudaTypedefs.h>
@@ -46,6 +47,28 @@ std::atomic<uint64_t> g_launches{0};
 inline cudaError_t launched() {
   g_launches.fetch_add(1, std::memory_order_relaxed);
   return cudaGetLastError();
+}
+
+// Launches a kernel of the library on st with programmatic stream
+// serialisation: it is scheduled as soon as the stream's previous kernel has
+// no CTA left, which hides the launch latency between the kernels of a step
+// (Switch-Base step 0.386 -> 0.368 ms, decode T=32 1.791 -> 1.775 ms on B300).
+// Every kernel waits for the previous one (pdl_wait, griddepcontrol.wait)
+// before its first global memory access, so memory sees plain stream order.
+// An error is also left for cudaGetLastError, which launched() reads.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_k(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st, Args&&... args) {
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
 }
 
 #define CUDA_TRY(expr)                               \
@@ -257,9 +280,9 @@ moe_status launch_logits_simt(const moe_config& c, const void* x, const void* w_
   p.col_bias = off;
   dim3 grid((c.E + kSimtBN - 1) / kSimtBN, (c.T + kSimtBM - 1) / kSimtBM);
   if (c.dtype == MOE_F32)
-    simt_gemm_kernel<float, kSimtLogits><<<grid, kSimtThreads, 0, st>>>(p);
+    (void)launch_k(simt_gemm_kernel<float, kSimtLogits>, grid, kSimtThreads, 0, st, p);
   else
-    simt_gemm_kernel<__nv_bfloat16, kSimtLogits><<<grid, kSimtThreads, 0, st>>>(p);
+    (void)launch_k(simt_gemm_kernel<__nv_bfloat16, kSimtLogits>, grid, kSimtThreads, 0, st, p);
   CUDA_TRY(launched());
   return MOE_OK;
 }
@@ -268,7 +291,7 @@ template <int PER>
 cudaError_t launch_route_per(const RouteParams& p, cudaStream_t st) {
   const int blocks = (p.T + kRouteWarps - 1) / kRouteWarps;
   const size_t smem = p.n_groups > 0 ? (size_t)kRouteWarps * p.E * sizeof(float) : 0;
-  route_kernel<PER><<<blocks, kRouteWarps * 32, smem, st>>>(p);
+  (void)launch_k(route_kernel<PER>, blocks, kRouteWarps * 32, smem, st, p);
   return launched();
 }
 
@@ -330,17 +353,17 @@ moe_status launch_layout(const moe_config& c, const int32_t* ids, int32_t* count
   if (p.A <= kLayoutSmallMax) {  // one block, one launch
     const size_t smem = layout_small_smem(p.E, p.n_ep);
     CUDA_TRY(allow_smem(layout_small_kernel, smem));
-    layout_small_kernel<<<1, kLayoutSmallThreads, smem, st>>>(p);
+    (void)launch_k(layout_small_kernel, 1, kLayoutSmallThreads, smem, st, p);
     CUDA_TRY(launched());
     return MOE_OK;
   }
   const size_t smem1 = (size_t)(kLayoutWarps + 2) * nphys(c) * sizeof(int32_t);
   CUDA_TRY(allow_smem(layout_rank_kernel, smem1));
-  layout_rank_kernel<<<p.num_tiles, kLayoutThreads, smem1, st>>>(p);
+  (void)launch_k(layout_rank_kernel, p.num_tiles, kLayoutThreads, smem1, st, p);
   CUDA_TRY(launched());
   const int64_t per_block = kFinalizeThreads * kFinalizeItems;
   const int blocks2 = (int)((p.A + per_block - 1) / per_block) > 0 ? (int)((p.A + per_block - 1) / per_block) : 1;
-  layout_finalize_kernel<<<blocks2, kFinalizeThreads, (nphys(c) + 1) * sizeof(int32_t), st>>>(p);
+  (void)launch_k(layout_finalize_kernel, blocks2, kFinalizeThreads, (nphys(c) + 1) * sizeof(int32_t), st, p);
   CUDA_TRY(launched());
   return MOE_OK;
 }
@@ -358,7 +381,7 @@ moe_status launch_permute(const moe_config& c, const void* x, const int32_t* slo
     const int64_t n = R * vecs;
     const int blocks = (int)((n + 255) / 256 < 148 * 8 ? (n + 255) / 256 : 148 * 8);
     if (n > 0) {
-      zero_pad_rows_kernel<<<blocks, 256, 0, st>>>(row_src, R, vecs, static_cast<uint4*>(xp));
+      (void)launch_k(zero_pad_rows_kernel, blocks, 256, 0, st, row_src, R, vecs, static_cast<uint4*>(xp));
       CUDA_TRY(launched());
     }
   }
@@ -373,7 +396,7 @@ moe_status launch_permute(const moe_config& c, const void* x, const int32_t* slo
     if (per_sm < 1) per_sm = 1;
     int64_t blocks = (int64_t)device_info().sms * per_sm;
     if (blocks > (units + 7) / 8) blocks = (units + 7) / 8;
-    kern<<<(unsigned)blocks, 256, 0, st>>>(static_cast<const uint4*>(x), slot, c.T, c.K, row_vecs,
+    (void)launch_k(kern, (unsigned)blocks, 256, 0, st, static_cast<const uint4*>(x), slot, c.T, c.K, row_vecs,
                                            static_cast<uint4*>(xp));
     CUDA_TRY(launched());
     return MOE_OK;
@@ -394,7 +417,7 @@ moe_status launch_permute(const moe_config& c, const void* x, const int32_t* slo
   if (per_sm < 1) per_sm = 1;
   int64_t blocks = (int64_t)device_info().sms * per_sm;
   if (blocks > c.T) blocks = c.T;
-  permute_bulk_kernel<<<(unsigned)blocks, 32, smem, st>>>(p);
+  (void)launch_k(permute_bulk_kernel, (unsigned)blocks, 32, smem, st, p);
   CUDA_TRY(launched());
   return MOE_OK;
 }
@@ -425,7 +448,7 @@ moe_status launch_combine(const moe_config& c, const void* yp, const int32_t* sl
   if (per_sm < 1) per_sm = 1;
   int64_t blocks = (int64_t)device_info().sms * per_sm;
   if (blocks > (units + 7) / 8) blocks = (units + 7) / 8;
-  kern<<<(unsigned)blocks, 256, 0, st>>>(p);
+  (void)launch_k(kern, (unsigned)blocks, 256, 0, st, p);
   CUDA_TRY(launched());
   return MOE_OK;
 }
@@ -452,7 +475,7 @@ cudaError_t launch_ffn_simt(const moe_config& c, const void* xp, const int32_t* 
   p.n_w = w_map != nullptr ? c.E : nphys(c);
   p.N = c.I;
   p.K = c.h;
-  simt_gemm_kernel<T, kSimtSwiglu><<<dim3((c.I + kSimtBN - 1) / kSimtBN, mblocks), kSimtThreads, 0, st>>>(p);
+  (void)launch_k(simt_gemm_kernel<T, kSimtSwiglu>, dim3((c.I + kSimtBN - 1) / kSimtBN, mblocks), kSimtThreads, 0, st, p);
   cudaError_t e = launched();
   if (e != cudaSuccess) return e;
   SimtParams q = p;
@@ -466,7 +489,7 @@ cudaError_t launch_ffn_simt(const moe_config& c, const void* xp, const int32_t* 
   q.ldc = c.h;
   q.N = c.h;
   q.K = c.I;
-  simt_gemm_kernel<T, kSimtPlain><<<dim3((c.h + kSimtBN - 1) / kSimtBN, mblocks), kSimtThreads, 0, st>>>(q);
+  (void)launch_k(simt_gemm_kernel<T, kSimtPlain>, dim3((c.h + kSimtBN - 1) / kSimtBN, mblocks), kSimtThreads, 0, st, q);
   return launched();
 }
 
@@ -548,9 +571,9 @@ moe_status launch_ffn_tokens_m_one(const moe_config& c, const void* xp, const in
   auto k2 = tc_gemm_kernel<kTcStore, kFfnBN, kFfnStages>;
   CUDA_TRY(allow_smem(k1, S::kDynSmem));
   CUDA_TRY(allow_smem(k2, S::kDynSmem));
-  k1<<<grid, kTcThreads, S::kDynSmem, st>>>(a1, b1, p1);
+  (void)launch_k(k1, grid, kTcThreads, S::kDynSmem, st, a1, b1, p1);
   CUDA_TRY(launched());
-  k2<<<grid, kTcThreads, S::kDynSmem, st>>>(a2, b2, p2);
+  (void)launch_k(k2, grid, kTcThreads, S::kDynSmem, st, a2, b2, p2);
   CUDA_TRY(launched());
   return MOE_OK;
 }
@@ -638,9 +661,9 @@ moe_status launch_ffn_grouped(const moe_config& c, const void* xp, const int32_t
                             : ffn_grouped_kernel<kTcStore, BT, ST>;
   CUDA_TRY(allow_smem(k1, S::kDynSmem));
   CUDA_TRY(allow_smem(k2, S::kDynSmem));
-  k1<<<grid, gather ? FgThreads<true, ST>::value : kFgThreads, S::kDynSmem, st>>>(w1m, x1, p1);
+  (void)launch_k(k1, grid, gather ? FgThreads<true, ST>::value : kFgThreads, S::kDynSmem, st, w1m, x1, p1);
   CUDA_TRY(launched());
-  k2<<<grid, kFgThreads, S::kDynSmem, st>>>(w2m, x2, p2);
+  (void)launch_k(k2, grid, kFgThreads, S::kDynSmem, st, w2m, x2, p2);
   CUDA_TRY(launched());
   return MOE_OK;
 }
@@ -693,14 +716,14 @@ moe_status launch_logits_tc_bn(const moe_config& c, const void* x, const void* w
   const int grid = (int)(items < sms ? items : sms);
   auto k = tc_gemm_kernel<kTcLogits, BN, STAGES>;
   CUDA_TRY(allow_smem(k, S::kDynSmem));
-  k<<<grid, kTcThreads, S::kDynSmem, st>>>(a, b, p);
+  (void)launch_k(k, grid, kTcThreads, S::kDynSmem, st, a, b, p);
   CUDA_TRY(launched());
   if (k_split > 1) {
     const int64_t n = (int64_t)c.T * c.E;
     const int64_t lanes = (c.E % 4 == 0) ? n / 4 : n;
     int64_t blocks = (lanes + 255) / 256;
     if (blocks > (int64_t)sms * 8) blocks = (int64_t)sms * 8;
-    logits_reduce_kernel<<<(unsigned)blocks, 256, 0, st>>>(p.partial, k_split, n, c.E, off, logits);
+    (void)launch_k(logits_reduce_kernel, (unsigned)blocks, 256, 0, st, p.partial, k_split, n, c.E, off, logits);
     CUDA_TRY(launched());
   }
   return MOE_OK;
@@ -812,13 +835,13 @@ moe_status launch_ffn_fp8(const moe_config& c, const uint8_t* xq, const float* s
   auto k2 = ffn_grouped_kernel<kTcStore, kFgTileRows, kFgStages, true>;
   CUDA_TRY(allow_smem(k1, S::kDynSmem));
   CUDA_TRY(allow_smem(k2, S::kDynSmem));
-  k1<<<grid, kFgThreads, S::kDynSmem, st>>>(w1m, x1, p1);
+  (void)launch_k(k1, grid, kFgThreads, S::kDynSmem, st, w1m, x1, p1);
   CUDA_TRY(launched());
   int64_t qb = (R + 7) / 8;
   if (qb > (int64_t)grid * 16) qb = (int64_t)grid * 16;
-  quant_rows_kernel<__nv_bfloat16><<<(unsigned)qb, 256, 0, st>>>(inter, R, c.I, interq, sinter);
+  (void)launch_k(quant_rows_kernel<__nv_bfloat16>, (unsigned)qb, 256, 0, st, inter, R, c.I, interq, sinter);
   CUDA_TRY(launched());
-  k2<<<grid, kFgThreads, S::kDynSmem, st>>>(w2m, x2, p2);
+  (void)launch_k(k2, grid, kFgThreads, S::kDynSmem, st, w2m, x2, p2);
   CUDA_TRY(launched());
   return MOE_OK;
 }
@@ -828,7 +851,7 @@ moe_status launch_permute_fp8(const moe_config& c, const void* x, const int32_t*
   if (c.T == 0) return MOE_OK;
   int64_t blocks = (c.T + 7) / 8;
   if (blocks > (int64_t)device_info().sms * 16) blocks = (int64_t)device_info().sms * 16;
-  quant_permute_kernel<__nv_bfloat16><<<(unsigned)blocks, 256, 0, st>>>(static_cast<const __nv_bfloat16*>(x), slot,
+  (void)launch_k(quant_permute_kernel<__nv_bfloat16>, (unsigned)blocks, 256, 0, st, static_cast<const __nv_bfloat16*>(x), slot,
                                                                        c.T, c.K, c.h, xq, sx);
   CUDA_TRY(launched());
   return MOE_OK;
@@ -883,7 +906,7 @@ moe_status launch_shared_ffn(const moe_config& c, const void* x, const void* w13
     p.N = Is;
     p.K = c.h;
     const unsigned mblocks = (unsigned)((c.T + kSimtBM - 1) / kSimtBM);
-    simt_gemm_kernel<float, kSimtSwiglu><<<dim3((Is + kSimtBN - 1) / kSimtBN, mblocks), kSimtThreads, 0, st>>>(p);
+    (void)launch_k(simt_gemm_kernel<float, kSimtSwiglu>, dim3((Is + kSimtBN - 1) / kSimtBN, mblocks), kSimtThreads, 0, st, p);
     CUDA_TRY(launched());
     SimtParams q = p;
     q.A = inter;
@@ -896,7 +919,7 @@ moe_status launch_shared_ffn(const moe_config& c, const void* x, const void* w13
     q.ldc = c.h;
     q.N = c.h;
     q.K = Is;
-    simt_gemm_kernel<float, kSimtPlain><<<dim3((c.h + kSimtBN - 1) / kSimtBN, mblocks), kSimtThreads, 0, st>>>(q);
+    (void)launch_k(simt_gemm_kernel<float, kSimtPlain>, dim3((c.h + kSimtBN - 1) / kSimtBN, mblocks), kSimtThreads, 0, st, q);
     CUDA_TRY(launched());
     return MOE_OK;
   }
@@ -933,9 +956,9 @@ moe_status launch_shared_ffn(const moe_config& c, const void* x, const void* w13
   auto k2 = tc_gemm_kernel<kTcStore, kFfnBN, kFfnStages>;
   CUDA_TRY(allow_smem(k1, S::kDynSmem));
   CUDA_TRY(allow_smem(k2, S::kDynSmem));
-  k1<<<g1, kTcThreads, S::kDynSmem, st>>>(a1, b1, p1);
+  (void)launch_k(k1, g1, kTcThreads, S::kDynSmem, st, a1, b1, p1);
   CUDA_TRY(launched());
-  k2<<<g2, kTcThreads, S::kDynSmem, st>>>(a2, b2, p2);
+  (void)launch_k(k2, g2, kTcThreads, S::kDynSmem, st, a2, b2, p2);
   CUDA_TRY(launched());
   return MOE_OK;
 }
@@ -961,7 +984,7 @@ moe_status launch_eplb_map(const moe_config& c, const int32_t* ids, const EplbDe
   if (A == 0) return MOE_OK;
   int64_t blocks = (A + 255) / 256;
   if (blocks > (int64_t)device_info().sms * 8) blocks = (int64_t)device_info().sms * 8;
-  eplb_map_kernel<<<(unsigned)blocks, 256, 0, st>>>(ids, A, c.K, c.E, nphys(c), plan.rep_offsets, plan.rep_phys,
+  (void)launch_k(eplb_map_kernel, (unsigned)blocks, 256, 0, st, ids, A, c.K, c.E, nphys(c), plan.rep_offsets, plan.rep_phys,
                                                       phys);
   CUDA_TRY(launched());
   return MOE_OK;
@@ -1490,10 +1513,10 @@ moe_status moe_quantize_fp8(int64_t rows, int32_t cols, int32_t dtype, const voi
   int64_t blocks = (rows + 7) / 8;
   if (blocks > (int64_t)device_info().sms * 16) blocks = (int64_t)device_info().sms * 16;
   if (dtype == MOE_BF16)
-    quant_rows_kernel<__nv_bfloat16><<<(unsigned)blocks, 256, 0, as_stream(stream)>>>(
+    (void)launch_k(quant_rows_kernel<__nv_bfloat16>, (unsigned)blocks, 256, 0, as_stream(stream), 
         static_cast<const __nv_bfloat16*>(src), rows, cols, codes, scales);
   else
-    quant_rows_kernel<float><<<(unsigned)blocks, 256, 0, as_stream(stream)>>>(static_cast<const float*>(src), rows,
+    (void)launch_k(quant_rows_kernel<float>, (unsigned)blocks, 256, 0, as_stream(stream), static_cast<const float*>(src), rows,
                                                                               cols, codes, scales);
   CUDA_TRY(launched());
   return MOE_OK;

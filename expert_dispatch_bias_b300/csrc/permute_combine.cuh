@@ -35,6 +35,7 @@ struct PermuteParams {
 };
 
 __global__ void __launch_bounds__(32) permute_bulk_kernel(PermuteParams p) {
+  pdl_wait();
   extern __shared__ __align__(128) uint8_t sbuf[];  // [nbuf][row_bytes]
   __shared__ __align__(8) uint64_t bar[kPermBufs];
   if (threadIdx.x != 0) return;
@@ -99,6 +100,7 @@ constexpr int kPermChunk = 128;  // 16-byte vectors per work unit (4 per lane)
 template <int KMAX>
 __global__ void __launch_bounds__(256) permute_warp_kernel(const uint4* x, const int32_t* slot, int64_t T, int K,
                                                            int row_vecs, uint4* xp) {
+  pdl_wait();
   const int lane = threadIdx.x & 31;
   const int64_t warps = (int64_t)gridDim.x * (blockDim.x >> 5);
   const int chunks = (row_vecs + kPermChunk - 1) / kPermChunk;
@@ -128,6 +130,7 @@ __global__ void __launch_bounds__(256) permute_warp_kernel(const uint4* x, const
 
 // Zero the pad rows (row_src == -1) of a padded permuted buffer.
 __global__ void zero_pad_rows_kernel(const int32_t* row_src, int64_t R, uint32_t row_vecs, uint4* xp) {
+  pdl_wait();
   const int64_t stride = (int64_t)gridDim.x * blockDim.x;
   const int64_t n = R * row_vecs;
   for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += stride) {
@@ -187,6 +190,7 @@ constexpr int kCombineChunk = 128;  // 16-byte vectors per work unit (4 per lane
 
 template <typename T, int KMAX>
 __global__ void __launch_bounds__(256) combine_kernel(CombineParams p) {
+  pdl_wait();
   constexpr int V = Vec<T>::N;
   const int lane = threadIdx.x & 31;
   const int64_t warps = (int64_t)gridDim.x * (blockDim.x >> 5);

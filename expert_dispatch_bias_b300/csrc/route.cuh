@@ -416,6 +416,7 @@ __device__ __forceinline__ void route_token(const RouteParams& p, int t, float* 
 // PER = experts held by each lane (contiguous: lane l holds l*PER .. l*PER+PER-1).
 template <int PER>
 __global__ void __launch_bounds__(kRouteWarps * 32, PER <= 8 ? 4 : 1) route_kernel(RouteParams p) {
+  pdl_wait();
   extern __shared__ float s_keys[];  // [kRouteWarps][E], used with a group limit
   __shared__ int32_t s_eid[kRouteWarps][kRefineMax];  // experts being refined
   __shared__ float s_eval[kRouteWarps][kRefineMax];   // their exact keys

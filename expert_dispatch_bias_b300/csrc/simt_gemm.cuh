@@ -84,6 +84,7 @@ __device__ __forceinline__ bool segment_of_block(const int32_t* offsets, const i
 
 template <typename T, int MODE>
 __global__ void __launch_bounds__(kSimtThreads) simt_gemm_kernel(SimtParams p) {
+  pdl_wait();
   constexpr int NB = MODE == kSimtSwiglu ? 2 * kSimtBN : kSimtBN;  // B rows per tile
   __shared__ __align__(16) float As[kSimtBK][kSimtBM];
   __shared__ __align__(16) float Bs[kSimtBK][NB];

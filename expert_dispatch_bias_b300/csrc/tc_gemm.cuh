@@ -246,6 +246,7 @@ __device__ __forceinline__ TcTile tc_decode(int t, const int32_t* mbp, const TcP
 template <int EPI, int BN, int STAGES>
 __global__ void __launch_bounds__(kTcThreads, 1)
     tc_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_b, TcParams p) {
+  pdl_wait();
   using S = TcShape<BN, STAGES>;
   constexpr int CH = S::kChunk;
   extern __shared__ uint8_t dyn_smem[];
@@ -498,6 +499,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 // float4 lanes when E % 4 == 0 (every partial starts 256-byte aligned).
 __global__ void __launch_bounds__(256) logits_reduce_kernel(const float* P, int k_split, int64_t n, int E,
                                                             const float* off, float* out) {
+  pdl_wait();
   const int64_t stride = (int64_t)gridDim.x * blockDim.x;
   if ((E & 3) == 0) {
     const int64_t n4 = n >> 2;
