@@ -326,27 +326,38 @@ class Layer:
     def timed(self, steps, warmup, world=1, clocks_csv=None):
         """W untimed steps, then exactly `steps` steps between a barrier and a
         synchronize on both sides, one library call each, timed by one event
-        before the first and one after the last (events between the kernels
-        would stop a kernel from starting while its predecessor finishes).
-        Then the same number of steps again, each recording its stage events,
-        for the per-stage means.  Returns (total ms, per-stage mean ms,
-        clocks, launches)."""
+        before the first and one after the last; inside, each step records only
+        the two events around its grouped FFN (an event between two kernels
+        keeps the second from being scheduled while the first drains, so the
+        other stage boundaries carry none).  Then the same number of steps
+        again, each recording every stage event, for the other stages' means.
+        Returns (total ms, per-stage mean ms, clocks, launches); the FFN's
+        mean is the timed region's own."""
         import torch
         import torch.distributed as dist
 
         moe = self.moe
         n_ev = len(moe.LAYER_STAGES) + 1
+        i_ffn = list(moe.LAYER_STAGES).index("ffn")
         plain = moe.layer_out(**self.out)
         for _ in range(warmup):
             self.call(self.y, plain, self.ws)
         st = moe.moe_check()
         if st != 0:
             raise RuntimeError(f"device error during warm-up: {moe.STATUS[st]}")
-        events = [[torch.cuda.Event(enable_timing=True) for _ in range(n_ev)] for _ in range(steps)]
-        for evs in events:          # torch creates each CUDA event on its first record
-            for e in evs:
+
+        def recorded_events(n):
+            evs = [torch.cuda.Event(enable_timing=True) for _ in range(n)]
+            for e in evs:              # torch creates each CUDA event on its first record
                 e.record(self.stream)
+            return evs
+
+        events = [recorded_events(n_ev) for _ in range(steps)]
         outs = [moe.layer_out(stage_events=evs, **self.out) for evs in events]
+        ffn_events = [recorded_events(2) for _ in range(steps)]
+        outs_ffn = [moe.layer_out(stage_events=[a if j == i_ffn else b if j == i_ffn + 1 else None
+                                                for j in range(n_ev)], **self.out)
+                    for a, b in ffn_events]
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         if world > 1:
             dist.barrier()
@@ -354,8 +365,8 @@ class Layer:
         launches0 = moe.moe_launch_count()   # the library counts every kernel it launches
         with ClockSampler(torch.cuda.current_device(), csv_path=clocks_csv) as clk:
             e0.record(self.stream)
-            for _ in range(steps):
-                self.call(self.y, plain, self.ws)
+            for o in outs_ffn:
+                self.call(self.y, o, self.ws)
             e1.record(self.stream)
             torch.cuda.synchronize()
         launches = moe.moe_launch_count() - launches0
@@ -365,6 +376,7 @@ class Layer:
         if st != 0:
             raise RuntimeError(f"device error in the timed region: {moe.STATUS[st]}")
         total = e0.elapsed_time(e1)
+        ffn_ms = statistics.mean(a.elapsed_time(b) for a, b in ffn_events)
         for o in outs:
             self.call(self.y, o, self.ws)
         torch.cuda.synchronize()
@@ -373,6 +385,7 @@ class Layer:
             raise RuntimeError(f"device error in the stage-timed steps: {moe.STATUS[st]}")
         stages = {s: statistics.mean(events[i][j].elapsed_time(events[i][j + 1]) for i in range(steps))
                   for j, s in enumerate(moe.LAYER_STAGES)}
+        stages["ffn"] = ffn_ms
         return total, stages, clk.summary(), launches
 
     def e2e(self, steps, warmup, world=1):

@@ -358,16 +358,17 @@ def moe_launch_count() -> int:
 
 def layer_out(stage_events=None, **tensors) -> MoeLayerOut:
     """Optional outputs of the layer calls.  ``stage_events``: MOE_LAYER_STAGES + 1
-    torch.cuda.Event objects, each already recorded once (torch creates the
-    CUDA event on its first record); the layer records them around its stages."""
+    torch.cuda.Event objects or None, each event already recorded once (torch
+    creates the CUDA event on its first record); the layer records them around
+    its stages and skips the None entries."""
     o = MoeLayerOut()
     for k, v in tensors.items():
         setattr(o, k, _ptr(v))
     if stage_events is not None:
         if len(stage_events) != len(LAYER_STAGES) + 1:
             raise ValueError(f"stage_events needs {len(LAYER_STAGES) + 1} events")
-        handles = [e.cuda_event for e in stage_events]
-        if not all(handles):
+        handles = [None if e is None else e.cuda_event for e in stage_events]
+        if not all(h for h, e in zip(handles, stage_events) if e is not None):
             raise ValueError("record every stage event once before passing it (torch creates it lazily)")
         o._events = (c_void_p * len(handles))(*handles)   # kept alive with the struct
         o.stage_events = ctypes.cast(o._events, c_void_p)

@@ -1010,7 +1010,7 @@ moe_status layer_core(const moe_config& c, const void* x, const void* w_r, const
   // caller's stage events: [0] before the first stage, [s + 1] after stage s
   cudaEvent_t const* ev = reinterpret_cast<cudaEvent_t const*>(o.stage_events);
   auto mark = [&](int i) -> moe_status {
-    if (ev != nullptr) CUDA_TRY(cudaEventRecord(ev[i], st));
+    if (ev != nullptr && ev[i] != nullptr) CUDA_TRY(cudaEventRecord(ev[i], st));
     return MOE_OK;
   };
   MOE_TRY(mark(0));

@@ -132,6 +132,9 @@ enum moe_layer_stage {
  * stream before its first kernel and stage_events[s + 1] after stage s
  * (moe_layer_stage), so cudaEventElapsedTime(stage_events[s],
  * stage_events[s + 1]) is the device time of stage s inside the one call.
+ * An entry may be NULL: that event is not recorded (an event between two
+ * kernels keeps the second from being scheduled while the first drains, so a
+ * caller timing one stage passes only that stage's two events).
  * Ignored by the host-buffer calls. */
 typedef struct moe_layer_out {
   float* logits;            /* [T, E] */
