@@ -17,9 +17,14 @@ def _recorded(n):
     return evs
 
 
-@pytest.mark.parametrize("name", ["dsv3_small", "switch_small"])
-def test_stage_events_all_and_partial(name):
-    w = workloads.ALL[name]
+SMALL = [
+    workloads.DSV3.replace(name="dsv3_small", T=256, h=512, I=256),
+    workloads.SWITCH.replace(name="switch_small", T=2048, h=256, I=256, capacity=16),
+]
+
+
+@pytest.mark.parametrize("w", SMALL, ids=lambda w: w.name)
+def test_stage_events_all_and_partial(w):
     inp = device.layer_inputs(w)
     cfg = moe.config_from(w)
     ws = moe.alloc_workspace(cfg, moe.MOE_OP_LAYER)
