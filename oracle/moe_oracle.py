@@ -193,8 +193,9 @@ def route(L: np.ndarray, cfg, bias: Optional[np.ndarray] = None):
 # against float64 sums) may route a token differently only where the decision
 # rests on keys that nearly tie.  The margins below measure, per token, how far
 # the decision is from a tie: the relative gap between the two scores the
-# decision compares.  READING (the benchmark spec tolerance rule; [overview] glossary
-# "top-K"): a top-K difference is excused only where such a gap is < 1e-4.
+# decision compares.  READING (the parity rule for routing; [overview]
+# glossary "top-K"): a top-K difference is excused only where such a gap is
+# < 1e-4.
 
 
 def group_margin(keys: np.ndarray, cfg) -> np.ndarray:
