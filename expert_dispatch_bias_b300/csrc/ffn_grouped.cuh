@@ -479,6 +479,33 @@ __global__ void __launch_bounds__(FgThreads<GATHER, ST>::value, 1)
         if (ok && big) ok = mbar_wait(&tmem_empty[1], ((slot_phase >> 1) & 1u) ^ 1u, &abort_flag);
         if (!ok) break;
         tc_fence_after();
+        if (st == 0 && p.k_blocks % ST == 0) {
+          // whole groups of ST k-blocks starting at stage 0 (every tile when
+          // k_blocks is a multiple of ST): unrolled over the stages, so stage
+          // indices, descriptors and the next stage to test are constants and
+          // the thread spends fewer cycles between k-blocks (MMA path alone:
+          // 2.50 -> 2.10 ms at DeepSeek-V3 T=4096)
+          for (int kb = 0; kb < p.k_blocks && ok; kb += ST) {
+#pragma unroll
+            for (int u = 0; u < ST; ++u) {
+              if (!ready && !mbar_wait(&full[u], ph, &abort_flag)) {
+                ok = false;
+                break;
+              }
+              tc_fence_after();
+              const uint64_t dw0 = dwb + (uint64_t)(u * (S::kWStage >> 4));
+              const uint64_t dw1 = dw0 + (S::kWBytes >> 4);
+              const uint64_t dx = dxb + (uint64_t)(u * (S::kXStage >> 4));
+              fg_mma_step<FP8>(c0, c1, dw0, dw1, dx, idesc, (kb + u) != 0 ? 1u : 0u, 0);
+              fg_mma_step<FP8>(c0, c1, dw0, dw1, dx, idesc, 1u, 1);
+              ready = mbar_try_wait(&full[(u + 1) % ST], u + 1 == ST ? ph ^ 1u : ph);
+              fg_mma_step<FP8>(c0, c1, dw0, dw1, dx, idesc, 1u, 2);
+              fg_mma_step<FP8>(c0, c1, dw0, dw1, dx, idesc, 1u, 3);
+              umma_commit(&empty[u]);
+            }
+            ph ^= 1u;
+          }
+        } else
         for (int kb = 0; kb < p.k_blocks; ++kb) {
           if (!ready && !mbar_wait(&full[st], ph, &abort_flag)) {
             ok = false;

@@ -362,6 +362,33 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         bool ok = true;
         int kb0, kb1;
         tc_k_range(t % KS, KS, p.k_blocks, &kb0, &kb1);
+        if (stage == 0 && (kb1 - kb0) % STAGES == 0) {
+          // whole groups of STAGES k-blocks starting at stage 0: unrolled over
+          // the stages, so stage indices, descriptors and the next stage to
+          // test are constants and the thread spends fewer cycles between
+          // k-blocks
+          for (int kb = kb0; kb < kb1 && ok; kb += STAGES) {
+#pragma unroll
+            for (int u = 0; u < STAGES; ++u) {
+              if (!ready && !mbar_wait(&full_bar[u], phase, &abort_flag)) {
+                abort_flag = 1;
+                raise_error(kErrTimeout);
+                ok = false;
+                break;
+              }
+              tc_fence_after();
+              const uint64_t da = d0 + (uint64_t)(u * (S::kStageBytes >> 4));
+              const uint64_t db = da + (S::kABytes >> 4);
+              umma_bf16(d_tmem, da, db, idesc, (kb + u) != kb0 ? 1u : 0u);
+              umma_bf16(d_tmem, da + 2, db + 2, idesc, 1u);
+              ready = mbar_try_wait(&full_bar[(u + 1) % STAGES], u + 1 == STAGES ? phase ^ 1u : phase);
+              umma_bf16(d_tmem, da + 4, db + 4, idesc, 1u);
+              umma_bf16(d_tmem, da + 6, db + 6, idesc, 1u);
+              umma_commit(&empty_bar[u]);
+            }
+            phase ^= 1u;
+          }
+        } else
         for (int kb = kb0; kb < kb1; ++kb) {
           if (!ready && !mbar_wait(&full_bar[stage], phase, &abort_flag)) {
             abort_flag = 1;
