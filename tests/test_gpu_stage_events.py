@@ -48,7 +48,7 @@ def test_stage_events_all_and_partial(w):
     stage_ms = [evs[j].elapsed_time(evs[j + 1]) for j in range(n_ev - 1)]
     assert all(t >= 0.0 for t in stage_ms)
     assert stage_ms[i_ffn] > 0.0
-    assert sum(stage_ms) == pytest.approx(evs[0].elapsed_time(evs[-1]), rel=1e-3, abs=1e-3)
+    assert sum(stage_ms) == pytest.approx(evs[0].elapsed_time(evs[-1]), rel=1e-3, abs=1e-2)  # event resolution ~0.5 us each
 
     # only the FFN's two events (NULL elsewhere): recorded around the FFN alone
     a, b = _recorded(2)
