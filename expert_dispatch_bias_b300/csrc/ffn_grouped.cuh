@@ -43,9 +43,10 @@
 // thread waits once and commits once per k-block.  That thread is the MMA
 // pipe's only feeder, and with N <= 160 a k-block's eight MMAs take about 500
 // cycles: every cycle it spends elsewhere leaves the pipe idle.  So it tests
-// the next stage's barrier while the current MMAs run and keeps the
-// descriptors as base + stage offsets (the launcher's choice of tile and ring
-// and the measurements behind it are beside kFgTileRows).
+// the next stage's barrier while the current MMAs run, keeps the descriptors
+// as base + stage offsets, and unrolls its loop over the ring when a tile's
+// k-blocks fill whole rounds of it (the launcher's choice of tile and ring and
+// the measurements behind it are beside kFgTileRows).
 // Rows past a tile's end are computed and masked on store.  Every wait is
 // bounded; a wait that runs out raises the sticky error, and the CTA drains its
 // copies and MMAs, frees TMEM and exits.
