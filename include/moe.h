@@ -27,6 +27,10 @@
  *    The library never allocates or frees memory.
  *  - Every call is asynchronous on `stream` (a cudaStream_t; NULL = legacy
  *    default stream) and does not synchronise the host, except moe_check.
+ *    Kernels are launched with programmatic stream serialisation: a kernel
+ *    may be scheduled while the stream's previous kernel finishes, but it
+ *    waits for that kernel's completion before touching memory, so results
+ *    follow plain stream order (also under stream capture).
  *  - Arguments are validated on the host before any launch; a bad argument
  *    returns an error status and launches nothing.  There is no CPU fallback.
  *  - Row-major layouts, the last index contiguous.  "dtype" tensors hold
