@@ -56,6 +56,10 @@ SMALL = [
     _small("bf16_many_experts", T=200, h=256, E=64, K=4, I=128, dtype="bf16", score="softmax"),
     _small("bf16_pad", T=250, h=256, E=16, K=2, I=256, dtype="bf16", score="softmax", capacity=40, pad=1),
     _small("bf16_empty_experts", T=40, h=768, E=32, K=1, I=256, dtype="bf16", score="softmax"),
+    # widths that are multiples of 64 only: the last feature tile reaches past I
+    # (or h) and the k-blocks (5) do not fill whole rounds of the 4-stage ring
+    _small("bf16_odd_widths", T=300, h=320, E=8, K=2, I=320, dtype="bf16", score="softmax"),
+    _small("bf16_odd_widths_tokens_as_m", T=2048, h=320, E=4, K=2, I=448, dtype="bf16", score="softmax"),
 ]
 
 
